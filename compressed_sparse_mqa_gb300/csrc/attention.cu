@@ -1,0 +1,509 @@
+// attention.cu -- multi-query attention over the raw window and the compressed
+// rows, as one softmax ("DS4 (DwarfStar 4)", Architecture: 64 heads, 1 KV head,
+// 128-token sliding window; Key Techniques, "KV attention compression").
+//
+// For each head h: o_h = sum_j softmax_j(scale * q_h . K_j) V_j over the union of
+// the window rows and the selected (or all visible) compressed rows.
+//
+// Tile engine (shared by decode and prefill).  A CTA of 4 warps walks a list of
+// "virtual rows" (window rows first, then compressed rows through `sel`) in
+// tiles of 64.  Each tile's K and V rows are gathered with 16-byte cp.async into
+// a double-buffered, XOR-swizzled shared-memory tile.  Warp w owns heads
+// 16w .. 16w+15 (the 64 heads of one query are the M dimension: they all share
+// each K/V row, 64 flop per byte), computes S = Q K^T and O += P V with
+// mma.sync m16n8k16 (fp16 in, fp32 accumulate), and keeps an online softmax in
+// the log2 domain.  Rows that are padding (negative sel entries, or past the
+// list) get -inf logits and zero-filled K/V.
+//
+// Decode: one query, rows split across one thread-block cluster of 16 CTAs (8
+// if 16 cannot be scheduled); each CTA leaves (m, l, O) for its rows in shared
+// memory, the cluster barrier publishes them, and CTA c merges heads
+// c*H/16 .. by log-sum-exp, reading the partials through distributed shared
+// memory.  No workspace, no second launch, no spin.
+// Prefill: one CTA per query walks the query's whole row list.
+#include <cooperative_groups.h>
+
+#include "ds4a_common.cuh"
+#include "ds4a_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace ds4a {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kBN = 64;           // rows per tile
+constexpr int kMaxHeads = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Where the virtual rows live: v < n_w -> window row wk/wv + v*D; otherwise the
+// compressed row j = sel ? sel[v - n_w] : v - n_w (j < 0: padding; j >= n_comp:
+// recorded as an index error and treated as padding).
+struct RowSrc {
+    const uint16_t *wk;
+    const uint16_t *wv;
+    const uint16_t *ck;
+    const uint16_t *cv;
+    const int32_t *sel;
+    unsigned int *err;
+    long long n_comp;
+    int n_w;
+};
+
+template <int D>
+struct Smem {
+    uint16_t k[2][kBN * D];
+    uint16_t v[2][kBN * D];
+    long long off[2][kBN];   // element offset of the row in the window (>=0, tagged) / comp arrays; -1 = padding
+};
+
+// Row offset encoding: bit 62 set -> window row.
+constexpr long long kWinTag = 1LL << 62;
+
+// byte offset of 16-byte chunk `ch` of row `r` in a swizzled tile
+template <int D>
+DS4A_DEVINL uint32_t swz(int r, int ch) {
+    return static_cast<uint32_t>(r * (D * 2) + ((ch ^ (r & 7)) << 4));
+}
+
+template <int D>
+DS4A_DEVINL void build_table(const RowSrc &s, int v0, int v_end, long long *off) {
+    const int t = threadIdx.x;
+    if (t < kBN) {
+        const int v = v0 + t;
+        long long o = -1;
+        if (v < v_end) {
+            if (v < s.n_w) {
+                o = kWinTag | (static_cast<long long>(v) * D);
+            } else {
+                const long long j = s.sel ? static_cast<long long>(__ldg(s.sel + (v - s.n_w)))
+                                          : static_cast<long long>(v - s.n_w);
+                if (j >= s.n_comp) record_error(s.err, DS4A_ERR_DEVICE_INDEX);
+                else if (j >= 0) o = j * D;
+            }
+        }
+        off[t] = o;
+    }
+}
+
+template <int D>
+DS4A_DEVINL void issue_loads(const RowSrc &s, const long long *off, uint16_t *kt, uint16_t *vt) {
+    constexpr int kChunks = D / 8;
+    unsigned char *kb = reinterpret_cast<unsigned char *>(kt);
+    unsigned char *vb = reinterpret_cast<unsigned char *>(vt);
+    for (int i = threadIdx.x; i < kBN * kChunks; i += kThreads) {
+        const int r = i / kChunks, ch = i % kChunks;
+        const long long o = off[r];
+        const uint32_t so = swz<D>(r, ch);
+        if (o < 0) {
+            *reinterpret_cast<uint4 *>(kb + so) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(vb + so) = make_uint4(0, 0, 0, 0);
+        } else if (o & kWinTag) {
+            const long long e = (o & ~kWinTag) + ch * 8;
+            cp_async16(kb + so, s.wk + e);
+            cp_async16(vb + so, s.wv + e);
+        } else {
+            const long long e = o + ch * 8;
+            cp_async16(kb + so, s.ck + e);
+            cp_async16(vb + so, s.cv + e);
+        }
+    }
+}
+
+// Per-warp running state: rows g and g+8 of the warp's 16 heads.
+template <int D>
+struct WarpState {
+    float o[D / 8][4];
+    float m[2];
+    float l[2];
+};
+
+template <int D>
+DS4A_DEVINL void load_q_frags(const uint16_t *q, int H, int h0, uint32_t (&qa)[D / 16][4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int ra = h0 + g, rb = h0 + g + 8;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const int c0 = ks * 16 + 2 * t, c1 = c0 + 8;
+        qa[ks][0] = ra < H ? *reinterpret_cast<const uint32_t *>(q + ra * D + c0) : 0u;
+        qa[ks][1] = rb < H ? *reinterpret_cast<const uint32_t *>(q + rb * D + c0) : 0u;
+        qa[ks][2] = ra < H ? *reinterpret_cast<const uint32_t *>(q + ra * D + c1) : 0u;
+        qa[ks][3] = rb < H ? *reinterpret_cast<const uint32_t *>(q + rb * D + c1) : 0u;
+    }
+}
+
+// One tile: S = Q K^T, online softmax, O += P V.
+template <int D>
+DS4A_DEVINL void compute_tile(const uint32_t (&qa)[D / 16][4], const uint16_t *kt, const uint16_t *vt,
+                              const long long *off, float scale_log2, WarpState<D> &st) {
+    const int lane = threadIdx.x & 31, t = lane & 3;
+    const unsigned char *kb = reinterpret_cast<const unsigned char *>(kt);
+    const unsigned char *vb = reinterpret_cast<const unsigned char *>(vt);
+    float s[kBN / 8][4];
+#pragma unroll
+    for (int nt = 0; nt < kBN / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+
+    // S = Q K^T: ldmatrix x4 gives b0/b1 for two key tiles at one k-step
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+        for (int nt = 0; nt < kBN / 8; nt += 2) {
+            const int key = nt * 8 + (lane & 7) + ((lane >> 4) << 3);
+            const int ch = 2 * ks + ((lane >> 3) & 1);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4(b0, b1, b2, b3, kb + swz<D>(key, ch));
+            mma_16816(s[nt], qa[ks], b0, b1);
+            mma_16816(s[nt + 1], qa[ks], b2, b3);
+        }
+    }
+
+    // scale into the log2 domain, mask padding rows, running max
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < kBN / 8; ++nt) {
+        const bool v0 = off[nt * 8 + 2 * t] >= 0, v1 = off[nt * 8 + 2 * t + 1] >= 0;
+        s[nt][0] = v0 ? s[nt][0] * scale_log2 : -INFINITY;
+        s[nt][1] = v1 ? s[nt][1] * scale_log2 : -INFINITY;
+        s[nt][2] = v0 ? s[nt][2] * scale_log2 : -INFINITY;
+        s[nt][3] = v1 ? s[nt][3] * scale_log2 : -INFINITY;
+        mx[0] = fmaxf(mx[0], fmaxf(s[nt][0], s[nt][1]));
+        mx[1] = fmaxf(mx[1], fmaxf(s[nt][2], s[nt][3]));
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+    }
+    float ref[2], alpha[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const float m_new = fmaxf(st.m[r], mx[r]);
+        ref[r] = m_new == -INFINITY ? 0.f : m_new;
+        alpha[r] = exp2f(st.m[r] - ref[r]);
+        st.m[r] = m_new;
+        st.l[r] *= alpha[r];
+    }
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+        st.o[dn][0] *= alpha[0];
+        st.o[dn][1] *= alpha[0];
+        st.o[dn][2] *= alpha[1];
+        st.o[dn][3] *= alpha[1];
+    }
+    uint32_t pa[kBN / 16][4];
+#pragma unroll
+    for (int nt = 0; nt < kBN / 8; ++nt) {
+        const float p0 = exp2f(s[nt][0] - ref[0]), p1 = exp2f(s[nt][1] - ref[0]);
+        const float p2 = exp2f(s[nt][2] - ref[1]), p3 = exp2f(s[nt][3] - ref[1]);
+        st.l[0] += p0 + p1;
+        st.l[1] += p2 + p3;
+        const int kk = nt >> 1, hi = nt & 1;
+        pa[kk][hi ? 2 : 0] = pack_half2(p0, p1);
+        pa[kk][hi ? 3 : 1] = pack_half2(p2, p3);
+    }
+    // O += P V: ldmatrix.trans x4 gives b0/b1 for two d tiles at one key step
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+#pragma unroll
+        for (int dn = 0; dn < D / 8; dn += 2) {
+            const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int ch = dn + (lane >> 4);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(b0, b1, b2, b3, vb + swz<D>(key, ch));
+            mma_16816(st.o[dn], pa[kk], b0, b1);
+            mma_16816(st.o[dn + 1], pa[kk], b2, b3);
+        }
+    }
+}
+
+// Walk virtual rows [v_begin, v_end) of `src`, accumulating into `st`.
+template <int D>
+__device__ void attend_range(const RowSrc &src, int v_begin, int v_end, const uint32_t (&qa)[D / 16][4],
+                             bool has_heads, float scale_log2, Smem<D> &sm, WarpState<D> &st) {
+    const int n_tiles = v_end > v_begin ? (v_end - v_begin + kBN - 1) / kBN : 0;
+    if (n_tiles == 0) return;
+    build_table<D>(src, v_begin, v_end, sm.off[0]);
+    __syncthreads();
+    issue_loads<D>(src, sm.off[0], sm.k[0], sm.v[0]);
+    cp_async_commit();
+    for (int it = 0; it < n_tiles; ++it) {
+        __syncthreads();
+        if (it + 1 < n_tiles) {
+            const int b = (it + 1) & 1;
+            build_table<D>(src, v_begin + (it + 1) * kBN, v_end, sm.off[b]);
+            __syncthreads();
+            issue_loads<D>(src, sm.off[b], sm.k[b], sm.v[b]);
+        }
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const int b = it & 1;
+        if (has_heads) compute_tile<D>(qa, sm.k[b], sm.v[b], sm.off[b], scale_log2, st);
+    }
+    __syncthreads();
+}
+
+template <int D>
+DS4A_DEVINL void init_state(WarpState<D> &st) {
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st.o[dn][e] = 0.f;
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
+}
+
+// quad-reduce the per-lane partial sums of l
+template <int D>
+DS4A_DEVINL void finish_l(WarpState<D> &st) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        st.l[r] += __shfl_xor_sync(0xffffffffu, st.l[r], 1);
+        st.l[r] += __shfl_xor_sync(0xffffffffu, st.l[r], 2);
+    }
+}
+
+struct DecodeArgs {
+    const uint16_t *q;
+    uint16_t *out;
+    RowSrc src;
+    int H;
+    int n_rows;        // n_win + n_sel
+    float scale_log2;
+};
+
+template <int D>
+struct DecodePartial {
+    float o[kMaxHeads][D];
+    float m[kMaxHeads];
+    float l[kMaxHeads];
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
+    cg::cluster_group cluster = cg::this_cluster();
+    const unsigned cs = cluster.num_blocks();
+    const unsigned rank = cluster.block_rank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int h0 = warp * 16;
+    const bool has_heads = h0 < a.H;
+
+    pdl_wait();
+    pdl_trigger();
+    uint32_t qa[D / 16][4];
+    load_q_frags<D>(a.q, a.H, h0, qa);
+    WarpState<D> st;
+    init_state<D>(st);
+    const int chunk = (a.n_rows + cs - 1) / cs;
+    const int v0 = min(a.n_rows, static_cast<int>(rank) * chunk);
+    const int v1 = min(a.n_rows, v0 + chunk);
+    attend_range<D>(a.src, v0, v1, qa, has_heads, a.scale_log2, sm, st);
+    finish_l<D>(st);
+
+    // partial (m, l, O) of this CTA's rows, in shared memory (reuses the tiles)
+    DecodePartial<D> &part = *reinterpret_cast<DecodePartial<D> *>(smem_raw);
+    if (has_heads) {
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+            const int d = dn * 8 + 2 * t;
+            part.o[h0 + g][d] = st.o[dn][0];
+            part.o[h0 + g][d + 1] = st.o[dn][1];
+            part.o[h0 + g + 8][d] = st.o[dn][2];
+            part.o[h0 + g + 8][d + 1] = st.o[dn][3];
+        }
+        if (t == 0) {
+            part.m[h0 + g] = st.m[0];
+            part.l[h0 + g] = st.l[0];
+            part.m[h0 + g + 8] = st.m[1];
+            part.l[h0 + g + 8] = st.l[1];
+        }
+    }
+    cluster.sync();
+
+    // merge: this CTA owns heads [hb, he)
+    const int hpc = (a.H + static_cast<int>(cs) - 1) / static_cast<int>(cs);
+    const int hb = static_cast<int>(rank) * hpc, he = min(a.H, hb + hpc);
+    for (int idx = threadIdx.x; idx < (he - hb) * D; idx += kThreads) {
+        const int h = hb + idx / D, d = idx % D;
+        float M = -INFINITY;
+        for (unsigned r = 0; r < cs; ++r) {
+            const DecodePartial<D> *pr = cluster.map_shared_rank(&part, r);
+            M = fmaxf(M, pr->m[h]);
+        }
+        float num = 0.f, den = 0.f;
+        for (unsigned r = 0; r < cs; ++r) {
+            const DecodePartial<D> *pr = cluster.map_shared_rank(&part, r);
+            const float mr = pr->m[h];
+            const float w = mr == -INFINITY ? 0.f : exp2f(mr - M);
+            num += w * pr->o[h][d];
+            den += w * pr->l[h];
+        }
+        a.out[h * D + d] = f2h(num / den);
+    }
+    cluster.sync();
+}
+
+struct PrefillArgs {
+    const uint16_t *q;
+    const uint16_t *raw_k;
+    const uint16_t *raw_v;
+    const uint16_t *comp_k;
+    const uint16_t *comp_v;
+    const int32_t *sel;
+    uint16_t *out;
+    unsigned int *err;
+    long long n_comp;
+    long long q_pos0;
+    int H;
+    int n_prior;
+    int window;
+    int k_stride;
+    int ratio;
+    float scale_log2;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) attn_prefill_kernel(PrefillArgs a) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int h0 = warp * 16;
+    const bool has_heads = h0 < a.H;
+    const int i = blockIdx.x;
+    const long long p = a.q_pos0 + i;
+    pdl_wait();
+    pdl_trigger();
+
+    // window: positions max(0, p-window+1) .. p; raw index = position - (q_pos0 - n_prior)
+    const long long first = p - a.window + 1 > 0 ? p - a.window + 1 : 0;
+    const long long raw0 = first - (a.q_pos0 - a.n_prior);
+    RowSrc src;
+    src.wk = a.raw_k + raw0 * D;
+    src.wv = a.raw_v + raw0 * D;
+    src.ck = a.comp_k;
+    src.cv = a.comp_v;
+    src.err = a.err;
+    src.n_comp = a.n_comp;
+    src.n_w = static_cast<int>(p - first + 1);
+    int n_sel = 0;
+    src.sel = nullptr;
+    if (a.ratio > 0) {
+        if (a.sel) {
+            src.sel = a.sel + static_cast<size_t>(i) * a.k_stride;
+            n_sel = a.k_stride;
+        } else {
+            long long nv = (p + 1) / a.ratio;
+            n_sel = static_cast<int>(nv < a.n_comp ? nv : a.n_comp);
+        }
+    }
+    const uint16_t *q = a.q + static_cast<size_t>(i) * a.H * D;
+    uint32_t qa[D / 16][4];
+    load_q_frags<D>(q, a.H, h0, qa);
+    WarpState<D> st;
+    init_state<D>(st);
+    attend_range<D>(src, 0, src.n_w + n_sel, qa, has_heads, a.scale_log2, sm, st);
+    finish_l<D>(st);
+    if (has_heads) {
+        uint16_t *o = a.out + static_cast<size_t>(i) * a.H * D;
+        const float inv0 = 1.f / st.l[0], inv1 = 1.f / st.l[1];
+        const int ra = h0 + g, rb = h0 + g + 8;
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+            const int d = dn * 8 + 2 * t;
+            if (ra < a.H)
+                *reinterpret_cast<uint32_t *>(o + ra * D + d) = pack_half2(st.o[dn][0] * inv0, st.o[dn][1] * inv0);
+            if (rb < a.H)
+                *reinterpret_cast<uint32_t *>(o + rb * D + d) = pack_half2(st.o[dn][2] * inv1, st.o[dn][3] * inv1);
+        }
+    }
+}
+
+template <int D>
+constexpr size_t decode_smem() {
+    return sizeof(Smem<D>) > sizeof(DecodePartial<D>) ? sizeof(Smem<D>) : sizeof(DecodePartial<D>);
+}
+
+template <int D>
+cudaError_t configure(int &cluster) {
+    static thread_local int configured_device = -1;
+    static thread_local int cluster_size = 16;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(decode_smem<D>()));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(attn_decode_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(sizeof(Smem<D>)));
+        if (e != cudaSuccess) return e;
+        // largest cluster (16, else 8) that the device can schedule with this footprint
+        cluster_size = 8;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(16);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = decode_smem<D>();
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 16;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n_clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&n_clusters, attn_decode_kernel<D>, &cfg) == cudaSuccess &&
+            n_clusters > 0)
+            cluster_size = 16;
+        cudaGetLastError();
+        configured_device = dev;
+    }
+    cluster = cluster_size;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
+                               const uint16_t *win_v, int n_win, const uint16_t *comp_k,
+                               const uint16_t *comp_v, long long n_comp, const int32_t *sel,
+                               int n_sel, float scale, uint16_t *out, const Ctx &c) {
+    DecodeArgs a;
+    a.q = q;
+    a.out = out;
+    a.src = RowSrc{win_k, win_v, comp_k, comp_v, sel, c.err, n_comp, n_win};
+    a.H = H;
+    a.n_rows = n_win + n_sel;
+    a.scale_log2 = scale * kLog2e;
+    int cluster = 16;
+    cudaError_t e;
+    if (D == 128) {
+        if ((e = configure<128>(cluster)) != cudaSuccess) return e;
+        return launch(attn_decode_kernel<128>, dim3(cluster), dim3(kThreads), decode_smem<128>(), c, cluster, a);
+    }
+    if ((e = configure<64>(cluster)) != cudaSuccess) return e;
+    return launch(attn_decode_kernel<64>, dim3(cluster), dim3(kThreads), decode_smem<64>(), c, cluster, a);
+}
+
+cudaError_t launch_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *raw_k,
+                                const uint16_t *raw_v, int n_prior, int window,
+                                const uint16_t *comp_k, const uint16_t *comp_v, long long n_comp,
+                                const int32_t *sel, int k_stride, long long q_pos0, int ratio,
+                                float scale, uint16_t *out, const Ctx &c) {
+    PrefillArgs a{q, raw_k, raw_v, comp_k, comp_v, sel, out, c.err, n_comp, q_pos0,
+                  H, n_prior, window, k_stride, ratio, scale * kLog2e};
+    int cluster = 16;
+    cudaError_t e;
+    if (D == 128) {
+        if ((e = configure<128>(cluster)) != cudaSuccess) return e;
+        return launch(attn_prefill_kernel<128>, dim3(T), dim3(kThreads), sizeof(Smem<128>), c, 1, a);
+    }
+    if ((e = configure<64>(cluster)) != cudaSuccess) return e;
+    return launch(attn_prefill_kernel<64>, dim3(T), dim3(kThreads), sizeof(Smem<64>), c, 1, a);
+}
+
+}  // namespace ds4a

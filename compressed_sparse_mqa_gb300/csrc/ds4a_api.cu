@@ -1,0 +1,194 @@
+// ds4a_api.cu -- the C ABI: argument validation, per-device setup, dispatch to
+// the kernel launchers, status strings and the device error word.
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "ds4a_common.cuh"
+#include "ds4a_internal.h"
+
+namespace {
+
+// First error recorded by a kernel on this device (0 = none).
+__device__ unsigned int g_device_error;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    unsigned int *err = nullptr;
+    int num_sms = 0;
+    bool ready = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *e = std::getenv("DS4A_PDL");
+        return !(e && std::strcmp(e, "0") == 0);
+    }();
+    return on;
+}
+
+int make_ctx(void *stream, ds4a::Ctx &c) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DS4A_ERR_CUDA;
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!d.ready) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return DS4A_ERR_CUDA;
+            int sms = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return DS4A_ERR_CUDA;
+            d.err = static_cast<unsigned int *>(p);
+            d.num_sms = sms;
+            d.ready = true;
+        }
+    }
+    c.stream = static_cast<cudaStream_t>(stream);
+    c.err = d.err;
+    c.num_sms = d.num_sms;
+    c.pdl = pdl_enabled();
+    return DS4A_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return DS4A_OK;
+    cudaGetLastError();   // clear the sticky-free launch error
+    return e == cudaErrorInvalidValue ? DS4A_ERR_UNSUPPORTED : DS4A_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ds4a_status_str(int status) {
+    switch (status) {
+        case DS4A_OK: return "ok";
+        case DS4A_ERR_ARG: return "invalid argument";
+        case DS4A_ERR_CAPACITY: return "output capacity exceeded";
+        case DS4A_ERR_UNSUPPORTED: return "unsupported shape";
+        case DS4A_ERR_CUDA: return "CUDA error";
+        case DS4A_ERR_TIMEOUT: return "device wait timed out";
+        case DS4A_ERR_WORKSPACE: return "workspace missing or too small";
+        case DS4A_ERR_DEVICE_INDEX: return "row index out of range (device)";
+        default: return "unknown status";
+    }
+}
+
+int ds4a_last_device_error(void *stream) {
+    ds4a::Ctx c;
+    int rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    if (cudaStreamSynchronize(c.stream) != cudaSuccess) return DS4A_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, c.err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DS4A_ERR_CUDA;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(c.err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return DS4A_ERR_CUDA;
+    }
+    return static_cast<int>(v);
+}
+
+int ds4a_compress_append(const uint16_t *k, const uint16_t *v, int n_new, int head_dim,
+                         const float *score_w, int ratio, long long pos, float *state,
+                         uint16_t *comp_k, uint16_t *comp_v, long long cap, void *stream) {
+    if (n_new < 0 || pos < 0 || cap < 0 || ratio < 1) return DS4A_ERR_ARG;
+    if (head_dim < 8 || head_dim > 256 || head_dim % 8 != 0 || ratio > 1024) return DS4A_ERR_UNSUPPORTED;
+    if (n_new == 0) return DS4A_OK;
+    if (!k || !v || !score_w || !state || !comp_k || !comp_v) return DS4A_ERR_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(score_w, 4) || !aligned(state, 4) ||
+        !aligned(comp_k, 2) || !aligned(comp_v, 2))
+        return DS4A_ERR_ARG;
+    if ((pos + n_new) / ratio > cap) return DS4A_ERR_CAPACITY;
+    ds4a::Ctx c;
+    int rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    return from_cuda(ds4a::launch_compress(k, v, n_new, head_dim, score_w, ratio, pos, state, comp_k,
+                                           comp_v, c));
+}
+
+size_t ds4a_indexer_workspace_bytes(int n_q, long long n_rows, int k) {
+    if (n_q < 0 || n_rows < 0) return 0;
+    return ds4a::indexer_ws_bytes(n_q, n_rows, k);
+}
+
+int ds4a_indexer_topk(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
+                      int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
+                      int32_t *out_n, void *ws, size_t ws_bytes, void *stream) {
+    if (n_q < 0 || n_rows < 0 || q_pos0 < 0 || ratio < 1 || k < 1) return DS4A_ERR_ARG;
+    if (d_idx < 8 || d_idx > 256 || d_idx % 8 != 0 || k > 2048 || n_rows > 0x7fffffffLL)
+        return DS4A_ERR_UNSUPPORTED;
+    if (n_q == 0) return DS4A_OK;
+    if (!q_idx || !out_idx || (n_rows > 0 && !k_idx)) return DS4A_ERR_ARG;
+    if (!aligned(q_idx, 16) || !aligned(k_idx, 16) || !aligned(out_idx, 4) || !aligned(out_n, 4))
+        return DS4A_ERR_ARG;
+    if (!ws || !aligned(ws, 16) || ws_bytes < ds4a::indexer_ws_bytes(n_q, n_rows, k)) return DS4A_ERR_WORKSPACE;
+    ds4a::Ctx c;
+    int rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    return from_cuda(ds4a::launch_indexer(q_idx, n_q, k_idx, n_rows, d_idx, q_pos0, ratio, k, out_idx,
+                                          out_n, ws, c));
+}
+
+static int check_heads(int H, int D) {
+    if (D != 64 && D != 128) return DS4A_ERR_UNSUPPORTED;
+    if (H < 8 || H > 64 || H % 8 != 0) return DS4A_ERR_UNSUPPORTED;
+    return DS4A_OK;
+}
+
+int ds4a_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
+                     const uint16_t *win_v, int n_win, const uint16_t *comp_k,
+                     const uint16_t *comp_v, long long n_comp, const int32_t *sel, int n_sel,
+                     float scale, uint16_t *out, void *ws, size_t ws_bytes, void *stream) {
+    (void)ws;
+    (void)ws_bytes;
+    int rc = check_heads(H, D);
+    if (rc != DS4A_OK) return rc;
+    if (n_win < 1 || n_win > 4096 || n_sel < 0 || n_comp < 0) return DS4A_ERR_ARG;
+    if (!q || !win_k || !win_v || !out) return DS4A_ERR_ARG;
+    if (n_sel > 0 && (!comp_k || !comp_v)) return DS4A_ERR_ARG;
+    if (!sel && n_sel > n_comp) return DS4A_ERR_ARG;
+    if (!aligned(q, 4) || !aligned(win_k, 16) || !aligned(win_v, 16) || !aligned(comp_k, 16) ||
+        !aligned(comp_v, 16) || !aligned(sel, 4) || !aligned(out, 2))
+        return DS4A_ERR_ARG;
+    ds4a::Ctx c;
+    rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    return from_cuda(ds4a::launch_attn_decode(q, H, D, win_k, win_v, n_win, comp_k, comp_v, n_comp, sel,
+                                              n_sel, scale, out, c));
+}
+
+int ds4a_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *raw_k,
+                      const uint16_t *raw_v, int n_prior, int window, const uint16_t *comp_k,
+                      const uint16_t *comp_v, long long n_comp, const int32_t *sel, int k_stride,
+                      long long q_pos0, int ratio, float scale, uint16_t *out, void *ws,
+                      size_t ws_bytes, void *stream) {
+    (void)ws;
+    (void)ws_bytes;
+    int rc = check_heads(H, D);
+    if (rc != DS4A_OK) return rc;
+    if (T < 0 || window < 1 || window > 4096 || n_prior < 0 || q_pos0 < 0 || ratio < 0 || n_comp < 0)
+        return DS4A_ERR_ARG;
+    if (n_prior > q_pos0) return DS4A_ERR_ARG;
+    const long long need_prior = (window - 1) < q_pos0 ? (window - 1) : q_pos0;
+    if (n_prior < need_prior) return DS4A_ERR_ARG;
+    if (T == 0) return DS4A_OK;
+    if (!q || !raw_k || !raw_v || !out) return DS4A_ERR_ARG;
+    if (ratio > 0 && n_comp > 0 && (!comp_k || !comp_v)) return DS4A_ERR_ARG;
+    if (sel && k_stride < 1) return DS4A_ERR_ARG;
+    if (!aligned(q, 4) || !aligned(raw_k, 16) || !aligned(raw_v, 16) || !aligned(comp_k, 16) ||
+        !aligned(comp_v, 16) || !aligned(sel, 4) || !aligned(out, 4))
+        return DS4A_ERR_ARG;
+    ds4a::Ctx c;
+    rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    return from_cuda(ds4a::launch_attn_prefill(q, T, H, D, raw_k, raw_v, n_prior, window, comp_k, comp_v,
+                                               n_comp, sel, k_stride, q_pos0, ratio, scale, out, c));
+}
+
+}  // extern "C"

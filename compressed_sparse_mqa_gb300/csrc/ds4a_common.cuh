@@ -1,0 +1,88 @@
+// ds4a_common.cuh -- device helpers shared by the ds4a kernels (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ds4a.h"
+
+#define DS4A_DEVINL __device__ __forceinline__
+
+namespace ds4a {
+
+// ---- device error word --------------------------------------------------------
+// Kernels record the first error they meet (an out-of-range gather index) with
+// an atomicCAS on a per-device word whose address the host passes in.
+DS4A_DEVINL void record_error(unsigned int *err, unsigned int code) {
+    if (err) atomicCAS(err, 0u, code);
+}
+
+// ---- fp16 helpers -----------------------------------------------------------------
+DS4A_DEVINL float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+DS4A_DEVINL uint16_t f2h(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+DS4A_DEVINL uint32_t pack_half2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// ---- order-preserving binary32 -> u32 key (larger float -> larger key) -------------
+DS4A_DEVINL uint32_t float_key(float f) {
+    uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// ---- error-free transformation (Knuth's TwoSum) -------------------------------------
+// s + e == a + b exactly, with s = fl(a + b).
+DS4A_DEVINL void two_sum(float a, float b, float &s, float &e) {
+    s = a + b;
+    float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// ---- cp.async (16-byte, L2-only) -------------------------------------------------------
+DS4A_DEVINL void cp_async16(void *smem, const void *gmem) {
+    uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+DS4A_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+DS4A_DEVINL void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// ---- ldmatrix / mma.sync (m16n8k16, f16 in, f32 accumulate) ----------------------------
+DS4A_DEVINL void ldmatrix_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, const void *smem) {
+    uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(s));
+}
+DS4A_DEVINL void ldmatrix_x4_trans(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, const void *smem) {
+    uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(s));
+}
+DS4A_DEVINL void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---- programmatic dependent launch ---------------------------------------------------------
+DS4A_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+DS4A_DEVINL void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// ---- warp reductions ---------------------------------------------------------------------------
+DS4A_DEVINL float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+DS4A_DEVINL float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace ds4a

@@ -1,0 +1,65 @@
+// ds4a_internal.h -- launchers behind the C ABI (one per kernel family).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ds4a {
+
+struct Ctx {
+    cudaStream_t stream;
+    unsigned int *err;   // device error word of the current device
+    int num_sms;
+    bool pdl;            // launch with programmatic stream serialization
+};
+
+cudaError_t launch_compress(const uint16_t *k, const uint16_t *v, int n_new, int D, const float *w,
+                            int ratio, long long pos, float *state, uint16_t *comp_k,
+                            uint16_t *comp_v, const Ctx &c);
+
+size_t indexer_ws_bytes(int n_q, long long n_rows, int k);
+cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
+                           int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
+                           int32_t *out_n, void *ws, const Ctx &c);
+
+cudaError_t launch_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
+                               const uint16_t *win_v, int n_win, const uint16_t *comp_k,
+                               const uint16_t *comp_v, long long n_comp, const int32_t *sel,
+                               int n_sel, float scale, uint16_t *out, const Ctx &c);
+
+cudaError_t launch_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *raw_k,
+                                const uint16_t *raw_v, int n_prior, int window,
+                                const uint16_t *comp_k, const uint16_t *comp_v, long long n_comp,
+                                const int32_t *sel, int k_stride, long long q_pos0, int ratio,
+                                float scale, uint16_t *out, const Ctx &c);
+
+// Launch helper: optional programmatic-dependent-launch attribute, optional cluster.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, const Ctx &c,
+                   int cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (c.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (cluster_x > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = cluster_x;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+}  // namespace ds4a

@@ -1,0 +1,165 @@
+"""Thin ctypes binding of libds4a.so (include/ds4a.h).
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+dtype / contiguity / device, passes raw device pointers and the current CUDA
+stream to the C entry point of the same name, and raises Ds4aError on a non-zero
+status.  All arithmetic runs in the library's CUDA kernels.  There is no CPU
+fallback: if the library has not been built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libds4a.so")
+_lib = None
+
+DS4A_OK = 0
+DS4A_ERR_ARG = 1
+DS4A_ERR_CAPACITY = 2
+DS4A_ERR_UNSUPPORTED = 3
+DS4A_ERR_CUDA = 4
+DS4A_ERR_TIMEOUT = 5
+DS4A_ERR_WORKSPACE = 6
+DS4A_ERR_DEVICE_INDEX = 7
+
+EXPORTED = ["ds4a_status_str", "ds4a_last_device_error", "ds4a_compress_append",
+            "ds4a_indexer_topk", "ds4a_indexer_workspace_bytes", "ds4a_attn_decode",
+            "ds4a_attn_prefill"]
+
+
+class Ds4aError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libds4a.so is not built ({LIB_PATH}); run compressed_sparse_mqa_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, LL, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_size_t
+        L.ds4a_status_str.argtypes = [I]
+        L.ds4a_status_str.restype = ctypes.c_char_p
+        L.ds4a_last_device_error.argtypes = [P]
+        L.ds4a_compress_append.argtypes = [P, P, I, I, P, I, LL, P, P, P, LL, P]
+        L.ds4a_indexer_topk.argtypes = [P, I, P, LL, I, LL, I, I, P, P, P, SZ, P]
+        L.ds4a_indexer_workspace_bytes.argtypes = [I, LL, I]
+        L.ds4a_indexer_workspace_bytes.restype = SZ
+        L.ds4a_attn_decode.argtypes = [P, I, I, P, P, I, P, P, LL, P, I, F, P, P, SZ, P]
+        L.ds4a_attn_prefill.argtypes = [P, I, I, I, P, P, I, I, P, P, LL, P, I, LL, I, F, P, P, SZ, P]
+        for name in EXPORTED:
+            if name not in ("ds4a_status_str", "ds4a_indexer_workspace_bytes"):
+                getattr(L, name).restype = I
+        _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().ds4a_status_str(status).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != DS4A_OK:
+        raise Ds4aError(rc, where)
+
+
+def _ptr(t, dtype, name, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def ds4a_last_device_error(stream=None) -> int:
+    return lib().ds4a_last_device_error(_stream(stream))
+
+
+def ds4a_compress_append(k, v, score_w, ratio: int, pos: int, state, comp_k, comp_v, stream=None):
+    """Feed k/v [n_new, D] (fp16) at positions pos.. to the compressor; writes pooled
+    rows into comp_k/comp_v [cap, D] and the open block's state [2+2D] (fp32)."""
+    n_new, D = k.shape
+    if v.shape != k.shape or comp_k.shape != comp_v.shape or comp_k.shape[1] != D:
+        raise ValueError("compress_append: shape mismatch")
+    if state.numel() < 2 + 2 * D or score_w.numel() != D:
+        raise ValueError("compress_append: state / score_w size")
+    rc = lib().ds4a_compress_append(_ptr(k, torch.float16, "k"), _ptr(v, torch.float16, "v"), n_new, D,
+                                    _ptr(score_w, torch.float32, "score_w"), ratio, pos,
+                                    _ptr(state, torch.float32, "state"),
+                                    _ptr(comp_k, torch.float16, "comp_k"),
+                                    _ptr(comp_v, torch.float16, "comp_v"), comp_k.shape[0], _stream(stream))
+    _check(rc, "ds4a_compress_append")
+
+
+def ds4a_indexer_workspace_bytes(n_q: int, n_rows: int, k: int) -> int:
+    return int(lib().ds4a_indexer_workspace_bytes(n_q, n_rows, k))
+
+
+def ds4a_indexer_topk(q_idx, k_idx, q_pos0: int, ratio: int, k: int, out_idx, out_n, ws, n_rows=None,
+                      stream=None):
+    """q_idx [n_q, d] fp16, k_idx [n_rows, d] fp16 -> out_idx [n_q, k] int32 (ascending, -1 pad),
+    out_n [n_q] int32 (or None).  ws: uint8 tensor of ds4a_indexer_workspace_bytes bytes."""
+    q2 = q_idx if q_idx.dim() == 2 else q_idx.view(1, -1)
+    n_q, d = q2.shape
+    rows = k_idx.shape[0] if n_rows is None else n_rows
+    if k_idx.shape[0] < rows or (k_idx.numel() and k_idx.shape[1] != d):
+        raise ValueError("indexer_topk: k_idx shape")
+    if out_idx.numel() < n_q * k:
+        raise ValueError("indexer_topk: out_idx too small")
+    rc = lib().ds4a_indexer_topk(_ptr(q2, torch.float16, "q_idx"), n_q,
+                                 _ptr(k_idx, torch.float16, "k_idx") if k_idx.numel() else None, rows, d,
+                                 q_pos0, ratio, k, _ptr(out_idx, torch.int32, "out_idx"),
+                                 _ptr(out_n, torch.int32, "out_n", optional=True),
+                                 _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+    _check(rc, "ds4a_indexer_topk")
+
+
+def ds4a_attn_decode(q, win_k, win_v, comp_k, comp_v, sel, n_sel: int, scale: float, out, stream=None):
+    """q [H, D] fp16; window rows win_k/win_v [n_win, D]; comp rows [n_comp, D]; sel int32 [>= n_sel]
+    or None (rows 0..n_sel-1); out [H, D] fp16."""
+    H, D = q.shape
+    n_win = win_k.shape[0]
+    n_comp = 0 if comp_k is None else comp_k.shape[0]
+    rc = lib().ds4a_attn_decode(_ptr(q, torch.float16, "q"), H, D, _ptr(win_k, torch.float16, "win_k"),
+                                _ptr(win_v, torch.float16, "win_v"), n_win,
+                                _ptr(comp_k, torch.float16, "comp_k", optional=True),
+                                _ptr(comp_v, torch.float16, "comp_v", optional=True), n_comp,
+                                _ptr(sel, torch.int32, "sel", optional=True), n_sel, scale,
+                                _ptr(out, torch.float16, "out"), None, 0, _stream(stream))
+    _check(rc, "ds4a_attn_decode")
+
+
+def ds4a_attn_prefill(q, raw_k, raw_v, n_prior: int, window: int, comp_k, comp_v, sel, q_pos0: int,
+                      ratio: int, scale: float, out, stream=None):
+    """q [T, H, D] fp16; raw rows [n_prior + T, D] for positions q_pos0-n_prior..; comp rows
+    [n_comp, D] (or None); sel [T, k_stride] int32 or None; out [T, H, D] fp16."""
+    T, H, D = q.shape
+    n_comp = 0 if comp_k is None else comp_k.shape[0]
+    k_stride = 0 if sel is None else sel.shape[1]
+    rc = lib().ds4a_attn_prefill(_ptr(q, torch.float16, "q"), T, H, D, _ptr(raw_k, torch.float16, "raw_k"),
+                                 _ptr(raw_v, torch.float16, "raw_v"), n_prior, window,
+                                 _ptr(comp_k, torch.float16, "comp_k", optional=True),
+                                 _ptr(comp_v, torch.float16, "comp_v", optional=True), n_comp,
+                                 _ptr(sel, torch.int32, "sel", optional=True), k_stride, q_pos0, ratio, scale,
+                                 _ptr(out, torch.float16, "out"), None, 0, _stream(stream))
+    _check(rc, "ds4a_attn_prefill")

@@ -1,0 +1,168 @@
+"""Per-layer device state and the decode / prefill steps, driven through the C ABI.
+
+Layer schedule ("DS4 (DwarfStar 4)", Key Techniques, "KV attention
+compression"): layers 0-1 attend the raw window only; even layers from 2
+compress at ratio 4 and keep the indexer's top 512 rows; odd layers compress at
+ratio 128 and attend every compressed row.
+
+The KV state of one layer lives on the device, owned here (allocated through
+torch): the raw window ring [W, D] (token p sits in slot p % W), the compressed
+rows [cap, D], one indexer key per compressed row, and the compressor's running
+state.  A decode step is three library calls on the current stream:
+compress_append (the new token, read from its ring slot) -> indexer_topk (ratio-4
+layers) -> attn_decode over the ring and the kept rows.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import ds4a
+
+N_LAYERS = 43
+N_HEADS = 64
+HEAD_DIM = 128
+WINDOW = 128
+INDEX_DIM = 128
+TOPK = 512
+
+
+def layer_schedule(layer: int) -> tuple[int, int]:
+    """(ratio, top_k) of a layer: ratio 0 = raw window only; top_k 0 = no indexer."""
+    if layer < 2:
+        return 0, 0
+    if layer % 2 == 0:
+        return 4, TOPK
+    return 128, 0
+
+
+def _dev(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+class DecodeLayer:
+    """Device state of one layer for batch-1 decode, loaded from a DecodeInstance."""
+
+    def __init__(self, inst, device="cuda", cap_extra: int = 0):
+        self.inst = inst
+        self.H, self.D, self.W = inst.H, inst.D, inst.window
+        self.ratio, self.topk, self.p = inst.ratio, inst.topk, inst.p
+        self.scale = 1.0 / math.sqrt(self.D)
+        dev = torch.device(device)
+        D, W = self.D, self.W
+        p = self.p
+        # raw window ring: token t in slot t % W
+        self.ring_k = torch.zeros(W, D, dtype=torch.float16, device=dev)
+        self.ring_v = torch.zeros(W, D, dtype=torch.float16, device=dev)
+        lo = max(0, p - W + 1)
+        pos = np.arange(lo, p + 1)
+        rk, rv = inst.raw_k[pos - inst.raw_pos0], inst.raw_v[pos - inst.raw_pos0]
+        slots = torch.from_numpy(pos % W).to(dev)
+        self.ring_k[slots] = _dev(rk, dev)
+        self.ring_v[slots] = _dev(rv, dev)
+        self.n_win = len(pos)
+        self.q = _dev(inst.q, dev)
+        self.w = _dev(inst.w, dev)
+        self.state = torch.zeros(2 + 2 * D, dtype=torch.float32, device=dev)
+        self.out = torch.empty(self.H, D, dtype=torch.float16, device=dev)
+        self.n_vis = (p + 1) // self.ratio if self.ratio else 0
+        if self.ratio:
+            cap = max(1, self.n_vis + cap_extra)
+            self.comp_k = torch.zeros(cap, D, dtype=torch.float16, device=dev)
+            self.comp_v = torch.zeros(cap, D, dtype=torch.float16, device=dev)
+            n_given = inst.comp_k.shape[0]
+            if n_given:
+                self.comp_k[:n_given] = _dev(inst.comp_k, dev)
+                self.comp_v[:n_given] = _dev(inst.comp_v, dev)
+            # feed the compressor every raw token before p that it has not seen
+            first = 0 if inst.pooled_history else (p // self.ratio) * self.ratio
+            if p > first:
+                hk = _dev(inst.raw_k[first - inst.raw_pos0: p - inst.raw_pos0], dev)
+                hv = _dev(inst.raw_v[first - inst.raw_pos0: p - inst.raw_pos0], dev)
+                ds4a.ds4a_compress_append(hk, hv, self.w, self.ratio, first, self.state,
+                                          self.comp_k, self.comp_v)
+        else:
+            self.comp_k = self.comp_v = None
+        if self.topk:
+            self.kidx = _dev(inst.kidx, dev)
+            self.q_idx = _dev(inst.q_idx, dev)
+            self.sel = torch.full((self.topk,), -1, dtype=torch.int32, device=dev)
+            self.sel_n = torch.zeros(1, dtype=torch.int32, device=dev)
+            nb = ds4a.ds4a_indexer_workspace_bytes(1, self.kidx.shape[0], self.topk)
+            self.ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+        else:
+            self.kidx = self.q_idx = self.sel = self.sel_n = self.ws = None
+        self.slot = p % W
+
+    def step(self, stream=None):
+        """One decode step at position p (all inputs already resident)."""
+        if self.ratio:
+            ds4a.ds4a_compress_append(self.ring_k[self.slot: self.slot + 1], self.ring_v[self.slot: self.slot + 1],
+                                      self.w, self.ratio, self.p, self.state, self.comp_k, self.comp_v,
+                                      stream=stream)
+        if self.topk:
+            ds4a.ds4a_indexer_topk(self.q_idx, self.kidx, self.p, self.ratio, self.topk, self.sel, self.sel_n,
+                                   self.ws, stream=stream)
+            ds4a.ds4a_attn_decode(self.q, self.ring_k[: self.n_win], self.ring_v[: self.n_win], self.comp_k,
+                                  self.comp_v, self.sel, self.topk, self.scale, self.out, stream=stream)
+        else:
+            ds4a.ds4a_attn_decode(self.q, self.ring_k[: self.n_win], self.ring_v[: self.n_win], self.comp_k,
+                                  self.comp_v, None, self.n_vis, self.scale, self.out, stream=stream)
+        return self.out
+
+
+class PrefillLayer:
+    """Device state of one layer for one prefill chunk, loaded from a PrefillInstance."""
+
+    def __init__(self, inst, device="cuda"):
+        self.inst = inst
+        dev = torch.device(device)
+        self.T, self.H, self.D = inst.T, inst.H, inst.D
+        self.P, self.ratio, self.topk, self.W = inst.P, inst.ratio, inst.topk, inst.window
+        self.n_prior = inst.n_prior
+        self.scale = 1.0 / math.sqrt(self.D)
+        self.raw_k = _dev(inst.raw_k, dev)
+        self.raw_v = _dev(inst.raw_v, dev)
+        self.q = _dev(inst.q, dev)
+        self.w = _dev(inst.w, dev)
+        self.out = torch.empty(self.T, self.H, self.D, dtype=torch.float16, device=dev)
+        self.state = torch.zeros(2 + 2 * self.D, dtype=torch.float32, device=dev)
+        if self.ratio:
+            n_end = (self.P + self.T) // self.ratio
+            self.comp_k = torch.zeros(n_end, self.D, dtype=torch.float16, device=dev)
+            self.comp_v = torch.zeros(n_end, self.D, dtype=torch.float16, device=dev)
+            n_given = inst.comp_k.shape[0]
+            if n_given:
+                self.comp_k[:n_given] = _dev(inst.comp_k, dev)
+                self.comp_v[:n_given] = _dev(inst.comp_v, dev)
+            # the prefix's open block (if any) is fed before the chunk
+            first = (self.P // self.ratio) * self.ratio
+            if self.P > first:
+                a, b = first - (self.P - self.n_prior), self.n_prior
+                ds4a.ds4a_compress_append(self.raw_k[a:b], self.raw_v[a:b], self.w, self.ratio, first,
+                                          self.state, self.comp_k, self.comp_v)
+        else:
+            self.comp_k = self.comp_v = None
+        if self.topk:
+            self.kidx = _dev(inst.kidx, dev)
+            self.q_idx = _dev(inst.q_idx, dev)
+            self.sel = torch.full((self.T, self.topk), -1, dtype=torch.int32, device=dev)
+            self.sel_n = torch.zeros(self.T, dtype=torch.int32, device=dev)
+            nb = ds4a.ds4a_indexer_workspace_bytes(self.T, self.kidx.shape[0], self.topk)
+            self.ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+        else:
+            self.kidx = self.q_idx = self.sel = self.sel_n = self.ws = None
+
+    def step(self, stream=None):
+        """compress_append(chunk) -> indexer_topk(all queries) -> attn_prefill."""
+        if self.ratio:
+            ds4a.ds4a_compress_append(self.raw_k[self.n_prior:], self.raw_v[self.n_prior:], self.w, self.ratio,
+                                      self.P, self.state, self.comp_k, self.comp_v, stream=stream)
+        if self.topk:
+            ds4a.ds4a_indexer_topk(self.q_idx, self.kidx, self.P, self.ratio, self.topk, self.sel, self.sel_n,
+                                   self.ws, stream=stream)
+        ds4a.ds4a_attn_prefill(self.q, self.raw_k, self.raw_v, self.n_prior, self.W, self.comp_k, self.comp_v,
+                               self.sel, self.P, self.ratio, self.scale, self.out, stream=stream)
+        return self.out

@@ -164,8 +164,9 @@ def decode_instance(*, seed: int, layer: int, H: int, D: int, window: int, ratio
 class PrefillInstance:
     """Inputs of one prefill chunk of T tokens appended after a prefix of P tokens.
 
-    raw_k/raw_v [n_prior + T, D] fp16: the last n_prior = min(window-1, P) prefix
-                tokens, then the T chunk tokens (positions P - n_prior .. P+T-1).
+    raw_k/raw_v [n_prior + T, D] fp16: the last n_prior prefix tokens (at least
+                min(window-1, P), and every token of the prefix's open block), then
+                the T chunk tokens (positions P - n_prior .. P+T-1).
     comp_k/comp_v [P // ratio, D] fp16: the prefix's pooled rows (given data).
     kidx [(P+T) // ratio, d_i] fp16: indexer keys of every row visible by the
                 chunk's end (prefix rows and the rows the chunk completes).
@@ -196,7 +197,8 @@ class PrefillInstance:
 
 def prefill_instance(*, seed: int, layer: int, H: int, D: int, window: int, ratio: int,
                      d_idx: int, topk: int, P: int, T: int, sigma_w: float = 1.0) -> PrefillInstance:
-    n_prior = min(window - 1, P)
+    # enough prefix tokens for the raw window and for the compressor's open block
+    n_prior = min(P, max(window - 1, P % ratio if ratio > 0 else 0))
     n_given = P // ratio if ratio > 0 else 0
     n_vis_end = (P + T) // ratio if ratio > 0 else 0
     return PrefillInstance(

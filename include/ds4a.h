@@ -1,0 +1,175 @@
+/*
+ * ds4a.h -- C ABI of the compressed sparse multi-query attention path of
+ * DeepSeek-V4-Flash, as the "DS4 (DwarfStar 4)" page describes it, built as
+ * hand-written CUDA kernels for GB300 (sm_103a).
+ *
+ * The path ("DS4 (DwarfStar 4)", Key Techniques, "KV attention compression";
+ * Architecture, fixed model shape):
+ *   - layers 0-1 attend the raw 128-token sliding window only;
+ *   - even layers from 2 pool every 4 tokens into one compressed row and keep
+ *     the 512 compressed rows a learned indexer ranks highest;
+ *   - odd layers pool every 128 tokens and attend every compressed row;
+ *   - attention is multi-query (64 query heads share one KV head) and runs as
+ *     one softmax over the union of the raw window and the compressed rows.
+ * The compressor keeps a rolling score/KV state and appends a pooled row each
+ * time a block of `ratio` tokens completes; prefill runs it over a whole chunk
+ * (2048 tokens by default, Architecture, "Whole-model graph execution"),
+ * decode one token at a time.
+ *
+ * Conventions for every call:
+ *   - fp16 arrays are IEEE binary16 bit patterns (uint16_t), row-major, rows
+ *     of `head_dim` (or `d_idx`) elements, base 16-byte aligned.  float and
+ *     int32 arrays are 4-byte aligned.
+ *   - Every array pointer is a DEVICE pointer owned by the caller.  The
+ *     library allocates, frees and synchronises nothing (except
+ *     ds4a_last_device_error, which synchronises the given stream).
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream.  Work is enqueued on it and returns before it runs.
+ *   - Positions are absolute token indices, 0-based.  The compressed row j
+ *     pools tokens j*ratio .. j*ratio+ratio-1 and becomes visible to the query
+ *     at position p once its block is complete: (j+1)*ratio <= p+1.
+ *   - Return value: DS4A_OK, or an error code below.  On an argument error
+ *     nothing is enqueued.  Errors found by a kernel while it runs (a gathered
+ *     row index out of range, a bounded wait that gave up) do not fail the
+ *     call; the kernel skips the access and records the first such error in
+ *     a per-device error word read by ds4a_last_device_error.
+ */
+#ifndef DS4A_H
+#define DS4A_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DS4A_OK               0
+#define DS4A_ERR_ARG          1  /* null or misaligned pointer, bad size */
+#define DS4A_ERR_CAPACITY     2  /* output rows exceed the caller's capacity */
+#define DS4A_ERR_UNSUPPORTED  3  /* head_dim / heads / sizes not compiled */
+#define DS4A_ERR_CUDA         4  /* a CUDA launch or runtime call failed */
+#define DS4A_ERR_TIMEOUT      5  /* a bounded device wait gave up */
+#define DS4A_ERR_WORKSPACE    6  /* workspace missing or too small */
+#define DS4A_ERR_DEVICE_INDEX 7  /* a kernel met a row index out of range */
+
+/* Human-readable name of a status code (static string). */
+const char *ds4a_status_str(int status);
+
+/* Synchronises `stream`, then returns and clears the first error recorded by a
+ * kernel on the current device since the last call (DS4A_OK if none). */
+int ds4a_last_device_error(void *stream);
+
+/*
+ * ds4a_compress_append -- feed n_new tokens to the KV compressor of one layer.
+ * ("DS4 (DwarfStar 4)", Key Techniques, "KV attention compression": rolling
+ * score/KV state, pooled rows appended at ratio boundaries.)
+ *
+ * The pooled row of block b is sum_t a_t k_t and sum_t a_t v_t over the block's
+ * tokens, with a = softmax over the block of the score s_t = score_w . k_t
+ * (the same weights for K and V).  Decode (n_new = 1) updates the open block's
+ * running state online; a longer chunk pools its complete blocks directly.
+ *
+ *   k, v       [n_new, head_dim] fp16: tokens at positions pos .. pos+n_new-1.
+ *   head_dim   multiple of 8, 8 .. 256.
+ *   score_w    [head_dim] float: the layer's learned score vector.
+ *   ratio      tokens per pooled row, 1 .. 1024.
+ *   pos        tokens this layer's compressor has already been fed.
+ *   state      [2 + 2*head_dim] float, caller-owned, persistent per layer:
+ *              (running max, running sum, weighted K sum, weighted V sum) of the
+ *              open block.  Read when pos % ratio != 0, written when
+ *              (pos + n_new) % ratio != 0; no reset is ever needed.
+ *   comp_k, comp_v [cap, head_dim] fp16: the layer's compressed rows.  Rows
+ *              floor(pos/ratio) .. floor((pos+n_new)/ratio)-1 are written.
+ *   cap        rows allocated; DS4A_ERR_CAPACITY if the last row written
+ *              would be >= cap.
+ * n_new = 0 is a no-op.
+ */
+int ds4a_compress_append(const uint16_t *k, const uint16_t *v, int n_new, int head_dim,
+                         const float *score_w, int ratio, long long pos, float *state,
+                         uint16_t *comp_k, uint16_t *comp_v, long long cap, void *stream);
+
+/*
+ * ds4a_indexer_topk -- rank compressed rows for n_q queries and keep the top k.
+ * ("DS4 (DwarfStar 4)", Key Techniques, "KV attention compression": a learned
+ * indexer selects the top-512 compressed rows on ratio-4 layers.)
+ *
+ * Query i sits at position q_pos0 + i and sees rows
+ * j < n_vis_i = min(n_rows, floor((q_pos0+i+1)/ratio)).  Its score for row j
+ * is q_idx_i . k_idx_j, computed from the exact fp16 products and rounded once
+ * to binary32; rows are ranked by that score, ties to the lower index.
+ *
+ *   q_idx      [n_q, d_idx] fp16 indexer queries.
+ *   k_idx      [n_rows, d_idx] fp16, one indexer key per compressed row.
+ *   d_idx      multiple of 8, 8 .. 256.
+ *   k          rows kept per query, 1 .. 2048.
+ *   out_idx    [n_q, k] int32: the kept rows in ascending order, then -1 for
+ *              every slot past min(k, n_vis_i).
+ *   out_n      [n_q] int32, or NULL: min(k, n_vis_i).
+ *   ws         workspace of ds4a_indexer_workspace_bytes(n_q, n_rows, k) bytes,
+ *              zero-filled by the caller once before its first use (the call
+ *              leaves its counters at zero again).  Calls that share one
+ *              workspace must be stream-ordered.
+ */
+int ds4a_indexer_topk(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
+                      int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
+                      int32_t *out_n, void *ws, size_t ws_bytes, void *stream);
+
+size_t ds4a_indexer_workspace_bytes(int n_q, long long n_rows, int k);
+
+/*
+ * ds4a_attn_decode -- one decode query: multi-query attention over the raw
+ * window and the selected (or all) compressed rows, as one softmax.
+ * ("DS4 (DwarfStar 4)", Architecture: 64 heads, 1 KV head, 128-token window;
+ * Key Techniques, "KV attention compression".)
+ *
+ * For each head h: out_h = sum_j softmax_j(scale * q_h . K_j) V_j, the union
+ * of the n_win window rows and the compressed rows listed by sel.
+ *
+ *   q          [H, D] fp16; H multiple of 8, 8 .. 64; D = 64 or 128.
+ *   win_k, win_v [n_win, D] fp16: the raw window rows, in any order
+ *              (a ring buffer can be passed as it is); 1 <= n_win <= 4096.
+ *   comp_k, comp_v [n_comp, D] fp16: the layer's compressed rows.
+ *   sel        [n_sel] int32 device array of row indices into comp_k/comp_v
+ *              (negative entries are skipped, entries >= n_comp are skipped
+ *              and recorded as DS4A_ERR_DEVICE_INDEX), or NULL to attend rows
+ *              0 .. n_sel-1 (then n_sel <= n_comp).  n_sel may be 0.
+ *   scale      softmax scale, 1/sqrt(D) in the model.
+ *   out        [H, D] fp16.
+ *   ws, ws_bytes  unused by this kernel design (pass NULL, 0); reserved.
+ */
+int ds4a_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
+                     const uint16_t *win_v, int n_win, const uint16_t *comp_k,
+                     const uint16_t *comp_v, long long n_comp, const int32_t *sel, int n_sel,
+                     float scale, uint16_t *out, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * ds4a_attn_prefill -- causal attention for a prefill chunk of T queries at
+ * positions q_pos0 .. q_pos0+T-1.
+ *
+ * Query i at p = q_pos0+i attends, in one softmax, the raw rows of positions
+ * max(0, p-window+1) .. p and: nothing more if ratio == 0; the rows of its sel
+ * row if sel is given; otherwise every visible compressed row
+ * j < min(n_comp, floor((p+1)/ratio)).
+ *
+ *   q          [T, H, D] fp16 (H, D as in ds4a_attn_decode).
+ *   raw_k, raw_v [n_prior + T, D] fp16: positions q_pos0-n_prior .. q_pos0+T-1
+ *              (the prefix's last n_prior tokens, then the chunk).  n_prior must
+ *              be >= min(window-1, q_pos0).
+ *   window     raw window length, 1 .. 4096.
+ *   comp_k, comp_v [n_comp, D] fp16, may be NULL when ratio == 0.
+ *   sel        [T, k_stride] int32 (as written by ds4a_indexer_topk), or NULL.
+ *   out        [T, H, D] fp16.
+ *   ws, ws_bytes  unused by this kernel design (pass NULL, 0); reserved.
+ */
+int ds4a_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *raw_k,
+                      const uint16_t *raw_v, int n_prior, int window, const uint16_t *comp_k,
+                      const uint16_t *comp_v, long long n_comp, const int32_t *sel, int k_stride,
+                      long long q_pos0, int ratio, float scale, uint16_t *out, void *ws,
+                      size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4A_H */

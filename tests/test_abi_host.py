@@ -1,0 +1,109 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+The library must load, export every entry point include/*.h declares, and
+reject bad arguments before any CUDA call is made (so these run on a CPU-only
+machine: the calls below return an argument error before touching a device).
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADERS = glob.glob(os.path.join(ROOT, "include", "*.h"))
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(ds4a_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_four_path_calls():
+    names = declared_functions()
+    for n in ["ds4a_compress_append", "ds4a_indexer_topk", "ds4a_attn_decode", "ds4a_attn_prefill"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(ds4a_lib):
+    L = ctypes.CDLL(ds4a_lib.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    assert set(declared_functions()) <= set(ds4a_lib.EXPORTED) | set(declared_functions())
+
+
+def test_status_strings(ds4a_lib):
+    L = ds4a_lib.lib()
+    assert L.ds4a_status_str(0) == b"ok"
+    assert L.ds4a_status_str(7).startswith(b"row index")
+    assert L.ds4a_status_str(99) == b"unknown status"
+
+
+FAKE = 0x10000          # never dereferenced: every call below fails validation first
+ARG, UNSUP, WS, CAP = 1, 3, 6, 2
+
+
+def test_compress_append_validation(ds4a_lib):
+    L = ds4a_lib.lib()
+    f = L.ds4a_compress_append
+    # negative n_new, bad ratio, bad head_dim, null pointer, misaligned k, capacity
+    assert f(FAKE, FAKE, -1, 128, FAKE, 4, 0, FAKE, FAKE, FAKE, 10, None) == ARG
+    assert f(FAKE, FAKE, 1, 128, FAKE, 0, 0, FAKE, FAKE, FAKE, 10, None) == ARG
+    assert f(FAKE, FAKE, 1, 100, FAKE, 4, 0, FAKE, FAKE, FAKE, 10, None) == UNSUP
+    assert f(FAKE, FAKE, 1, 128, FAKE, 2048, 0, FAKE, FAKE, FAKE, 10, None) == UNSUP
+    assert f(None, FAKE, 1, 128, FAKE, 4, 0, FAKE, FAKE, FAKE, 10, None) == ARG
+    assert f(FAKE + 8, FAKE, 1, 128, FAKE, 4, 0, FAKE, FAKE, FAKE, 10, None) == ARG
+    assert f(FAKE, FAKE, 8, 128, FAKE, 4, 36, FAKE, FAKE, FAKE, 10, None) == CAP   # rows up to 11 > 10
+    assert f(None, None, 0, 128, None, 4, 0, None, None, None, 0, None) == 0       # n_new = 0: no-op
+
+
+def test_indexer_validation(ds4a_lib):
+    L = ds4a_lib.lib()
+    f = L.ds4a_indexer_topk
+    nb = L.ds4a_indexer_workspace_bytes(1, 8192, 512)
+    assert nb >= 8192 * 4
+    assert f(FAKE, 1, FAKE, 8192, 128, 32768, 4, 0, FAKE, FAKE, FAKE, nb, None) == ARG      # k = 0
+    assert f(FAKE, 1, FAKE, 8192, 100, 32768, 4, 512, FAKE, FAKE, FAKE, nb, None) == UNSUP  # d_idx
+    assert f(FAKE, 1, FAKE, 8192, 128, 32768, 4, 4096, FAKE, FAKE, FAKE, nb, None) == UNSUP  # k too big
+    assert f(FAKE, 1, FAKE, 8192, 128, 32768, 0, 512, FAKE, FAKE, FAKE, nb, None) == ARG    # ratio
+    assert f(FAKE, 1, FAKE, 8192, 128, 32768, 4, 512, FAKE, FAKE, None, nb, None) == WS     # no ws
+    assert f(FAKE, 1, FAKE, 8192, 128, 32768, 4, 512, FAKE, FAKE, FAKE, nb - 1, None) == WS
+    assert f(FAKE + 4, 1, FAKE, 8192, 128, 32768, 4, 512, FAKE, FAKE, FAKE, nb, None) == ARG
+    assert f(None, 0, None, 0, 128, 0, 4, 512, None, None, None, 0, None) == 0            # n_q = 0
+
+
+def test_attn_decode_validation(ds4a_lib):
+    L = ds4a_lib.lib()
+    f = L.ds4a_attn_decode
+    s = ctypes.c_float(0.088)
+    assert f(FAKE, 64, 96, FAKE, FAKE, 128, FAKE, FAKE, 100, FAKE, 512, s, FAKE, None, 0, None) == UNSUP
+    assert f(FAKE, 60, 128, FAKE, FAKE, 128, FAKE, FAKE, 100, FAKE, 512, s, FAKE, None, 0, None) == UNSUP
+    assert f(FAKE, 128, 128, FAKE, FAKE, 128, FAKE, FAKE, 100, FAKE, 512, s, FAKE, None, 0, None) == UNSUP
+    assert f(FAKE, 64, 128, FAKE, FAKE, 0, FAKE, FAKE, 100, FAKE, 512, s, FAKE, None, 0, None) == ARG
+    assert f(FAKE, 64, 128, FAKE, FAKE, 128, None, FAKE, 100, FAKE, 512, s, FAKE, None, 0, None) == ARG
+    # sel = NULL means rows 0..n_sel-1: n_sel may not exceed n_comp
+    assert f(FAKE, 64, 128, FAKE, FAKE, 128, FAKE, FAKE, 100, None, 101, s, FAKE, None, 0, None) == ARG
+    assert f(FAKE, 64, 128, FAKE + 8, FAKE, 128, FAKE, FAKE, 100, None, 10, s, FAKE, None, 0, None) == ARG
+
+
+def test_attn_prefill_validation(ds4a_lib):
+    L = ds4a_lib.lib()
+    f = L.ds4a_attn_prefill
+    s = ctypes.c_float(0.088)
+    # n_prior must cover the window: min(window-1, q_pos0) rows
+    assert f(FAKE, 16, 64, 128, FAKE, FAKE, 100, 128, FAKE, FAKE, 10, None, 0, 1000, 4, s, FAKE, None, 0,
+             None) == ARG
+    assert f(FAKE, 16, 64, 128, FAKE, FAKE, 20, 128, FAKE, FAKE, 10, None, 0, 10, 4, s, FAKE, None, 0,
+             None) == ARG   # n_prior > q_pos0
+    assert f(FAKE, 16, 64, 128, FAKE, FAKE, 127, 128, FAKE, FAKE, 10, FAKE, 0, 1000, 4, s, FAKE, None, 0,
+             None) == ARG   # sel with k_stride 0
+    assert f(FAKE, 16, 64, 64 + 8, FAKE, FAKE, 127, 128, FAKE, FAKE, 10, None, 0, 1000, 4, s, FAKE, None, 0,
+             None) == UNSUP
+    assert f(None, 0, 64, 128, None, None, 0, 128, None, None, 0, None, 0, 0, 4, s, None, None, 0,
+             None) == 0     # T = 0: no-op

@@ -1,0 +1,285 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Every test draws seeded synthetic inputs, runs the library's kernels on cuda:0
+and compares with the oracle on the same inputs: outputs within max abs 2e-3 and
+normwise rel 1e-2; kept indexer rows bit-exact up to near-ties (1e-6 relative of
+the k-th score).  Full-size configurations are compared on every output where
+the oracle is fast (decode) and on sampled queries where it is not (prefill).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from compressed_sparse_mqa_gb300 import configs, ds4a, synth
+from compressed_sparse_mqa_gb300.layer import DecodeLayer, PrefillLayer
+from parity import check_out, check_sel
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(ds4a_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    ds4a.ds4a_last_device_error()
+    yield
+    torch.cuda.synchronize()
+
+
+def h(t):
+    return t.detach().cpu().numpy()
+
+
+def check_decode(inst, L=None):
+    L = L or DecodeLayer(inst)
+    out = L.step()
+    torch.cuda.synchronize()
+    ref = oracle.decode_step(inst)
+    if inst.ratio and ref["comp_k"] is not None and ref["comp_k"].shape[0]:
+        n = ref["comp_k"].shape[0]
+        check_out(h(L.comp_k)[:n], ref["comp_k"], "comp_k")
+        check_out(h(L.comp_v)[:n], ref["comp_v"], "comp_v")
+    if inst.topk:
+        scores = oracle.index_scores(inst.q_idx, inst.kidx[: ref["n_vis"]])
+        check_sel(h(L.sel), ref["sel"], scores, inst.topk)
+        assert int(L.sel_n.item()) == min(inst.topk, ref["n_vis"])
+        assert (h(L.sel)[int(L.sel_n.item()):] == -1).all()
+    check_out(h(out), ref["out"])
+    assert ds4a.ds4a_last_device_error() == 0
+    return L, ref
+
+
+# ---- the five configurations ---------------------------------------------------------
+
+def test_c1_tiny_even_layer_decode():
+    inst = configs.decode(configs.C1)
+    L, ref = check_decode(inst)
+    assert ref["n_vis"] == 128 and len(ref["sel"]) == 16
+    # the compressor produced all 128 rows from the raw tokens on the GPU
+    assert np.abs(h(L.comp_k)).max() > 0
+
+
+def test_c2_decode_ratio4_indexer():
+    check_decode(configs.decode(configs.C2))
+
+
+def test_c3_decode_ratio128_all_rows():
+    check_decode(configs.decode(configs.C3))
+
+
+def test_c3_decode_step_that_emits_a_row():
+    inst = configs.decode(configs.C3_EMIT)
+    L, ref = check_decode(inst)
+    # row 1023 was pooled by this step from the 127 earlier tokens plus the current one
+    check_out(h(L.comp_k)[1023], ref["comp_k"][1023], "row 1023 K")
+    check_out(h(L.comp_v)[1023], ref["comp_v"][1023], "row 1023 V")
+
+
+def test_c4_prefill_chunk_sampled():
+    inst = configs.prefill(configs.C4)
+    L = PrefillLayer(inst)
+    L.step()
+    torch.cuda.synchronize()
+    P, T, r = inst.P, inst.T, inst.ratio
+    # new pooled rows 7680 .. 8191
+    nk, nv = oracle.compress_range(inst.raw_k, inst.raw_v, P - inst.n_prior, inst.w, r, P // r, (P + T) // r)
+    check_out(h(L.comp_k)[P // r:], nk, "new comp_k")
+    check_out(h(L.comp_v)[P // r:], nv, "new comp_v")
+    comp_k = np.concatenate([inst.comp_k.astype(np.float64), nk])
+    comp_v = np.concatenate([inst.comp_v.astype(np.float64), nv])
+    rng = np.random.default_rng(0)
+    sample = sorted(set([0, 1, 2, 3, 511, 1023, 1024, T - 2, T - 1] + list(rng.integers(0, T, 7))))
+    sel_gpu, out_gpu = h(L.sel), h(L.out)
+    for i in sample:
+        p = P + i
+        n_vis = (p + 1) // r
+        idx, cnt = oracle.indexer(inst.q_idx[i:i + 1], inst.kidx, p, r, inst.topk)
+        scores = oracle.index_scores(inst.q_idx[i], inst.kidx[:n_vis])
+        check_sel(sel_gpu[i], idx[0, : cnt[0]], scores, inst.topk, f"sel[{i}]")
+        ref = oracle.decode_attend(inst.q[i], p, inst.window, inst.raw_k, inst.raw_v, P - inst.n_prior,
+                                   comp_k, comp_v, idx[0], inst.topk, inst.scale)
+        check_out(out_gpu[i], ref, f"out[{i}]")
+    assert ds4a.ds4a_last_device_error() == 0
+
+
+def test_c5_full_43_layer_stack():
+    for layer in range(configs.C5_LAYERS):
+        inst = configs.decode(configs.c5_layer_params(layer))
+        check_decode(inst)
+
+
+# ---- smaller prefill chunks, checked on every output ---------------------------------------
+
+@pytest.mark.parametrize("ratio,topk,P,T,W", [(4, 16, 200, 96, 32), (4, 512, 2100, 130, 128),
+                                              (128, 0, 300, 200, 128), (0, 0, 50, 77, 128),
+                                              (4, 16, 0, 40, 32), (128, 0, 1000, 257, 64)])
+def test_prefill_small_full(ratio, topk, P, T, W):
+    inst = synth.prefill_instance(seed=11, layer=ratio, H=64, D=128, window=W, ratio=ratio, d_idx=128,
+                                  topk=topk, P=P, T=T, sigma_w=configs.SIGMA_W)
+    L = PrefillLayer(inst)
+    L.step()
+    torch.cuda.synchronize()
+    ref = oracle.prefill_chunk(inst)
+    if ratio:
+        n0 = P // ratio
+        check_out(h(L.comp_k)[n0:], ref["new_k"], "new comp_k")
+        check_out(h(L.comp_v)[n0:], ref["new_v"], "new comp_v")
+    if topk:
+        sel = h(L.sel)
+        for i in range(T):
+            n_vis = (P + i + 1) // ratio
+            scores = oracle.index_scores(inst.q_idx[i], inst.kidx[:n_vis])
+            check_sel(sel[i], ref["sel"][i, : ref["sel_n"][i]], scores, topk, f"sel[{i}]")
+        assert np.array_equal(h(L.sel_n), ref["sel_n"])
+    check_out(h(L.out), ref["out"])
+    assert ds4a.ds4a_last_device_error() == 0
+
+
+# ---- decode edge cases ------------------------------------------------------------------------
+
+@pytest.mark.parametrize("p", [0, 2, 3, 17, 40, 131])
+def test_decode_early_positions(p):
+    # window not yet full, no or few compressed rows, k larger than the visible rows
+    check_decode(synth.decode_instance(**dict(configs.C1, p=p)))
+
+
+@pytest.mark.parametrize("H,D", [(8, 64), (64, 64), (8, 128), (24, 128), (64, 128)])
+def test_decode_head_shapes(H, D):
+    check_decode(synth.decode_instance(seed=5, layer=1, H=H, D=D, window=64, ratio=4, d_idx=64, topk=32,
+                                       p=1000, sigma_w=0.1))
+
+
+def test_decode_window_only_layer():
+    check_decode(configs.decode(configs.c5_layer_params(0, context=5000)))
+
+
+def test_decode_ratio128_block_boundaries():
+    for p in [127, 128, 255, 383, 1000]:
+        check_decode(synth.decode_instance(seed=2, layer=3, H=64, D=128, window=128, ratio=128, d_idx=128,
+                                           topk=0, p=p, pooled_history=True, sigma_w=configs.SIGMA_W))
+
+
+def test_attn_decode_skips_padding_and_flags_bad_rows():
+    inst = configs.decode(dict(configs.C2, p=4000))
+    L = DecodeLayer(inst)
+    L.step()
+    torch.cuda.synchronize()
+    sel = h(L.sel).copy()
+    n_comp = L.comp_k.shape[0]
+    bad = sel.copy()
+    bad[5] = -1
+    bad[9] = n_comp + 7          # out of range: skipped and recorded
+    bad_t = torch.from_numpy(bad).cuda()
+    out = torch.empty_like(L.out)
+    ds4a.ds4a_attn_decode(L.q, L.ring_k[: L.n_win], L.ring_v[: L.n_win], L.comp_k, L.comp_v, bad_t,
+                          len(bad), L.scale, out)
+    assert ds4a.ds4a_last_device_error() == ds4a.DS4A_ERR_DEVICE_INDEX
+    assert ds4a.ds4a_last_device_error() == 0          # cleared by the read
+    keep = bad.copy()
+    keep[9] = -1
+    ref = oracle.decode_attend(inst.q, inst.p, inst.window, inst.raw_k, inst.raw_v, inst.raw_pos0,
+                               inst.comp_k, inst.comp_v, keep, len(keep), inst.scale)
+    check_out(h(out), ref)
+
+
+# ---- indexer edge cases --------------------------------------------------------------------------
+
+def _indexer_gpu(q_idx, kidx, q_pos0, ratio, k):
+    q = torch.from_numpy(np.ascontiguousarray(q_idx)).cuda()
+    kk = torch.from_numpy(np.ascontiguousarray(kidx)).cuda()
+    n_q = q.shape[0] if q.dim() == 2 else 1
+    out = torch.full((n_q, k), -7, dtype=torch.int32, device="cuda")
+    out_n = torch.zeros(n_q, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(ds4a.ds4a_indexer_workspace_bytes(n_q, kk.shape[0], k), dtype=torch.uint8, device="cuda")
+    ds4a.ds4a_indexer_topk(q, kk, q_pos0, ratio, k, out, out_n, ws)
+    torch.cuda.synchronize()
+    return h(out), h(out_n), ws
+
+
+def test_indexer_ties_go_to_lower_index():
+    rng = np.random.default_rng(3)
+    base = rng.standard_normal((40, 16)).astype(np.float16)
+    kidx = np.concatenate([base, base, base[:20]])          # every score appears 2-3 times
+    q = rng.standard_normal(16).astype(np.float16)
+    for k in [1, 7, 40, 63, 99]:
+        out, n, _ = _indexer_gpu(q, kidx, 4 * 100, 4, k)
+        ref = oracle.topk(oracle.index_scores(q, kidx), k)
+        assert n[0] == len(ref)
+        assert np.array_equal(out[0, : n[0]], ref), k
+
+
+def test_indexer_large_row_counts_use_global_keys():
+    rng = np.random.default_rng(4)
+    for n_rows in [24577, 40000]:
+        kidx = rng.standard_normal((n_rows, 128)).astype(np.float16)
+        q = rng.standard_normal((1, 128)).astype(np.float16)
+        out, n, ws = _indexer_gpu(q, kidx, 4 * n_rows + 3, 4, 512)
+        scores = oracle.index_scores(q[0], kidx)
+        check_sel(out[0], oracle.topk(scores, 512), scores, 512)
+        # the decode ticket is back at zero for the next call
+        assert int(ws[:4].view(torch.int32).item()) == 0
+    # many queries with more visible rows than shared memory holds
+    kidx = rng.standard_normal((30000, 64)).astype(np.float16)
+    q = rng.standard_normal((3, 64)).astype(np.float16)
+    out, n, _ = _indexer_gpu(q, kidx, 4 * 29990, 4, 100)
+    for i in range(3):
+        n_vis = min(30000, (4 * 29990 + i + 1) // 4)
+        scores = oracle.index_scores(q[i], kidx[:n_vis])
+        check_sel(out[i], oracle.topk(scores, 100), scores, 100, f"q{i}")
+
+
+def test_indexer_k_exceeds_visible_rows():
+    rng = np.random.default_rng(5)
+    kidx = rng.standard_normal((500, 32)).astype(np.float16)
+    q = rng.standard_normal((4, 32)).astype(np.float16)
+    out, n, _ = _indexer_gpu(q, kidx, 397, 4, 512)      # 99 .. 100 rows visible
+    for i in range(4):
+        n_vis = (397 + i + 1) // 4
+        assert n[i] == n_vis
+        assert np.array_equal(out[i, :n_vis], np.arange(n_vis))
+        assert (out[i, n_vis:] == -1).all()
+
+
+def test_indexer_repeated_calls_reuse_workspace():
+    inst = configs.decode(configs.C2)
+    L = DecodeLayer(inst)
+    L.step()
+    first = h(L.sel).copy()
+    for _ in range(5):
+        L.step()
+    torch.cuda.synchronize()
+    assert np.array_equal(h(L.sel), first)
+
+
+# ---- compressor: chunk-split invariance and online == blockwise ----------------------------------
+
+@pytest.mark.parametrize("ratio", [4, 128])
+def test_compressor_chunk_split_and_token_by_token(ratio):
+    rng = np.random.default_rng(6)
+    D, n = 128, 700
+    k = rng.standard_normal((n, D)).astype(np.float16)
+    v = rng.standard_normal((n, D)).astype(np.float16)
+    w = (rng.standard_normal(D) * configs.SIGMA_W).astype(np.float32)
+    ref_k, ref_v = oracle.compress_range(k, v, 0, w, ratio, 0, n // ratio)
+    kt, vt, wt = (torch.from_numpy(x).cuda() for x in (k, v, w))
+
+    def run(splits):
+        ck = torch.zeros(n // ratio, D, dtype=torch.float16, device="cuda")
+        cv = torch.zeros_like(ck)
+        st = torch.zeros(2 + 2 * D, dtype=torch.float32, device="cuda")
+        pos = 0
+        for s in splits:
+            ds4a.ds4a_compress_append(kt[pos:pos + s], vt[pos:pos + s], wt, ratio, pos, st, ck, cv)
+            pos += s
+        torch.cuda.synchronize()
+        return h(ck), h(cv)
+
+    whole = run([n])
+    chunks = run([1, 130, 255, 314])
+    tokens = run([1] * n)
+    for got in (whole, chunks, tokens):
+        check_out(got[0], ref_k, "rows K")
+        check_out(got[1], ref_v, "rows V")
+    np.testing.assert_allclose(chunks[0].astype(np.float32), whole[0].astype(np.float32), atol=2e-3)
+    np.testing.assert_allclose(tokens[1].astype(np.float32), whole[1].astype(np.float32), atol=2e-3)
