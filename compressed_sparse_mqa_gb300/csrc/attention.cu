@@ -5,21 +5,26 @@
 // For each head h: o_h = sum_j softmax_j(scale * q_h . K_j) V_j over the union of
 // the window rows and the selected (or all visible) compressed rows.
 //
-// Tile engine (shared by decode and prefill).  A CTA of 4 warps walks a list of
+// Tile engine (shared by decode and prefill).  A CTA of 8 warps walks a list of
 // "virtual rows" (window rows first, then compressed rows through `sel`) in
 // tiles of 64.  Each tile's K and V rows are gathered with 16-byte cp.async into
 // a double-buffered, XOR-swizzled shared-memory tile.  Warp w owns heads
-// 16w .. 16w+15 (the 64 heads of one query are the M dimension: they all share
-// each K/V row, 64 flop per byte), computes S = Q K^T and O += P V with
-// mma.sync m16n8k16 (fp16 in, fp32 accumulate), and keeps an online softmax in
-// the log2 domain.  Rows that are padding (negative sel entries, or past the
-// list) get -inf logits and zero-filled K/V.
+// 16(w%4) .. 16(w%4)+15 (the 64 heads of one query are the M dimension: they
+// all share each K/V row, 64 flop per byte) and keys 32(w/4) .. +31 of each
+// tile; it computes S = Q K^T and O += P V with mma.sync m16n8k16 (fp16 in,
+// fp32 accumulate) and keeps an online softmax in the log2 domain.  16-key
+// groups past the end of the list are skipped; rows that are padding (negative
+// sel entries) get -inf logits and zero-filled K/V.  The two key halves of a
+// head group are combined through shared memory at the end.
 //
 // Decode: one query, rows split across one thread-block cluster of 16 CTAs (8
-// if 16 cannot be scheduled); each CTA leaves (m, l, O) for its rows in shared
-// memory, the cluster barrier publishes them, and CTA c merges heads
-// c*H/16 .. by log-sum-exp, reading the partials through distributed shared
-// memory.  No workspace, no second launch, no spin.
+// if 16 cannot be scheduled).  Each CTA stores its (m, l, O) of head h straight
+// into the shared memory of the CTA that owns h (distributed shared memory),
+// one cluster barrier publishes the stores, and each CTA merges its own heads
+// by log-sum-exp from local shared memory.  A relaxed cluster arrive at kernel
+// start, waited on just before the first remote store, guarantees every peer
+// is running.  Window rows are cache state and are gathered before waiting on
+// the previous kernel.  No workspace, no second launch, no spin.
 // Prefill: one CTA per query walks the query's whole row list.
 #include <cooperative_groups.h>
 
@@ -31,9 +36,9 @@ namespace cg = cooperative_groups;
 namespace ds4a {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;    // 8 warps: 4 head groups x 2 key halves
 constexpr int kBN = 64;           // rows per tile
-constexpr int kMaxHeads = 64;
+constexpr int kHalf = kBN / 2;    // keys per warp per tile
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Where the virtual rows live: v < n_w -> window row wk/wv + v*D; otherwise the
@@ -55,6 +60,7 @@ struct Smem {
     uint16_t k[2][kBN * D];
     uint16_t v[2][kBN * D];
     long long off[2][kBN];   // element offset of the row in the window (>=0, tagged) / comp arrays; -1 = padding
+    int nvalid[2];           // rows of the tile inside the list (the rest is padding)
 };
 
 // Row offset encoding: bit 62 set -> window row.
@@ -67,8 +73,9 @@ DS4A_DEVINL uint32_t swz(int r, int ch) {
 }
 
 template <int D>
-DS4A_DEVINL void build_table(const RowSrc &s, int v0, int v_end, long long *off) {
+DS4A_DEVINL void build_table(const RowSrc &s, int v0, int v_end, long long *off, int *nvalid) {
     const int t = threadIdx.x;
+    if (t == 0) *nvalid = min(kBN, v_end - v0);
     if (t < kBN) {
         const int v = v0 + t;
         long long o = -1;
@@ -132,38 +139,44 @@ DS4A_DEVINL void load_q_frags(const uint16_t *q, int H, int h0, uint32_t (&qa)[D
     }
 }
 
-// One tile: S = Q K^T, online softmax, O += P V.
+// One tile, keys kh*32 .. kh*32+31 of it: S = Q K^T, online softmax, O += P V.
 template <int D>
 DS4A_DEVINL void compute_tile(const uint32_t (&qa)[D / 16][4], const uint16_t *kt, const uint16_t *vt,
-                              const long long *off, float scale_log2, WarpState<D> &st) {
+                              const long long *off, int nvalid, int kh, float scale_log2, WarpState<D> &st) {
     const int lane = threadIdx.x & 31, t = lane & 3;
+    const int kbase = kh * kHalf;
+    if (kbase >= nvalid) return;                                  // warp-uniform
+    const int groups = min(2, (nvalid - kbase + 15) / 16);        // 16-key groups holding list rows
     const unsigned char *kb = reinterpret_cast<const unsigned char *>(kt);
     const unsigned char *vb = reinterpret_cast<const unsigned char *>(vt);
-    float s[kBN / 8][4];
+    float s[kHalf / 8][4];
 #pragma unroll
-    for (int nt = 0; nt < kBN / 8; ++nt)
+    for (int nt = 0; nt < kHalf / 8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
 
-    // S = Q K^T: ldmatrix x4 gives b0/b1 for two key tiles at one k-step
+    // S = Q K^T: ldmatrix x4 gives b0/b1 for two key tiles (one 16-key group) at one k-step
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
-        for (int nt = 0; nt < kBN / 8; nt += 2) {
-            const int key = nt * 8 + (lane & 7) + ((lane >> 4) << 3);
-            const int ch = 2 * ks + ((lane >> 3) & 1);
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4(b0, b1, b2, b3, kb + swz<D>(key, ch));
-            mma_16816(s[nt], qa[ks], b0, b1);
-            mma_16816(s[nt + 1], qa[ks], b2, b3);
+        for (int gq = 0; gq < 2; ++gq) {
+            if (gq < groups) {
+                const int key = kbase + gq * 16 + (lane & 7) + ((lane >> 4) << 3);
+                const int ch = 2 * ks + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(b0, b1, b2, b3, kb + swz<D>(key, ch));
+                mma_16816(s[2 * gq], qa[ks], b0, b1);
+                mma_16816(s[2 * gq + 1], qa[ks], b2, b3);
+            }
         }
     }
 
     // scale into the log2 domain, mask padding rows, running max
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < kBN / 8; ++nt) {
-        const bool v0 = off[nt * 8 + 2 * t] >= 0, v1 = off[nt * 8 + 2 * t + 1] >= 0;
+    for (int nt = 0; nt < kHalf / 8; ++nt) {
+        const int kr = kbase + nt * 8 + 2 * t;
+        const bool v0 = off[kr] >= 0, v1 = off[kr + 1] >= 0;
         s[nt][0] = v0 ? s[nt][0] * scale_log2 : -INFINITY;
         s[nt][1] = v1 ? s[nt][1] * scale_log2 : -INFINITY;
         s[nt][2] = v0 ? s[nt][2] * scale_log2 : -INFINITY;
@@ -192,9 +205,9 @@ DS4A_DEVINL void compute_tile(const uint32_t (&qa)[D / 16][4], const uint16_t *k
         st.o[dn][2] *= alpha[1];
         st.o[dn][3] *= alpha[1];
     }
-    uint32_t pa[kBN / 16][4];
+    uint32_t pa[kHalf / 16][4];
 #pragma unroll
-    for (int nt = 0; nt < kBN / 8; ++nt) {
+    for (int nt = 0; nt < kHalf / 8; ++nt) {
         const float p0 = exp2f(s[nt][0] - ref[0]), p1 = exp2f(s[nt][1] - ref[0]);
         const float p2 = exp2f(s[nt][2] - ref[1]), p3 = exp2f(s[nt][3] - ref[1]);
         st.l[0] += p0 + p1;
@@ -203,36 +216,43 @@ DS4A_DEVINL void compute_tile(const uint32_t (&qa)[D / 16][4], const uint16_t *k
         pa[kk][hi ? 2 : 0] = pack_half2(p0, p1);
         pa[kk][hi ? 3 : 1] = pack_half2(p2, p3);
     }
-    // O += P V: ldmatrix.trans x4 gives b0/b1 for two d tiles at one key step
+    // O += P V: ldmatrix.trans x4 gives b0/b1 for two d tiles at one 16-key step
 #pragma unroll
-    for (int kk = 0; kk < kBN / 16; ++kk) {
+    for (int kk = 0; kk < kHalf / 16; ++kk) {
+        if (kk < groups) {
 #pragma unroll
-        for (int dn = 0; dn < D / 8; dn += 2) {
-            const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-            const int ch = dn + (lane >> 4);
-            uint32_t b0, b1, b2, b3;
-            ldmatrix_x4_trans(b0, b1, b2, b3, vb + swz<D>(key, ch));
-            mma_16816(st.o[dn], pa[kk], b0, b1);
-            mma_16816(st.o[dn + 1], pa[kk], b2, b3);
+            for (int dn = 0; dn < D / 8; dn += 2) {
+                const int key = kbase + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                const int ch = dn + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4_trans(b0, b1, b2, b3, vb + swz<D>(key, ch));
+                mma_16816(st.o[dn], pa[kk], b0, b1);
+                mma_16816(st.o[dn + 1], pa[kk], b2, b3);
+            }
         }
     }
 }
 
-// Walk virtual rows [v_begin, v_end) of `src`, accumulating into `st`.
+// Walk virtual rows [v_begin, v_end) of `src`, accumulating into `st`.  If
+// `tile0_issued`, the caller has already built the first tile's table and
+// issued (and committed) its loads.
 template <int D>
 __device__ void attend_range(const RowSrc &src, int v_begin, int v_end, const uint32_t (&qa)[D / 16][4],
-                             bool has_heads, float scale_log2, Smem<D> &sm, WarpState<D> &st) {
+                             bool has_heads, int kh, float scale_log2, Smem<D> &sm, WarpState<D> &st,
+                             bool tile0_issued) {
     const int n_tiles = v_end > v_begin ? (v_end - v_begin + kBN - 1) / kBN : 0;
     if (n_tiles == 0) return;
-    build_table<D>(src, v_begin, v_end, sm.off[0]);
-    __syncthreads();
-    issue_loads<D>(src, sm.off[0], sm.k[0], sm.v[0]);
-    cp_async_commit();
+    if (!tile0_issued) {
+        build_table<D>(src, v_begin, v_end, sm.off[0], &sm.nvalid[0]);
+        __syncthreads();
+        issue_loads<D>(src, sm.off[0], sm.k[0], sm.v[0]);
+        cp_async_commit();
+    }
     for (int it = 0; it < n_tiles; ++it) {
         __syncthreads();
         if (it + 1 < n_tiles) {
             const int b = (it + 1) & 1;
-            build_table<D>(src, v_begin + (it + 1) * kBN, v_end, sm.off[b]);
+            build_table<D>(src, v_begin + (it + 1) * kBN, v_end, sm.off[b], &sm.nvalid[b]);
             __syncthreads();
             issue_loads<D>(src, sm.off[b], sm.k[b], sm.v[b]);
         }
@@ -240,7 +260,7 @@ __device__ void attend_range(const RowSrc &src, int v_begin, int v_end, const ui
         cp_async_wait<1>();
         __syncthreads();
         const int b = it & 1;
-        if (has_heads) compute_tile<D>(qa, sm.k[b], sm.v[b], sm.off[b], scale_log2, st);
+        if (has_heads) compute_tile<D>(qa, sm.k[b], sm.v[b], sm.off[b], sm.nvalid[b], kh, scale_log2, st);
     }
     __syncthreads();
 }
@@ -255,6 +275,47 @@ DS4A_DEVINL void init_state(WarpState<D> &st) {
     st.l[0] = st.l[1] = 0.f;
 }
 
+// Combine the two key halves of each head group: warps 4..7 hand their state
+// to warps 0..3 through shared memory (`xch` must hold 4*32*(D/2+4) floats).
+template <int D>
+DS4A_DEVINL void combine_halves(WarpState<D> &st, float *xch) {
+    constexpr int kStride = D / 2 + 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= 4) {
+        float *p = xch + ((warp - 4) * 32 + lane) * kStride;
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p[dn * 4 + e] = st.o[dn][e];
+        p[D / 2 + 0] = st.m[0];
+        p[D / 2 + 1] = st.m[1];
+        p[D / 2 + 2] = st.l[0];
+        p[D / 2 + 3] = st.l[1];
+    }
+    __syncthreads();
+    if (warp < 4) {
+        const float *p = xch + (warp * 32 + lane) * kStride;
+        float wa[2], wb[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const float mb = p[D / 2 + r];
+            const float M = fmaxf(st.m[r], mb);
+            wa[r] = st.m[r] == -INFINITY ? 0.f : exp2f(st.m[r] - M);
+            wb[r] = mb == -INFINITY ? 0.f : exp2f(mb - M);
+            st.l[r] = st.l[r] * wa[r] + p[D / 2 + 2 + r] * wb[r];
+            st.m[r] = M;
+        }
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+            st.o[dn][0] = st.o[dn][0] * wa[0] + p[dn * 4 + 0] * wb[0];
+            st.o[dn][1] = st.o[dn][1] * wa[0] + p[dn * 4 + 1] * wb[0];
+            st.o[dn][2] = st.o[dn][2] * wa[1] + p[dn * 4 + 2] * wb[1];
+            st.o[dn][3] = st.o[dn][3] * wa[1] + p[dn * 4 + 3] * wb[1];
+        }
+    }
+    __syncthreads();
+}
+
 // quad-reduce the per-lane partial sums of l
 template <int D>
 DS4A_DEVINL void finish_l(WarpState<D> &st) {
@@ -265,6 +326,10 @@ DS4A_DEVINL void finish_l(WarpState<D> &st) {
     }
 }
 
+DS4A_DEVINL void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory"); }
+DS4A_DEVINL void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
+DS4A_DEVINL void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
+
 struct DecodeArgs {
     const uint16_t *q;
     uint16_t *out;
@@ -274,77 +339,99 @@ struct DecodeArgs {
     float scale_log2;
 };
 
+constexpr int kRecvRows = 80;   // >= cluster size * ceil(H / cluster size) for H <= 64
+
 template <int D>
-struct DecodePartial {
-    float o[kMaxHeads][D];
-    float m[kMaxHeads];
-    float l[kMaxHeads];
-};
+__host__ __device__ constexpr size_t recv_offset() { return (sizeof(Smem<D>) + 127) / 128 * 128; }
+template <int D>
+constexpr size_t decode_smem() { return recv_offset<D>() + kRecvRows * (D + 4) * sizeof(float); }
+template <int D>
+constexpr size_t prefill_smem() { return sizeof(Smem<D>); }
+static_assert(4 * 32 * (128 / 2 + 4) * sizeof(float) <= sizeof(Smem<128>), "exchange fits in the tiles");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
+    float *recv = reinterpret_cast<float *>(smem_raw + recv_offset<D>());
     cg::cluster_group cluster = cg::this_cluster();
-    const unsigned cs = cluster.num_blocks();
-    const unsigned rank = cluster.block_rank();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int h0 = warp * 16;
-    const bool has_heads = h0 < a.H;
+    const int cs = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
+    cluster_arrive_relaxed();   // this CTA is running; waited on before the first remote store
 
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int h0 = (warp & 3) * 16, kh = warp >> 2;
+    const bool has_heads = h0 < a.H;
+    const int chunk = (a.n_rows + cs - 1) / cs;
+    const int v0 = min(a.n_rows, rank * chunk);
+    const int v1 = min(a.n_rows, v0 + chunk);
+    // a first tile of window rows only (cache state) is gathered before the dependency wait
+    const bool pre = v1 > v0 && min(v1, v0 + kBN) <= a.src.n_w;
+    if (pre) {
+        build_table<D>(a.src, v0, v1, sm.off[0], &sm.nvalid[0]);
+        __syncthreads();
+        issue_loads<D>(a.src, sm.off[0], sm.k[0], sm.v[0]);
+        cp_async_commit();
+    }
     pdl_wait();
     pdl_trigger();
     uint32_t qa[D / 16][4];
     load_q_frags<D>(a.q, a.H, h0, qa);
     WarpState<D> st;
     init_state<D>(st);
-    const int chunk = (a.n_rows + cs - 1) / cs;
-    const int v0 = min(a.n_rows, static_cast<int>(rank) * chunk);
-    const int v1 = min(a.n_rows, v0 + chunk);
-    attend_range<D>(a.src, v0, v1, qa, has_heads, a.scale_log2, sm, st);
+    attend_range<D>(a.src, v0, v1, qa, has_heads, kh, a.scale_log2, sm, st, pre);
+    combine_halves<D>(st, reinterpret_cast<float *>(smem_raw));
     finish_l<D>(st);
 
-    // partial (m, l, O) of this CTA's rows, in shared memory (reuses the tiles)
-    DecodePartial<D> &part = *reinterpret_cast<DecodePartial<D> *>(smem_raw);
-    if (has_heads) {
+    // push (O, m, l) of each head to the CTA that owns it: recv[src rank][local head][D + 4]
+    const int hpc = (a.H + cs - 1) / cs;
+    cluster_wait();
+    if (warp < 4 && has_heads) {
 #pragma unroll
-        for (int dn = 0; dn < D / 8; ++dn) {
-            const int d = dn * 8 + 2 * t;
-            part.o[h0 + g][d] = st.o[dn][0];
-            part.o[h0 + g][d + 1] = st.o[dn][1];
-            part.o[h0 + g + 8][d] = st.o[dn][2];
-            part.o[h0 + g + 8][d + 1] = st.o[dn][3];
-        }
-        if (t == 0) {
-            part.m[h0 + g] = st.m[0];
-            part.l[h0 + g] = st.l[0];
-            part.m[h0 + g + 8] = st.m[1];
-            part.l[h0 + g + 8] = st.l[1];
+        for (int r = 0; r < 2; ++r) {
+            const int h = h0 + g + 8 * r;
+            if (h < a.H) {
+                const int owner = h / hpc;
+                float *dst = cluster.map_shared_rank(recv, owner) + (rank * hpc + (h - owner * hpc)) * (D + 4);
+#pragma unroll
+                for (int dn = 0; dn < D / 8; ++dn)
+                    *reinterpret_cast<float2 *>(dst + dn * 8 + 2 * t) = make_float2(st.o[dn][2 * r], st.o[dn][2 * r + 1]);
+                if (t == 0) {
+                    dst[D] = st.m[r];
+                    dst[D + 1] = st.l[r];
+                }
+            }
         }
     }
-    cluster.sync();
+    cluster_arrive_release();
+    cluster_wait();
 
-    // merge: this CTA owns heads [hb, he)
-    const int hpc = (a.H + static_cast<int>(cs) - 1) / static_cast<int>(cs);
-    const int hb = static_cast<int>(rank) * hpc, he = min(a.H, hb + hpc);
-    for (int idx = threadIdx.x; idx < (he - hb) * D; idx += kThreads) {
-        const int h = hb + idx / D, d = idx % D;
+    // merge this CTA's heads from local shared memory
+    const int hb = rank * hpc;
+    const int nh = max(0, min(a.H, hb + hpc) - hb);
+    for (int idx = threadIdx.x; idx < nh * (D / 4); idx += kThreads) {
+        const int hh = idx / (D / 4), d = (idx % (D / 4)) * 4;
         float M = -INFINITY;
-        for (unsigned r = 0; r < cs; ++r) {
-            const DecodePartial<D> *pr = cluster.map_shared_rank(&part, r);
-            M = fmaxf(M, pr->m[h]);
-        }
-        float num = 0.f, den = 0.f;
-        for (unsigned r = 0; r < cs; ++r) {
-            const DecodePartial<D> *pr = cluster.map_shared_rank(&part, r);
-            const float mr = pr->m[h];
+        for (int r = 0; r < cs; ++r) M = fmaxf(M, recv[(r * hpc + hh) * (D + 4) + D]);
+        float den = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < cs; ++r) {
+            const float *row = recv + (r * hpc + hh) * (D + 4);
+            const float mr = row[D];
             const float w = mr == -INFINITY ? 0.f : exp2f(mr - M);
-            num += w * pr->o[h][d];
-            den += w * pr->l[h];
+            den = fmaf(w, row[D + 1], den);
+            const float4 o = *reinterpret_cast<const float4 *>(row + d);
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
         }
-        a.out[h * D + d] = f2h(num / den);
+        const float inv = 1.f / den;
+        uint2 packed;
+        packed.x = pack_half2(acc.x * inv, acc.y * inv);
+        packed.y = pack_half2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(a.out + (hb + hh) * D + d) = packed;
     }
-    cluster.sync();
 }
 
 struct PrefillArgs {
@@ -371,7 +458,7 @@ __global__ void __launch_bounds__(kThreads) attn_prefill_kernel(PrefillArgs a) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int h0 = warp * 16;
+    const int h0 = (warp & 3) * 16, kh = warp >> 2;
     const bool has_heads = h0 < a.H;
     const int i = blockIdx.x;
     const long long p = a.q_pos0 + i;
@@ -396,7 +483,7 @@ __global__ void __launch_bounds__(kThreads) attn_prefill_kernel(PrefillArgs a) {
             src.sel = a.sel + static_cast<size_t>(i) * a.k_stride;
             n_sel = a.k_stride;
         } else {
-            long long nv = (p + 1) / a.ratio;
+            const long long nv = (p + 1) / a.ratio;
             n_sel = static_cast<int>(nv < a.n_comp ? nv : a.n_comp);
         }
     }
@@ -405,9 +492,10 @@ __global__ void __launch_bounds__(kThreads) attn_prefill_kernel(PrefillArgs a) {
     load_q_frags<D>(q, a.H, h0, qa);
     WarpState<D> st;
     init_state<D>(st);
-    attend_range<D>(src, 0, src.n_w + n_sel, qa, has_heads, a.scale_log2, sm, st);
+    attend_range<D>(src, 0, src.n_w + n_sel, qa, has_heads, kh, a.scale_log2, sm, st, false);
+    combine_halves<D>(st, reinterpret_cast<float *>(smem_raw));
     finish_l<D>(st);
-    if (has_heads) {
+    if (warp < 4 && has_heads) {
         uint16_t *o = a.out + static_cast<size_t>(i) * a.H * D;
         const float inv0 = 1.f / st.l[0], inv1 = 1.f / st.l[1];
         const int ra = h0 + g, rb = h0 + g + 8;
@@ -423,11 +511,6 @@ __global__ void __launch_bounds__(kThreads) attn_prefill_kernel(PrefillArgs a) {
 }
 
 template <int D>
-constexpr size_t decode_smem() {
-    return sizeof(Smem<D>) > sizeof(DecodePartial<D>) ? sizeof(Smem<D>) : sizeof(DecodePartial<D>);
-}
-
-template <int D>
 cudaError_t configure(int &cluster) {
     static thread_local int configured_device = -1;
     static thread_local int cluster_size = 16;
@@ -436,11 +519,17 @@ cudaError_t configure(int &cluster) {
     if (configured_device != dev) {
         cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(decode_smem<D>()));
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(attn_decode_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(sizeof(Smem<D>)));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_decode_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(prefill_smem<D>()));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_decode_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         // largest cluster (16, else 8) that the device can schedule with this footprint
         cluster_size = 8;
@@ -500,10 +589,10 @@ cudaError_t launch_attn_prefill(const uint16_t *q, int T, int H, int D, const ui
     cudaError_t e;
     if (D == 128) {
         if ((e = configure<128>(cluster)) != cudaSuccess) return e;
-        return launch(attn_prefill_kernel<128>, dim3(T), dim3(kThreads), sizeof(Smem<128>), c, 1, a);
+        return launch(attn_prefill_kernel<128>, dim3(T), dim3(kThreads), prefill_smem<128>(), c, 1, a);
     }
     if ((e = configure<64>(cluster)) != cudaSuccess) return e;
-    return launch(attn_prefill_kernel<64>, dim3(T), dim3(kThreads), sizeof(Smem<64>), c, 1, a);
+    return launch(attn_prefill_kernel<64>, dim3(T), dim3(kThreads), prefill_smem<64>(), c, 1, a);
 }
 
 }  // namespace ds4a

@@ -143,6 +143,16 @@ cudaError_t launch_compress(const uint16_t *k, const uint16_t *v, int n_new, int
     const bool last_open = (end % ratio) != 0;
     long long n_fc = (b_last - (last_open ? 1 : 0)) - (b_first + (first_open ? 1 : 0)) + 1;
     if (n_fc < 0) n_fc = 0;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        // same shared-memory carveout as the other ds4a kernels: no reconfiguration between them
+        cudaError_t e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
     CompressArgs a{k, v, w, state, comp_k, comp_v, pos, n_new, D, ratio};
     return launch(compress_kernel, dim3(static_cast<unsigned>(1 + n_fc)), dim3(kThreads), 0, c, 1, a);
 }

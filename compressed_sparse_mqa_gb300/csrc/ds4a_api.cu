@@ -154,7 +154,7 @@ int ds4a_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
     if (n_sel > 0 && (!comp_k || !comp_v)) return DS4A_ERR_ARG;
     if (!sel && n_sel > n_comp) return DS4A_ERR_ARG;
     if (!aligned(q, 4) || !aligned(win_k, 16) || !aligned(win_v, 16) || !aligned(comp_k, 16) ||
-        !aligned(comp_v, 16) || !aligned(sel, 4) || !aligned(out, 2))
+        !aligned(comp_v, 16) || !aligned(sel, 4) || !aligned(out, 16))
         return DS4A_ERR_ARG;
     ds4a::Ctx c;
     rc = make_ctx(stream, c);

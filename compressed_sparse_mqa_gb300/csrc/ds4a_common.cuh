@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ds4a.h"
+#include "ds4a.h"   // include/ (passed with -I)
 
 #define DS4A_DEVINL __device__ __forceinline__
 

@@ -10,14 +10,18 @@
 // fl(s + c) is the binary32 rounding of the exact score.  The ranking decision
 // is therefore taken on the correctly rounded binary32 score.
 //
-// Select.  Scores map to order-preserving u32 keys; a radix select over four
-// 8-bit digits (per-warp shared-memory histograms) finds the k-th largest key;
-// rows above it, then rows equal to it in ascending index order, are emitted in
-// ascending index order with two block-wide scans.
+// Select.  Scores map to order-preserving u32 keys held in registers (16 or 32
+// per thread; larger row counts re-read them from memory).  A radix select over
+// 8-bit digits with one shared histogram per pass (plain shared atomics) finds
+// the k-th largest key, stopping early once the boundary digit holds exactly
+// the rows still needed.  Rows above the boundary, then
+// boundary rows in ascending index order, are written in ascending index order
+// using warp ballots and one scan over (item, warp) counts.
 //
-// Decode (one query): a grid of CTAs sized to the SM count scores slices of the
-// rows into the workspace; the last CTA to finish (atomic ticket, no waiting)
-// runs the select and resets the ticket.  Prefill (many queries): one CTA per
+// Decode (one query): CTAs of 64 rows each load their key rows before waiting on
+// the previous kernel (the keys are cache state, not produced by it), score
+// them into the workspace, and the last CTA to finish (atomic ticket, no
+// waiting) selects and resets the ticket.  Prefill (many queries): one CTA per
 // query scores its visible rows into shared memory and selects.
 #include "ds4a_common.cuh"
 #include "ds4a_internal.h"
@@ -29,26 +33,47 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kGroup = 16;                        // threads per scored row
 constexpr int kRowsPerPass = kThreads / kGroup;   // 32
+constexpr int kRowsPerCta = 2 * kRowsPerPass;     // decode slice: 64 rows
 constexpr int kMaxDIdx = 256;
+constexpr int kMaxItems = 32;                     // register select: n <= 512 * 32
 constexpr size_t kWsHeader = 256;                 // ticket lives here
-constexpr int kSmemKeyCap = 24576;                // keys staged in shared memory
+constexpr int kSmemKeyCap = 16384;                // prefill: keys staged in shared memory
 
 struct SelectSmem {
-    uint32_t hist[kWarps][256];
-    uint32_t total[256];
+    uint32_t hist[256];
+    uint32_t cnt[kMaxItems * kWarps];
     uint32_t scan[kWarps];
     uint32_t bin;
     uint32_t above;
+    uint32_t count_bin;
 };
 
-// Score rows [j0, j1) of one query into keys[j - key_base].  q is staged once
-// per thread: thread (group lane gl) owns 8-dim chunks gl and gl + 16.
-__device__ void score_rows(const uint16_t *__restrict__ q, const uint16_t *__restrict__ kidx, int d_idx,
-                           long long j0, long long j1, uint32_t *keys, long long key_base) {
-    const int tid = threadIdx.x;
-    const int gl = tid % kGroup;
+// ---- scoring ---------------------------------------------------------------------------
+
+struct RowLoads {
+    uint4 v[2][2];   // [row pass][chunk]
+};
+
+DS4A_DEVINL void load_rows(const uint16_t *__restrict__ kidx, int d_idx, long long base, long long j1,
+                           RowLoads &L) {
+    const int tid = threadIdx.x, gl = tid % kGroup;
     const int n_chunks = d_idx / 8;
-    float qf[2][8];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const long long j = base + p * kRowsPerPass + tid / kGroup;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const int ch = gl + cc * kGroup;
+            L.v[p][cc] = (j < j1 && ch < n_chunks)
+                             ? __ldg(reinterpret_cast<const uint4 *>(kidx + j * d_idx + ch * 8))
+                             : make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+DS4A_DEVINL void load_query(const uint16_t *__restrict__ q, int d_idx, float (&qf)[2][8]) {
+    const int gl = threadIdx.x % kGroup;
+    const int n_chunks = d_idx / 8;
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
         const int ch = gl + cc * kGroup;
@@ -62,20 +87,24 @@ __device__ void score_rows(const uint16_t *__restrict__ q, const uint16_t *__res
             for (int e = 0; e < 8; ++e) qf[cc][e] = 0.f;
         }
     }
-    for (long long j = j0 + tid / kGroup; j < j1; j += kRowsPerPass) {
+}
+
+// Scores of the (up to) 64 rows base .. base+63 held in L; keys[j - base] for j < j1.
+// Every lane of every warp reaches the shuffles (the loop bounds are block-uniform).
+DS4A_DEVINL void score_loaded(const float (&qf)[2][8], const RowLoads &L, long long base, long long j1,
+                              uint32_t *keys) {
+    const int tid = threadIdx.x, gl = tid % kGroup;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
         float s = 0.f, c = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-            const int ch = gl + cc * kGroup;
-            if (ch < n_chunks) {
-                uint4 raw = __ldg(reinterpret_cast<const uint4 *>(kidx + j * d_idx + ch * 8));
-                const uint16_t *h = reinterpret_cast<const uint16_t *>(&raw);
+            const uint16_t *h = reinterpret_cast<const uint16_t *>(&L.v[p][cc]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float err;
-                    two_sum(s, qf[cc][e] * h2f(h[e]), s, err);
-                    c += err;
-                }
+            for (int e = 0; e < 8; ++e) {
+                float err;
+                two_sum(s, qf[cc][e] * h2f(h[e]), s, err);
+                c += err;
             }
         }
 #pragma unroll
@@ -86,12 +115,15 @@ __device__ void score_rows(const uint16_t *__restrict__ q, const uint16_t *__res
             two_sum(s, s2, s, err);
             c = (c + c2) + err;
         }
-        if (gl == 0) keys[j - key_base] = float_key(s + c);
+        const long long j = base + p * kRowsPerPass + tid / kGroup;
+        if (j < j1 && gl == 0) keys[j - base] = float_key(s + c);
     }
 }
 
+// ---- select ------------------------------------------------------------------------------
+
 // Block-wide exclusive scan of one value per thread (kThreads threads).
-__device__ uint32_t block_excl_scan(uint32_t v, uint32_t *scratch, uint32_t &total) {
+DS4A_DEVINL uint32_t block_excl_scan(uint32_t v, uint32_t *scratch, uint32_t &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t incl = v;
 #pragma unroll
@@ -103,6 +135,7 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t *scratch, uint32_t &tot
     if (lane == 31) scratch[warp] = incl;
     __syncthreads();
     uint32_t before = 0, all = 0;
+#pragma unroll
     for (int w = 0; w < kWarps; ++w) {
         const uint32_t t = scratch[w];
         if (w < warp) before += t;
@@ -112,79 +145,187 @@ __device__ uint32_t block_excl_scan(uint32_t v, uint32_t *scratch, uint32_t &tot
     return before + incl - v;
 }
 
-// Keep the k largest of keys[0..n) (ties to the lower index); write them in
-// ascending order to out[0..k), -1 past min(k, n); out_n (if given) = min(k, n).
-__device__ void block_topk(const uint32_t *keys, int n, int k, int32_t *out, int32_t *out_n,
-                           SelectSmem &sm) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (n <= k) {
-        for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
-        if (out_n && tid == 0) *out_n = n;
-        return;
+// In-place exclusive scan of cnt[0..m), m <= 2 * kThreads.
+DS4A_DEVINL void scan_counts(uint32_t *cnt, int m, uint32_t *scratch) {
+    const int e0 = 2 * threadIdx.x, e1 = e0 + 1;
+    const uint32_t a = e0 < m ? cnt[e0] : 0u, b = e1 < m ? cnt[e1] : 0u;
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan(a + b, scratch, tot);
+    if (e0 < m) cnt[e0] = ex;
+    if (e1 < m) cnt[e1] = ex + a;
+    __syncthreads();
+}
+
+// Histogram increment (b = 256 adds nothing).  Plain shared atomics: cheaper
+// here than aggregating equal digits across the warp first.
+DS4A_DEVINL void hist_add(uint32_t *hist, uint32_t b) {
+    if (b < 256u) atomicAdd(&hist[b], 1u);
+}
+
+// Warp 0: the digit (scanning from the largest) that holds the kk-th largest key.
+DS4A_DEVINL void find_bin(SelectSmem &sm, uint32_t kk) {
+    if ((threadIdx.x >> 5) != 0) return;
+    const int lane = threadIdx.x & 31;
+    uint32_t cnt[8], lsum = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) { cnt[e] = sm.hist[255 - 8 * lane - e]; lsum += cnt[e]; }
+    uint32_t incl = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
     }
+    const unsigned hit = __ballot_sync(0xffffffffu, incl >= kk);
+    if (lane == __ffs(hit) - 1) {
+        uint32_t before = incl - lsum;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (before + cnt[e] >= kk) {
+                sm.bin = 255 - 8 * lane - e;
+                sm.above = before;
+                sm.count_bin = cnt[e];
+                break;
+            }
+            before += cnt[e];
+        }
+    }
+}
+
+template <bool GLOBAL>
+DS4A_DEVINL uint32_t ld_key(const uint32_t *src, int i) {
+    if constexpr (GLOBAL) return __ldcg(src + i);
+    else return src[i];
+}
+
+// Keys in registers: item `it` of thread t is index it * kThreads + t.  n > k.
+template <int ITEMS, bool GLOBAL>
+__device__ void select_regs(const uint32_t *src, int n, int k, int32_t *out, SelectSmem &sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    uint32_t key[ITEMS];
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int i = it * kThreads + tid;
+        key[it] = i < n ? ld_key<GLOBAL>(src, i) : 0u;
+    }
+    uint32_t prefix = 0, mask = 0, kk = static_cast<uint32_t>(k), count_eq = 0;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        if (tid < 256) sm.hist[tid] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) {
+            const bool part = (it * kThreads + tid) < n && (key[it] & mask) == prefix;
+            hist_add(sm.hist, part ? (key[it] >> shift) & 255u : 256u);
+        }
+        __syncthreads();
+        find_bin(sm, kk);
+        __syncthreads();
+        kk -= sm.above;
+        prefix |= sm.bin << shift;
+        mask |= 255u << shift;
+        count_eq = sm.count_bin;
+        if (count_eq == kk) break;   // every boundary row is kept: no tie ranking needed
+    }
+    const bool all_eq = count_eq == kk;
+    uint32_t take_eq = 0u;
+    if (!all_eq) {
+        // rank the boundary rows in index order; keep the first kk
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) {
+            const bool eq = (it * kThreads + tid) < n && (key[it] & mask) == prefix;
+            const unsigned b = __ballot_sync(0xffffffffu, eq);
+            if (lane == 0) sm.cnt[it * kWarps + warp] = __popc(b);
+        }
+        __syncthreads();
+        scan_counts(sm.cnt, ITEMS * kWarps, sm.scan);
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) {
+            const bool eq = (it * kThreads + tid) < n && (key[it] & mask) == prefix;
+            const unsigned b = __ballot_sync(0xffffffffu, eq);
+            if (eq && sm.cnt[it * kWarps + warp] + __popc(b & lt) < kk) take_eq |= 1u << it;
+        }
+        __syncthreads();
+    }
+    // final flags, their warp ballots kept in registers, one scan of (item, warp) counts
+    unsigned fb[ITEMS];
+    uint32_t fbits = 0;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const uint32_t km = key[it] & mask;
+        const bool f = (it * kThreads + tid) < n &&
+                       (km > prefix || (km == prefix && (all_eq || ((take_eq >> it) & 1u))));
+        fb[it] = __ballot_sync(0xffffffffu, f);
+        fbits |= static_cast<uint32_t>(f) << it;
+        if (lane == 0) sm.cnt[it * kWarps + warp] = __popc(fb[it]);
+    }
+    __syncthreads();
+    scan_counts(sm.cnt, ITEMS * kWarps, sm.scan);
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it)
+        if ((fbits >> it) & 1u) out[sm.cnt[it * kWarps + warp] + __popc(fb[it] & lt)] = it * kThreads + tid;
+}
+
+// Any n > k: keys re-read from memory each pass; thread t emits the contiguous range [t*C, t*C + C).
+template <bool GLOBAL>
+__device__ void select_generic(const uint32_t *src, int n, int k, int32_t *out, SelectSmem &sm) {
+    const int tid = threadIdx.x;
     uint32_t prefix = 0, mask = 0, kk = static_cast<uint32_t>(k);
     for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < kWarps * 256; i += kThreads) (&sm.hist[0][0])[i] = 0;
+        if (tid < 256) sm.hist[tid] = 0;
         __syncthreads();
-        for (int i = tid; i < n; i += kThreads) {
-            const uint32_t key = keys[i];
-            if ((key & mask) == prefix) atomicAdd(&sm.hist[warp][(key >> shift) & 255u], 1u);
-        }
-        __syncthreads();
-        if (tid < 256) {
-            uint32_t t = 0;
-            for (int w = 0; w < kWarps; ++w) t += sm.hist[w][tid];
-            sm.total[tid] = t;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // lane L covers bins 255-8L down to 248-8L (largest bins first)
-            uint32_t cnt[8], lsum = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { cnt[e] = sm.total[255 - 8 * lane - e]; lsum += cnt[e]; }
-            uint32_t incl = lsum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
+        for (int base = 0; base < n; base += kThreads) {
+            const int i = base + tid;
+            uint32_t b = 256u;
+            if (i < n) {
+                const uint32_t key = ld_key<GLOBAL>(src, i);
+                if ((key & mask) == prefix) b = (key >> shift) & 255u;
             }
-            const unsigned hit = __ballot_sync(0xffffffffu, incl >= kk);
-            const int first = __ffs(hit) - 1;
-            if (lane == first) {
-                uint32_t before = incl - lsum;
-                for (int e = 0; e < 8; ++e) {
-                    if (before + cnt[e] >= kk) { sm.bin = 255 - 8 * lane - e; sm.above = before; break; }
-                    before += cnt[e];
-                }
-            }
+            hist_add(sm.hist, b);
         }
+        __syncthreads();
+        find_bin(sm, kk);
         __syncthreads();
         kk -= sm.above;
         prefix |= sm.bin << shift;
         mask |= 255u << shift;
         __syncthreads();
     }
-    // emit in ascending index order: thread t owns the contiguous range [t*C, t*C + C)
     const int C = (n + kThreads - 1) / kThreads;
     const int lo = tid * C, hi = min(n, lo + C);
     uint32_t n_gt = 0, n_eq = 0;
     for (int i = lo; i < hi; ++i) {
-        const uint32_t key = keys[i];
+        const uint32_t key = ld_key<GLOBAL>(src, i);
         n_gt += key > prefix;
         n_eq += key == prefix;
     }
     uint32_t tot;
     const uint32_t eq_before = block_excl_scan(n_eq, sm.scan, tot);
     const uint32_t take = eq_before >= kk ? 0u : min(n_eq, kk - eq_before);
-    const uint32_t pos0 = block_excl_scan(n_gt + take, sm.scan, tot);
-    uint32_t p = pos0, taken = 0;
+    uint32_t p = block_excl_scan(n_gt + take, sm.scan, tot), taken = 0;
     for (int i = lo; i < hi; ++i) {
-        const uint32_t key = keys[i];
+        const uint32_t key = ld_key<GLOBAL>(src, i);
         if (key > prefix) out[p++] = i;
         else if (key == prefix && taken < take) { out[p++] = i; ++taken; }
     }
-    if (out_n && tid == 0) *out_n = k;
 }
+
+// Keep the k largest of src[0..n) (ties to the lower index): ascending indices in
+// out[0..min(k,n)), -1 after; out_n (if given) = min(k, n).
+template <bool GLOBAL>
+__device__ void select_topk(const uint32_t *src, int n, int k, int32_t *out, int32_t *out_n, SelectSmem &sm) {
+    if (n <= k) {
+        for (int i = threadIdx.x; i < k; i += kThreads) out[i] = i < n ? i : -1;
+    } else if (n <= kThreads * 16) {
+        select_regs<16, GLOBAL>(src, n, k, out, sm);
+    } else if (n <= kThreads * kMaxItems) {
+        select_regs<kMaxItems, GLOBAL>(src, n, k, out, sm);
+    } else {
+        select_generic<GLOBAL>(src, n, k, out, sm);
+    }
+    if (out_n && threadIdx.x == 0) *out_n = n < k ? n : k;
+}
+
+// ---- kernels -----------------------------------------------------------------------------
 
 struct IndexerArgs {
     const uint16_t *q_idx;
@@ -200,68 +341,77 @@ struct IndexerArgs {
     int k;
 };
 
-__device__ __forceinline__ long long visible_rows(const IndexerArgs &a, int i) {
+DS4A_DEVINL long long visible_rows(const IndexerArgs &a, int i) {
     const long long v = (a.q_pos0 + i + 1) / a.ratio;
     return v < a.n_rows ? v : a.n_rows;
 }
 
-// one query, many CTAs: score a slice each, the last CTA selects
-__global__ void __launch_bounds__(kThreads) indexer_decode_kernel(IndexerArgs a, int rows_per_cta) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    SelectSmem &sm = *reinterpret_cast<SelectSmem *>(smem_raw);
+// one query: CTA b scores rows [b*rows_per_cta, (b+1)*rows_per_cta) in 64-row
+// slices; the last CTA to finish selects
+__global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs a, int rows_per_cta) {
+    __shared__ SelectSmem sm;
     __shared__ bool s_last;
-    pdl_wait();
-    pdl_trigger();
-    unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws);
-    uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + kWsHeader);
     const long long n_vis = visible_rows(a, 0);
     const long long j0 = static_cast<long long>(blockIdx.x) * rows_per_cta;
     const long long j1 = min(n_vis, j0 + rows_per_cta);
-    if (j0 < j1) score_rows(a.q_idx, a.k_idx, a.d_idx, j0, j1, keys, 0);
+    RowLoads L;
+    load_rows(a.k_idx, a.d_idx, j0, j1, L);   // key rows: cache state, independent of the previous kernel
+    pdl_wait();
+    pdl_trigger();
+    float qf[2][8];
+    load_query(a.q_idx, a.d_idx, qf);
+    unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws);
+    uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + kWsHeader);
+    score_loaded(qf, L, j0, j1, keys + j0);
+    for (long long base = j0 + kRowsPerCta; base < j1; base += kRowsPerCta) {
+        load_rows(a.k_idx, a.d_idx, base, j1, L);
+        score_loaded(qf, L, base, j1, keys + base);
+    }
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    // keys written by other CTAs: read through L2 (they were never cached in this SM's L1)
-    uint32_t *skeys = reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelectSmem));
-    const uint32_t *src = keys;
-    if (n_vis <= kSmemKeyCap) {
-        for (long long i = threadIdx.x; i < n_vis; i += kThreads) skeys[i] = __ldcg(keys + i);
-        src = skeys;
-        __syncthreads();
-    }
-    block_topk(src, static_cast<int>(n_vis), a.k, a.out_idx, a.out_n, sm);
+    select_topk<true>(keys, static_cast<int>(n_vis), a.k, a.out_idx, a.out_n, sm);
     if (threadIdx.x == 0) *ticket = 0u;
 }
 
 // many queries: one CTA per query
-__global__ void __launch_bounds__(kThreads) indexer_query_kernel(IndexerArgs a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    SelectSmem &sm = *reinterpret_cast<SelectSmem *>(smem_raw);
+__global__ void __launch_bounds__(kThreads, 1) indexer_query_kernel(IndexerArgs a) {
+    extern __shared__ __align__(16) uint32_t skeys[];
+    __shared__ SelectSmem sm;
     pdl_wait();
     pdl_trigger();
     const int i = blockIdx.x;
     const long long n_vis = visible_rows(a, i);
-    uint32_t *keys;
-    if (n_vis <= kSmemKeyCap) keys = reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelectSmem));
-    else keys = reinterpret_cast<uint32_t *>(a.ws + kWsHeader) + static_cast<size_t>(i) * a.n_rows;
-    score_rows(a.q_idx + static_cast<size_t>(i) * a.d_idx, a.k_idx, a.d_idx, 0, n_vis, keys, 0);
+    const bool in_smem = n_vis <= kSmemKeyCap;
+    uint32_t *keys = in_smem ? skeys
+                             : reinterpret_cast<uint32_t *>(a.ws + kWsHeader) + static_cast<size_t>(i) * a.n_rows;
+    float qf[2][8];
+    load_query(a.q_idx + static_cast<size_t>(i) * a.d_idx, a.d_idx, qf);
+    for (long long base = 0; base < n_vis; base += kRowsPerCta) {
+        RowLoads L;
+        load_rows(a.k_idx, a.d_idx, base, n_vis, L);
+        score_loaded(qf, L, base, n_vis, keys + base);
+    }
     __syncthreads();
-    block_topk(keys, static_cast<int>(n_vis), a.k, a.out_idx + static_cast<size_t>(i) * a.k,
-               a.out_n ? a.out_n + i : nullptr, sm);
+    int32_t *out = a.out_idx + static_cast<size_t>(i) * a.k;
+    int32_t *out_n = a.out_n ? a.out_n + i : nullptr;
+    if (in_smem) select_topk<false>(keys, static_cast<int>(n_vis), a.k, out, out_n, sm);
+    else select_topk<true>(keys, static_cast<int>(n_vis), a.k, out, out_n, sm);
 }
 
-constexpr size_t kSelectSmem = (sizeof(SelectSmem) + 15) / 16 * 16;
-constexpr size_t kMaxSmem = kSelectSmem + kSmemKeyCap * sizeof(uint32_t);
+constexpr size_t kQuerySmem = kSmemKeyCap * sizeof(uint32_t);
 
 }  // namespace
 
 size_t indexer_ws_bytes(int n_q, long long n_rows, int k) {
     (void)k;
-    const long long nq = n_q > 1 ? n_q : 1;
-    return kWsHeader + static_cast<size_t>(nq) * static_cast<size_t>(n_rows) * sizeof(uint32_t);
+    size_t keys = 0;
+    if (n_q <= 1) keys = static_cast<size_t>(n_rows);
+    else if (n_rows > kSmemKeyCap) keys = static_cast<size_t>(n_q) * static_cast<size_t>(n_rows);
+    return kWsHeader + keys * sizeof(uint32_t);
 }
 
 cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
@@ -272,11 +422,14 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(indexer_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kMaxSmem));
+        cudaError_t e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kQuerySmem));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kMaxSmem));
+            e = cudaFuncSetAttribute(indexer_decode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -285,14 +438,16 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
     if (n_q == 1) {
         long long n_vis = (q_pos0 + 1) / ratio;
         if (n_vis > n_rows) n_vis = n_rows;
-        long long grid = (n_vis + kRowsPerPass - 1) / kRowsPerPass;
-        if (grid > c.num_sms) grid = c.num_sms;
+        // 64-row slices, spread so that the grid is at most one CTA per SM
+        const long long slices = (n_vis + kRowsPerCta - 1) / kRowsPerCta;
+        const long long per_cta = slices > c.num_sms ? (slices + c.num_sms - 1) / c.num_sms : 1;
+        const int rows_per_cta = static_cast<int>(per_cta * kRowsPerCta);
+        long long grid = (n_vis + rows_per_cta - 1) / rows_per_cta;
         if (grid < 1) grid = 1;
-        const int rows_per_cta = static_cast<int>((n_vis + grid - 1) / grid);
-        return launch(indexer_decode_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kMaxSmem,
-                      c, 1, a, rows_per_cta);
+        return launch(indexer_decode_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, c, 1, a,
+                      rows_per_cta);
     }
-    return launch(indexer_query_kernel, dim3(static_cast<unsigned>(n_q)), dim3(kThreads), kMaxSmem, c, 1, a);
+    return launch(indexer_query_kernel, dim3(static_cast<unsigned>(n_q)), dim3(kThreads), kQuerySmem, c, 1, a);
 }
 
 }  // namespace ds4a

@@ -9,11 +9,12 @@ The KV state of one layer lives on the device, owned here (allocated through
 torch): the raw window ring [W, D] (token p sits in slot p % W), the compressed
 rows [cap, D], one indexer key per compressed row, and the compressor's running
 state.  A decode step is three library calls on the current stream:
-compress_append (the new token, read from its ring slot) -> indexer_topk (ratio-4
-layers) -> attn_decode over the ring and the kept rows.
+indexer_topk (ratio-4 layers) -> compress_append (the new token, read from its
+ring slot) -> attn_decode over the ring and the kept rows.
 """
 from __future__ import annotations
 
+import copy
 import math
 
 import numpy as np
@@ -96,15 +97,45 @@ class DecodeLayer:
             self.kidx = self.q_idx = self.sel = self.sel_n = self.ws = None
         self.slot = p % W
 
+    def clone(self) -> "DecodeLayer":
+        """An independent copy of the device state (same values, new buffers)."""
+        c = copy.copy(self)
+        for name, val in vars(self).items():
+            if isinstance(val, torch.Tensor):
+                setattr(c, name, val.clone())
+        if c.ws is not None:
+            c.ws.zero_()
+        return c
+
+    def bytes_touched(self) -> int:
+        """Device bytes one decode step reads or writes (the algorithmic traffic)."""
+        D = self.D
+        b = 2 * self.H * D * 2                                  # q in, out
+        b += 2 * self.n_win * D * 2                             # window K, V
+        if self.ratio:
+            b += 2 * D * 2 + D * 4 + (2 + 2 * D) * 4            # new token K, V; w; state
+            n_rows = self.topk if self.topk else self.n_vis
+            b += 2 * min(n_rows, self.n_vis) * D * 2            # kept compressed rows K, V
+        if self.topk:
+            b += self.n_vis * self.kidx.shape[1] * 2 + self.kidx.shape[1] * 2  # indexer keys, query
+            b += self.topk * 4 * 2 + 4                          # kept indices written, read back
+        return b
+
     def step(self, stream=None):
-        """One decode step at position p (all inputs already resident)."""
+        """One decode step at position p (all inputs already resident).
+
+        The indexer runs first: it reads only the indexer keys (caller-supplied for
+        every visible row), not the compressor's output, so under programmatic
+        dependent launch its key-row loads overlap the previous layer's attention.
+        """
+        if self.topk:
+            ds4a.ds4a_indexer_topk(self.q_idx, self.kidx, self.p, self.ratio, self.topk, self.sel, self.sel_n,
+                                   self.ws, stream=stream)
         if self.ratio:
             ds4a.ds4a_compress_append(self.ring_k[self.slot: self.slot + 1], self.ring_v[self.slot: self.slot + 1],
                                       self.w, self.ratio, self.p, self.state, self.comp_k, self.comp_v,
                                       stream=stream)
         if self.topk:
-            ds4a.ds4a_indexer_topk(self.q_idx, self.kidx, self.p, self.ratio, self.topk, self.sel, self.sel_n,
-                                   self.ws, stream=stream)
             ds4a.ds4a_attn_decode(self.q, self.ring_k[: self.n_win], self.ring_v[: self.n_win], self.comp_k,
                                   self.comp_v, self.sel, self.topk, self.scale, self.out, stream=stream)
         else:
