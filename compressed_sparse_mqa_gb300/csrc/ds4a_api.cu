@@ -192,3 +192,62 @@ int ds4a_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *ra
 }
 
 }  // extern "C"
+
+// ---- indexer entry point that allocates nothing -------------------------------------------
+// Some callers cannot give the library a workspace: plugin and callback hosts
+// whose enqueue step must not allocate device memory (an allocation there can
+// synchronise the device or is simply not allowed by the host), and callers that
+// run under a fixed, pre-reserved memory budget.  For them this file keeps the
+// one-query indexer's scratch (ticket header + one u32 key per row) in a
+// statically sized device array that every GPU loading the library holds until
+// the process exits.
+namespace {
+
+constexpr long long kNoAllocMaxRows = 65536;   // 65536 rows: 256 KiB of keys
+constexpr size_t kNoAllocHeaderBytes = 256;
+constexpr size_t kNoAllocScratchBytes = kNoAllocHeaderBytes + kNoAllocMaxRows * sizeof(uint32_t);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void *g_noalloc_addr[kMaxDevices];
+bool g_noalloc_ready[kMaxDevices];
+
+}  // namespace
+
+extern "C" int ds4a_indexer_topk_noalloc(const uint16_t *q_idx, const uint16_t *k_idx, long long n_rows,
+                                         int d_idx, long long q_pos, int ratio, int k, int32_t *out_idx,
+                                         int32_t *out_n, void *stream) {
+    if (n_rows < 0 || q_pos < 0 || ratio < 1 || k < 1) return DS4A_ERR_ARG;
+    if (d_idx < 8 || d_idx > 256 || d_idx % 8 != 0 || k > 2048) return DS4A_ERR_UNSUPPORTED;
+    if (n_rows > kNoAllocMaxRows) return DS4A_ERR_WORKSPACE;   // beyond the built-in scratch
+    if (!q_idx || !out_idx || (n_rows > 0 && !k_idx)) return DS4A_ERR_ARG;
+    if (!aligned(q_idx, 16) || !aligned(k_idx, 16) || !aligned(out_idx, 4) || !aligned(out_n, 4))
+        return DS4A_ERR_ARG;
+    if (ds4a::indexer_ws_bytes(1, n_rows, k) > kNoAllocScratchBytes) return DS4A_ERR_WORKSPACE;
+    ds4a::Ctx c;
+    int rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DS4A_ERR_CUDA;
+    if (!g_noalloc_ready[dev]) {
+        // once per device, with that device current: the device address of the array
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_noalloc_ready[dev]) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+                cudaGetLastError();
+                return DS4A_ERR_CUDA;
+            }
+            g_noalloc_addr[dev] = p;
+            g_noalloc_ready[dev] = true;
+        }
+    }
+    void *scratch = g_noalloc_addr[dev];
+    // the completion ticket in the header must start at zero; the keys need no clearing
+    if (cudaMemsetAsync(scratch, 0, kNoAllocHeaderBytes, c.stream) != cudaSuccess) {
+        cudaGetLastError();
+        return DS4A_ERR_CUDA;
+    }
+    return from_cuda(ds4a::launch_indexer(q_idx, 1, k_idx, n_rows, d_idx, q_pos, ratio, k, out_idx, out_n,
+                                          scratch, c));
+}

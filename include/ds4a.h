@@ -118,6 +118,33 @@ int ds4a_indexer_topk(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, lon
 size_t ds4a_indexer_workspace_bytes(int n_q, long long n_rows, int k);
 
 /*
+ * ds4a_indexer_topk_noalloc -- ds4a_indexer_topk for one query (n_q = 1) with no
+ * workspace argument and no allocation.  The pages have no counterpart: this is
+ * a convenience of this library.
+ *
+ * For callers that cannot allocate device memory at the point of the call --
+ * plugin or callback hosts whose enqueue step may not allocate (allocation
+ * there can synchronise the device, or the host forbids it) and programs that
+ * run inside a fixed, pre-reserved memory budget.  The scratch lives in a
+ * statically sized device array inside the library (256 KiB + 256 bytes), held
+ * by every GPU that loads the library until the process exits.
+ *
+ *   Arguments as ds4a_indexer_topk with n_q = 1 and q_pos0 = q_pos.
+ *   n_rows     at most 65536; larger returns DS4A_ERR_WORKSPACE and enqueues
+ *              nothing.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Each call enqueues a cudaMemsetAsync that clears the array's ticket
+ *   header, then the indexer kernel.  All calls share the one array and it keeps
+ *   the last call's contents: calls whose work overlaps on the GPU (different
+ *   streams, or different host threads, without ordering between them) race
+ *   and give wrong results.
+ */
+int ds4a_indexer_topk_noalloc(const uint16_t *q_idx, const uint16_t *k_idx, long long n_rows,
+                              int d_idx, long long q_pos, int ratio, int k, int32_t *out_idx,
+                              int32_t *out_n, void *stream);
+
+/*
  * ds4a_attn_decode -- one decode query: multi-query attention over the raw
  * window and the selected (or all) compressed rows, as one softmax.
  * ("DS4 (DwarfStar 4)", Architecture: 64 heads, 1 KV head, 128-token window;
