@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the C3/C4/C5 sub-results")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=["c3", "c4", "c5"], default=None,
+                    help="run one sub-configuration alone and print its result (for profiling)")
     return ap.parse_args()
 
 
@@ -92,6 +94,26 @@ def rotation_copies(bytes_per_copy: int, l2_bytes: int, minimum: int = 2) -> int
     return max(minimum, math.ceil(2 * l2_bytes / max(bytes_per_copy, 1)) + 1)
 
 
+KERNEL_SOURCES = {"indexer_topk": "indexer.cu", "attn_decode": "attention.cu", "compress_append": "compress.cu"}
+
+
+def kernel_traffic(name: str):
+    """DRAM bytes per launch from the committed ncu capture of this kernel, or None
+    when the kernel's source has changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "compressed_sparse_mqa_gb300", "csrc", KERNEL_SOURCES.get(name, ""))
+    if not os.path.exists(path) or not os.path.isfile(src):
+        return None
+    with open(path) as f:
+        entry = json.load(f).get(name)
+    if not entry:
+        return None
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    return entry["dram_bytes_per_launch"] if entry.get("source_sha256") == digest else None
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -133,6 +155,11 @@ def run_ours(args, rank, world, local):
     peaks, peak_src = timing.load_peaks(ROOT)
     hbm_peak = float(peaks["hbm_gbs"])
     stream = torch.cuda.Stream()
+    if args.only:
+        fn = {"c3": lambda: sub_decode(configs.C3, l2, stream, hbm_peak),
+              "c4": lambda: sub_prefill(configs.C4, l2, stream, peaks),
+              "c5": lambda: sub_stack(l2, stream, hbm_peak)}[args.only]
+        return {"only": args.only, "result": fn()}
 
     # ---- headline: C2 decode step --------------------------------------------------------
     inst = configs.decode(configs.C2)
@@ -189,7 +216,7 @@ def run_ours(args, rank, world, local):
     dom = max(kt, key=kt.get)
     achieved = kbytes[dom] / (kt[dom] / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
-                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": kernel_traffic(dom),
                 "peak_source": f"{peak_src} hbm_gbs",
                 "kernel_us": {k: round(v * 1e3, 3) for k, v in kt.items()},
                 "kernel_bytes": kbytes}

@@ -23,6 +23,13 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
                            int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
                            int32_t *out_n, void *ws, const Ctx &c);
 
+// tensor-core prefill indexer (many queries): availability, workspace, launch
+bool indexer_prefill_tc_ok(int n_q, long long n_rows, int d_idx);
+size_t indexer_prefill_tc_ws_bytes(int n_q, long long n_rows);
+cudaError_t launch_indexer_prefill_tc(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
+                                      int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
+                                      int32_t *out_n, void *ws, const Ctx &c);
+
 cudaError_t launch_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
                                const uint16_t *win_v, int n_win, const uint16_t *comp_k,
                                const uint16_t *comp_v, long long n_comp, const int32_t *sel,

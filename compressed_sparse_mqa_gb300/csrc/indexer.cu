@@ -21,8 +21,9 @@
 // Decode (one query): CTAs of 64 rows each load their key rows before waiting on
 // the previous kernel (the keys are cache state, not produced by it), score
 // them into the workspace, and the last CTA to finish (atomic ticket, no
-// waiting) selects and resets the ticket.  Prefill (many queries): one CTA per
-// query scores its visible rows into shared memory and selects.
+// waiting) selects and resets the ticket.  Many queries: the tensor-core path
+// (indexer_tc.cu) when the shapes allow it, else one CTA per query scores its
+// visible rows into shared memory and selects.
 #include "ds4a_common.cuh"
 #include "ds4a_internal.h"
 
@@ -411,7 +412,13 @@ size_t indexer_ws_bytes(int n_q, long long n_rows, int k) {
     size_t keys = 0;
     if (n_q <= 1) keys = static_cast<size_t>(n_rows);
     else if (n_rows > kSmemKeyCap) keys = static_cast<size_t>(n_q) * static_cast<size_t>(n_rows);
-    return kWsHeader + keys * sizeof(uint32_t);
+    size_t bytes = kWsHeader + keys * sizeof(uint32_t);
+    // the tensor-core path for many queries keeps [n_q][rows] approximate scores and the key norms
+    if (n_q > 1) {
+        const size_t tc_bytes = indexer_prefill_tc_ws_bytes(n_q, n_rows);
+        if (tc_bytes > bytes) bytes = tc_bytes;
+    }
+    return bytes;
 }
 
 cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
@@ -447,6 +454,8 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
         return launch(indexer_decode_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, c, 1, a,
                       rows_per_cta);
     }
+    if (indexer_prefill_tc_ok(n_q, n_rows, d_idx))
+        return launch_indexer_prefill_tc(q_idx, n_q, k_idx, n_rows, d_idx, q_pos0, ratio, k, out_idx, out_n, ws, c);
     return launch(indexer_query_kernel, dim3(static_cast<unsigned>(n_q)), dim3(kThreads), kQuerySmem, c, 1, a);
 }
 

@@ -1,0 +1,571 @@
+// indexer_tc.cu -- the prefill indexer on the 5th-generation tensor cores.
+//
+// "DS4 (DwarfStar 4)", Key Techniques, "KV attention compression": on ratio-4
+// layers a learned indexer keeps the top-512 compressed rows for every query of
+// a prefill chunk.  For a chunk of T queries this is a [T x d] . [d x n_rows]
+// score matrix followed by a per-query top-k.
+//
+// 1. indexer_scores_tc_kernel: tcgen05.mma (M = 128 queries, N = 256 rows,
+//    K = d_idx, fp16 in, fp32 accumulate in tensor memory, two accumulator
+//    buffers so the epilogue of one tile overlaps the MMAs of the next) writes
+//    approximate scores s~ to the workspace, and the squared norm of every key
+//    row.
+// 2. indexer_select_kernel: per query, the approximate scores s~ differ from the
+//    exact scores s by at most eps = 2^-12 |q| max_j |k_j| (a bound far above the
+//    tensor cores' fp32 accumulation error over d_idx <= 128 exact products).  Two
+//    11-bit radix passes over s~ bracket the k-th largest s~ in [T_lo, T_hi].
+//    Rows with s~ > T_hi + 2 eps + 4 ulp are kept for certain, rows with
+//    s~ < T_lo - 2 eps - 4 ulp are dropped for certain; only the rows in between
+//    (a handful) are rescored exactly (TwoSum over the exact fp16 products,
+//    rounded once to binary32) and ranked (higher score, then lower index).  The
+//    result is the exact top-k of the binary32-rounded exact scores.  If the band
+//    is ever larger than its buffer (e.g. many equal keys), the query falls back
+//    to exact scores for every row and an exact radix select.
+#include "ds4a_common.cuh"
+#include "ds4a_internal.h"
+#include "tcgen05.cuh"
+
+namespace ds4a {
+namespace {
+
+constexpr int kTM = 128;                 // queries per tile (MMA M)
+constexpr int kTN = 256;                 // rows per tile (MMA N)
+constexpr int kGemmThreads = 128;
+constexpr uint32_t kMaxPolls = 1u << 26;  // bounded mbarrier wait
+
+struct TcScoreArgs {
+    const uint16_t *q_idx;
+    const uint16_t *k_idx;
+    float *scores;     // [n_q][ld]
+    float *knorm2;     // [ld]
+    unsigned int *err;
+    long long n_rows;
+    int n_q;
+    int ld;
+    int n_ntiles;
+    int n_split;
+};
+
+template <int DI>
+__global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcScoreArgs a) {
+    constexpr int kAtoms = DI / 64;                 // 128-byte swizzle atoms along K
+    constexpr int kChunks = DI / 8;                 // 16-byte chunks per row
+    constexpr int kABytes = kAtoms * kTM * 128;
+    constexpr int kBBytes = kAtoms * kTN * 128;
+    constexpr uint32_t kIdesc = tc::idesc_f16_f32(kTM, kTN, false, false);
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *sa = smem;
+    unsigned char *sb[2] = {smem + kABytes, smem + kABytes + kBBytes};
+    __shared__ uint32_t s_tmem;
+    __shared__ __align__(8) uint64_t s_bar[2];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int m0 = blockIdx.x * kTM;
+    const int ns = blockIdx.y;
+    const int n_my = ns < a.n_ntiles ? (a.n_ntiles - ns + a.n_split - 1) / a.n_split : 0;
+
+    if (tid == 0) {
+        tc::mbar_init(&s_bar[0], 1);
+        tc::mbar_init(&s_bar[1], 1);
+        tc::mbar_fence_init();
+    }
+    if (warp == 0) tc::tmem_alloc(&s_tmem, 2 * kTN);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+
+    auto load_b = [&](int it, int buf) {
+        const long long row0 = static_cast<long long>(ns + it * a.n_split) * kTN;
+        for (int i = tid; i < kTN * kChunks; i += kGemmThreads) {
+            const int r = i / kChunks, c = i % kChunks;
+            unsigned char *dst = sb[buf] + (c >> 3) * (kTN * 128) + tc::sw128_chunk(r, c & 7);
+            const long long row = row0 + r;
+            if (row < a.n_rows) cp_async16(dst, a.k_idx + row * DI + c * 8);
+            else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+        }
+    };
+    // key rows are cache state: the first tile is fetched before waiting on the previous kernel
+    if (n_my > 0) load_b(0, 0);
+    pdl_wait();
+    pdl_trigger();
+    for (int i = tid; i < kTM * kChunks; i += kGemmThreads) {
+        const int r = i / kChunks, c = i % kChunks;
+        unsigned char *dst = sa + (c >> 3) * (kTM * 128) + tc::sw128_chunk(r, c & 7);
+        if (m0 + r < a.n_q) cp_async16(dst, a.q_idx + static_cast<long long>(m0 + r) * DI + c * 8);
+        else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    cp_async_commit();
+    if (n_my > 1) {
+        load_b(1, 1);
+        cp_async_commit();
+    }
+
+    bool ok = true;
+    auto epilogue = [&](int it) {
+        const int buf = it & 1;
+        if (!tc::mbar_wait(&s_bar[buf], (it >> 1) & 1, kMaxPolls)) ok = false;
+        tc::fence_after_sync();
+        const int row = warp * 32 + lane;
+        const int q = m0 + row;
+        const long long col0 = static_cast<long long>(ns + it * a.n_split) * kTN;
+        float *dst = a.scores + static_cast<long long>(q) * a.ld + col0;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kTN; c0 += 16) {
+            uint32_t r[16];
+            tc::ld_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + buf * kTN + c0, r);
+            tc::wait_ld();
+            if (ok && q < a.n_q) {
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4 *>(dst + c0 + j) =
+                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                    __uint_as_float(r[j + 3]));
+            }
+        }
+    };
+
+    for (int it = 0; it < n_my; ++it) {
+        if (it == 0 && n_my > 1) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        tc::fence_proxy_async();
+        __syncthreads();
+        tc::fence_after_sync();
+        const int buf = it & 1;
+        if (tid == 0) {
+#pragma unroll
+            for (int s = 0; s < DI / 16; ++s) {
+                const uint64_t da = tc::desc_sw128(tc::smem_u32(sa) + (s / 4) * (kTM * 128) + (s % 4) * 32, 16, 1024);
+                const uint64_t db = tc::desc_sw128(tc::smem_u32(sb[buf]) + (s / 4) * (kTN * 128) + (s % 4) * 32, 16, 1024);
+                tc::mma_f16(tmem + buf * kTN, da, db, kIdesc, s > 0 ? 1u : 0u);
+            }
+            tc::commit(&s_bar[buf]);
+        }
+        // squared norms of the key rows (one M tile computes them)
+        if (blockIdx.x == 0) {
+            const long long row0 = static_cast<long long>(ns + it * a.n_split) * kTN;
+            for (int r = tid; r < kTN; r += kGemmThreads) {
+                float acc = 0.f;
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(sb[buf] + (c >> 3) * (kTN * 128) + tc::sw128_chunk(r, c & 7));
+                    const uint16_t *h = reinterpret_cast<const uint16_t *>(&raw);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float x = h2f(h[e]);
+                        acc = fmaf(x, x, acc);
+                    }
+                }
+                if (row0 + r < a.n_rows) a.knorm2[row0 + r] = acc;
+            }
+        }
+        if (it >= 1) {
+            epilogue(it - 1);
+            // MMA it-1 has completed: its B buffer takes tile it+1
+            if (it + 1 < n_my) {
+                load_b(it + 1, (it + 1) & 1);
+                cp_async_commit();
+            }
+        }
+        tc::fence_before_sync();
+    }
+    if (n_my > 0) epilogue(n_my - 1);
+    if (!ok && tid == 0) record_error(a.err, DS4A_ERR_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 2 * kTN);
+}
+
+// ---- per-query select on approximate scores with an exact band ------------------------------
+
+constexpr int kSelThreads = 256;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelMaxItems = 32;          // n_vis <= 8192
+constexpr int kBandCap = 1024;
+constexpr int kBins = 2048;               // 11-bit digits
+
+struct SelArgs {
+    const uint16_t *q_idx;
+    const uint16_t *k_idx;
+    float *scores;          // [n_q][ld] approximate scores (overwritten by exact keys on fallback)
+    const float *knorm2;
+    int32_t *out_idx;
+    int32_t *out_n;
+    long long n_rows;
+    long long q_pos0;
+    int d_idx;
+    int ratio;
+    int k;
+    int ld;
+};
+
+struct SelSmem {
+    uint32_t hist[kBins];
+    uint32_t cnt[kSelMaxItems * kSelWarps];
+    uint32_t scan[kSelWarps];
+    int band_idx[kBandCap];
+    uint32_t band_key[kBandCap];
+    uint32_t sel_bits[kSelMaxItems * kSelThreads / 32];
+    float red[kSelWarps];
+    uint32_t bin, above, count_bin, band_n, n_in;
+    float eps;
+};
+
+DS4A_DEVINL float key_to_float(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+DS4A_DEVINL uint32_t sel_block_excl_scan(uint32_t v, uint32_t *scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    __syncthreads();
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0;
+#pragma unroll
+    for (int w = 0; w < kSelWarps; ++w)
+        if (w < warp) before += scratch[w];
+    return before + incl - v;
+}
+
+DS4A_DEVINL float sel_block_max(float v, float *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_max(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float m = red[0];
+#pragma unroll
+    for (int w = 1; w < kSelWarps; ++w) m = fmaxf(m, red[w]);
+    return m;
+}
+
+// One radix pass over `bits` bits at `shift` among keys with (key & mask) == prefix:
+// finds the digit holding the kk-th largest; sets sm.bin, sm.above, sm.count_bin.
+template <int ITEMS>
+DS4A_DEVINL void radix_pass(const uint32_t (&key)[ITEMS], int n, uint32_t prefix, uint32_t mask, int shift,
+                            int bits, uint32_t kk, SelSmem &sm) {
+    const int tid = threadIdx.x;
+    const int nb = 1 << bits;
+    for (int b = tid; b < nb; b += kSelThreads) sm.hist[b] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        if (it * kSelThreads + tid < n && (key[it] & mask) == prefix)
+            atomicAdd(&sm.hist[(key[it] >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    // thread t covers bins nb-1-8t .. nb-8-8t (largest first)
+    const int per = nb / kSelThreads;   // 8 for 2048 bins, 4 for 1024
+    uint32_t lsum = 0;
+    for (int e = 0; e < per; ++e) lsum += sm.hist[nb - 1 - per * tid - e];
+    const uint32_t before = sel_block_excl_scan(lsum, sm.scan);
+    if (before < kk && before + lsum >= kk) {
+        uint32_t acc = before;
+        for (int e = 0; e < per; ++e) {
+            const uint32_t c = sm.hist[nb - 1 - per * tid - e];
+            if (acc + c >= kk) {
+                sm.bin = static_cast<uint32_t>(nb - 1 - per * tid - e);
+                sm.above = acc;
+                sm.count_bin = c;
+                break;
+            }
+            acc += c;
+        }
+    }
+    __syncthreads();
+}
+
+// TwoSum-exact score of one row, computed by a group of 16 threads (all 32 lanes of
+// every warp call this; `valid` masks the rows).
+DS4A_DEVINL uint32_t exact_key16(const uint16_t *q, const uint16_t *krow, int d_idx, bool valid) {
+    const int gl = threadIdx.x & 15;
+    float s = 0.f, c = 0.f;
+    for (int ch = gl; ch < d_idx / 8; ch += 16) {
+        if (valid) {
+            const uint4 qa = *reinterpret_cast<const uint4 *>(q + ch * 8);
+            const uint4 ka = __ldg(reinterpret_cast<const uint4 *>(krow + ch * 8));
+            const uint16_t *hq = reinterpret_cast<const uint16_t *>(&qa);
+            const uint16_t *hk = reinterpret_cast<const uint16_t *>(&ka);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float err;
+                two_sum(s, h2f(hq[e]) * h2f(hk[e]), s, err);
+                c += err;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        float err;
+        two_sum(s, s2, s, err);
+        c = (c + c2) + err;
+    }
+    return float_key(s + c);
+}
+
+// Ascending emission of the rows whose flag is set (flags per item bit), using
+// warp ballots and one scan over (item, warp) counts.
+template <int ITEMS>
+DS4A_DEVINL void emit(uint32_t flags, int32_t *out, SelSmem &sm) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const unsigned b = __ballot_sync(0xffffffffu, (flags >> it) & 1u);
+        if (lane == 0) sm.cnt[it * kSelWarps + warp] = __popc(b);
+    }
+    __syncthreads();
+    // exclusive scan of ITEMS * kSelWarps counts (<= 256 = one per thread)
+    const int m = ITEMS * kSelWarps;
+    const uint32_t v = tid < m ? sm.cnt[tid] : 0u;
+    const uint32_t ex = sel_block_excl_scan(v, sm.scan);
+    __syncthreads();
+    if (tid < m) sm.cnt[tid] = ex;
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const unsigned b = __ballot_sync(0xffffffffu, (flags >> it) & 1u);
+        if ((flags >> it) & 1u) out[sm.cnt[it * kSelWarps + warp] + __popc(b & lt)] = it * kSelThreads + tid;
+    }
+}
+
+template <int ITEMS>
+__global__ void __launch_bounds__(kSelThreads, 2) indexer_select_kernel(SelArgs a) {
+    __shared__ SelSmem sm;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.x;
+    long long nv = (a.q_pos0 + i + 1) / a.ratio;
+    const int n = static_cast<int>(nv < a.n_rows ? nv : a.n_rows);
+    int32_t *out = a.out_idx + static_cast<size_t>(i) * a.k;
+    if (a.out_n && tid == 0) a.out_n[i] = n < a.k ? n : a.k;
+    if (n <= a.k) {
+        for (int j = tid; j < a.k; j += kSelThreads) out[j] = j < n ? j : -1;
+        return;
+    }
+    const uint16_t *q = a.q_idx + static_cast<size_t>(i) * a.d_idx;
+    float *row = a.scores + static_cast<size_t>(i) * a.ld;
+
+    // error bound of the approximate scores
+    float kmax2 = 0.f;
+    for (int j = tid; j < n; j += kSelThreads) kmax2 = fmaxf(kmax2, a.knorm2[j]);
+    kmax2 = sel_block_max(kmax2, sm.red);
+    if (warp == 0) {
+        float qn2 = 0.f;
+        for (int c = lane; c < a.d_idx; c += 32) {
+            const float x = h2f(q[c]);
+            qn2 = fmaf(x, x, qn2);
+        }
+        qn2 = warp_sum(qn2);
+        if (lane == 0) sm.eps = ldexpf(sqrtf(qn2 * kmax2) * 1.01f, -12) + 1e-30f;
+    }
+
+    uint32_t key[ITEMS];
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int j = it * kSelThreads + tid;
+        key[it] = j < n ? float_key(row[j]) : 0u;
+    }
+    __syncthreads();
+    const float eps = sm.eps;
+
+    // bracket the k-th largest approximate score: bits 31..21, then 20..10
+    uint32_t kk = static_cast<uint32_t>(a.k);
+    radix_pass<ITEMS>(key, n, 0u, 0u, 21, 11, kk, sm);
+    uint32_t prefix = sm.bin << 21, mask = 0xFFE00000u;
+    kk -= sm.above;
+    radix_pass<ITEMS>(key, n, prefix, mask, 10, 11, kk, sm);
+    prefix |= sm.bin << 10;
+    const uint32_t lo_key = prefix, hi_key = prefix | 0x3FFu;
+    const float t_lo = key_to_float(lo_key), t_hi = key_to_float(hi_key);
+    const float big = fmaxf(fabsf(t_lo), fabsf(t_hi));
+    const float ulp = ldexpf(1.f, ilogbf(big > 0.f ? big : 1.f) - 23);
+    const float margin = 2.f * eps + 4.f * ulp;
+    const float in_thr = t_hi + margin, out_thr = t_lo - margin;
+
+    // classify: certainly in, certainly out, or band (rescored exactly)
+    if (tid == 0) {
+        sm.band_n = 0;
+        sm.n_in = 0;
+    }
+    for (int w = tid; w < ITEMS * kSelThreads / 32; w += kSelThreads) sm.sel_bits[w] = 0;
+    __syncthreads();
+    uint32_t flags = 0, my_in = 0;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int j = it * kSelThreads + tid;
+        if (j < n) {
+            const float s = key_to_float(key[it]);
+            if (s > in_thr) {
+                flags |= 1u << it;
+                ++my_in;
+            } else if (s >= out_thr) {
+                const uint32_t b = atomicAdd(&sm.band_n, 1u);
+                if (b < kBandCap) sm.band_idx[b] = j;
+            }
+        }
+    }
+    if (my_in) atomicAdd(&sm.n_in, my_in);
+    __syncthreads();
+    const uint32_t band_n = sm.band_n, n_in = sm.n_in;
+    const bool fits = band_n <= kBandCap && n_in <= static_cast<uint32_t>(a.k) &&
+                      n_in + band_n >= static_cast<uint32_t>(a.k);
+    if (fits) {
+        // exact keys of the band rows: 16 threads per row
+        for (uint32_t b0 = 0; b0 < band_n; b0 += kSelThreads / 16) {
+            const uint32_t b = b0 + tid / 16;
+            const bool valid = b < band_n;
+            const int j = valid ? sm.band_idx[b] : 0;
+            const uint32_t kx = exact_key16(q, a.k_idx + static_cast<size_t>(j) * a.d_idx, a.d_idx, valid);
+            if (valid && (tid & 15) == 0) sm.band_key[b] = kx;
+        }
+        __syncthreads();
+        // keep the (k - n_in) best band rows: higher exact key, then lower index
+        const uint32_t need = static_cast<uint32_t>(a.k) - n_in;
+        for (uint32_t b = tid; b < band_n; b += kSelThreads) {
+            const uint32_t kb = sm.band_key[b];
+            const int jb = sm.band_idx[b];
+            uint32_t rank = 0;
+            for (uint32_t o = 0; o < band_n; ++o) {
+                const uint32_t ko = sm.band_key[o];
+                rank += (ko > kb) || (ko == kb && sm.band_idx[o] < jb);
+            }
+            if (rank < need) atomicOr(&sm.sel_bits[jb >> 5], 1u << (jb & 31));
+        }
+        __syncthreads();
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) {
+            const int j = it * kSelThreads + tid;
+            if (j < n && ((sm.sel_bits[j >> 5] >> (j & 31)) & 1u)) flags |= 1u << it;
+        }
+        emit<ITEMS>(flags, out, sm);
+        return;
+    }
+
+    // fallback: exact keys for every visible row, then an exact radix select
+    for (int b0 = 0; b0 < ITEMS * kSelThreads; b0 += kSelThreads / 16) {
+        const int j = b0 + tid / 16;
+        const uint32_t kx = exact_key16(q, a.k_idx + static_cast<size_t>(j < n ? j : 0) * a.d_idx, a.d_idx, j < n);
+        if (j < n && (tid & 15) == 0) reinterpret_cast<uint32_t *>(row)[j] = kx;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int j = it * kSelThreads + tid;
+        key[it] = j < n ? reinterpret_cast<const uint32_t *>(row)[j] : 0u;
+    }
+    kk = static_cast<uint32_t>(a.k);
+    prefix = 0u;
+    mask = 0u;
+    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+    for (int p = 0; p < 3; ++p) {
+        radix_pass<ITEMS>(key, n, prefix, mask, shifts[p], widths[p], kk, sm);
+        kk -= sm.above;
+        prefix |= sm.bin << shifts[p];
+        mask |= ((1u << widths[p]) - 1u) << shifts[p];
+    }
+    // rows above the k-th key, then ties in index order up to kk of them
+    const unsigned lt = (1u << lane) - 1u;
+    uint32_t eqf = 0;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int j = it * kSelThreads + tid;
+        if (j < n && key[it] == prefix) eqf |= 1u << it;
+    }
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const unsigned b = __ballot_sync(0xffffffffu, (eqf >> it) & 1u);
+        if (lane == 0) sm.cnt[it * kSelWarps + warp] = __popc(b);
+    }
+    __syncthreads();
+    {
+        const int m = ITEMS * kSelWarps;
+        const uint32_t v = tid < m ? sm.cnt[tid] : 0u;
+        const uint32_t ex = sel_block_excl_scan(v, sm.scan);
+        __syncthreads();
+        if (tid < m) sm.cnt[tid] = ex;
+        __syncthreads();
+    }
+    flags = 0;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int j = it * kSelThreads + tid;
+        const unsigned b = __ballot_sync(0xffffffffu, (eqf >> it) & 1u);
+        const bool tie_kept = ((eqf >> it) & 1u) && sm.cnt[it * kSelWarps + warp] + __popc(b & lt) < kk;
+        if (j < n && (key[it] > prefix || tie_kept)) flags |= 1u << it;
+    }
+    __syncthreads();
+    emit<ITEMS>(flags, out, sm);
+}
+
+template <int DI>
+constexpr size_t gemm_smem() { return (DI / 64) * (kTM + 2 * kTN) * 128 + 1024; }
+
+}  // namespace
+
+bool indexer_prefill_tc_ok(int n_q, long long n_rows, int d_idx) {
+    return n_q >= 64 && (d_idx == 64 || d_idx == 128) && n_rows <= kSelThreads * kSelMaxItems;
+}
+
+size_t indexer_prefill_tc_ws_bytes(int n_q, long long n_rows) {
+    const long long ld = (n_rows + kTN - 1) / kTN * kTN;
+    return 256 + static_cast<size_t>(ld) * sizeof(float) + static_cast<size_t>(n_q) * ld * sizeof(float);
+}
+
+cudaError_t launch_indexer_prefill_tc(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
+                                      int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
+                                      int32_t *out_n, void *ws, const Ctx &c) {
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(indexer_scores_tc_kernel<64>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(gemm_smem<64>()));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(indexer_scores_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(gemm_smem<128>()));
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    const int ld = static_cast<int>((n_rows + kTN - 1) / kTN * kTN);
+    unsigned char *base = static_cast<unsigned char *>(ws) + 256;
+    float *knorm2 = reinterpret_cast<float *>(base);
+    float *scores = reinterpret_cast<float *>(base + static_cast<size_t>(ld) * sizeof(float));
+    TcScoreArgs g;
+    g.q_idx = q_idx;
+    g.k_idx = k_idx;
+    g.scores = scores;
+    g.knorm2 = knorm2;
+    g.err = c.err;
+    g.n_rows = n_rows;
+    g.n_q = n_q;
+    g.ld = ld;
+    g.n_ntiles = ld / kTN;
+    const int n_mtiles = (n_q + kTM - 1) / kTM;
+    g.n_split = c.num_sms / n_mtiles;
+    if (g.n_split < 1) g.n_split = 1;
+    if (g.n_split > g.n_ntiles) g.n_split = g.n_ntiles;
+    const dim3 grid(n_mtiles, g.n_split);
+    cudaError_t e = d_idx == 128
+                        ? launch(indexer_scores_tc_kernel<128>, grid, dim3(kGemmThreads), gemm_smem<128>(), c, 1, g)
+                        : launch(indexer_scores_tc_kernel<64>, grid, dim3(kGemmThreads), gemm_smem<64>(), c, 1, g);
+    if (e != cudaSuccess) return e;
+    SelArgs s{q_idx, k_idx, scores, knorm2, out_idx, out_n, n_rows, q_pos0, d_idx, ratio, k, ld};
+    const long long n_max = n_rows;
+    if (n_max <= 8 * kSelThreads) return launch(indexer_select_kernel<8>, dim3(n_q), dim3(kSelThreads), 0, c, 1, s);
+    if (n_max <= 16 * kSelThreads) return launch(indexer_select_kernel<16>, dim3(n_q), dim3(kSelThreads), 0, c, 1, s);
+    return launch(indexer_select_kernel<32>, dim3(n_q), dim3(kSelThreads), 0, c, 1, s);
+}
+
+}  // namespace ds4a

@@ -283,3 +283,26 @@ def test_compressor_chunk_split_and_token_by_token(ratio):
         check_out(got[1], ref_v, "rows V")
     np.testing.assert_allclose(chunks[0].astype(np.float32), whole[0].astype(np.float32), atol=2e-3)
     np.testing.assert_allclose(tokens[1].astype(np.float32), whole[1].astype(np.float32), atol=2e-3)
+
+
+def test_indexer_many_queries_tensor_core_path_with_ties():
+    """Many queries take the tensor-core scoring path.  Heavily duplicated key rows
+    put thousands of exact ties at the k-th score, which overflows the exactly
+    rescored band and exercises the exact fallback; ties must go to the lower index."""
+    rng = np.random.default_rng(8)
+    base = rng.standard_normal((4, 128)).astype(np.float16)
+    kidx = np.repeat(base, 2048, axis=0)                   # 8192 rows, 4 distinct
+    q = rng.standard_normal((64, 128)).astype(np.float16)
+    out, n, _ = _indexer_gpu(q, kidx, 4 * 8192, 4, 512)
+    for i in range(64):
+        ref = oracle.topk(oracle.index_scores(q[i], kidx), 512)
+        assert np.array_equal(out[i], ref), i
+    # random keys, many queries, mixed visibility (the approximate bracket + exact band path)
+    kidx = rng.standard_normal((3000, 64)).astype(np.float16)
+    q = rng.standard_normal((200, 64)).astype(np.float16)
+    out, n, _ = _indexer_gpu(q, kidx, 4 * 2900, 4, 300)
+    for i in range(0, 200, 7):
+        n_vis = min(3000, (4 * 2900 + i + 1) // 4)
+        scores = oracle.index_scores(q[i], kidx[:n_vis])
+        check_sel(out[i], oracle.topk(scores, 300), scores, 300, f"q{i}")
+    assert ds4a.ds4a_last_device_error() == 0
