@@ -25,7 +25,8 @@
 // start, waited on just before the first remote store, guarantees every peer
 // is running.  Window rows are cache state and are gathered before waiting on
 // the previous kernel.  No workspace, no second launch, no spin.
-// Prefill: one CTA per query walks the query's whole row list.
+// Prefill: one CTA per query walks the query's whole row list (the shapes the
+// tensor-core kernel in attention_tc.cu does not take).
 #include <cooperative_groups.h>
 
 #include "ds4a_common.cuh"
@@ -583,6 +584,18 @@ cudaError_t launch_attn_prefill(const uint16_t *q, int T, int H, int D, const ui
                                 const uint16_t *comp_k, const uint16_t *comp_v, long long n_comp,
                                 const int32_t *sel, int k_stride, long long q_pos0, int ratio,
                                 float scale, uint16_t *out, const Ctx &c) {
+    // the largest key list of any query: its window plus its selected (or visible) rows
+    long long max_keys = window;
+    if (ratio > 0) {
+        if (sel) max_keys += k_stride;
+        else {
+            const long long nv = (q_pos0 + T) / ratio;
+            max_keys += nv < n_comp ? nv : n_comp;
+        }
+    }
+    if (attn_prefill_tc_ok(H, D, max_keys))
+        return launch_attn_prefill_tc(q, T, raw_k, raw_v, n_prior, window, comp_k, comp_v, n_comp, sel, k_stride,
+                                      q_pos0, ratio, scale, out, c);
     PrefillArgs a{q, raw_k, raw_v, comp_k, comp_v, sel, out, c.err, n_comp, q_pos0,
                   H, n_prior, window, k_stride, ratio, scale * kLog2e};
     int cluster = 16;

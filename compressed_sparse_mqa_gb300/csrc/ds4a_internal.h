@@ -35,6 +35,13 @@ cudaError_t launch_attn_decode(const uint16_t *q, int H, int D, const uint16_t *
                                const uint16_t *comp_v, long long n_comp, const int32_t *sel,
                                int n_sel, float scale, uint16_t *out, const Ctx &c);
 
+// tensor-core prefill attention (64 heads, head_dim 128, <= 768 keys per query)
+bool attn_prefill_tc_ok(int H, int D, long long max_keys);
+cudaError_t launch_attn_prefill_tc(const uint16_t *q, int T, const uint16_t *raw_k, const uint16_t *raw_v,
+                                   int n_prior, int window, const uint16_t *comp_k, const uint16_t *comp_v,
+                                   long long n_comp, const int32_t *sel, int k_stride, long long q_pos0,
+                                   int ratio, float scale, uint16_t *out, const Ctx &c);
+
 cudaError_t launch_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *raw_k,
                                 const uint16_t *raw_v, int n_prior, int window,
                                 const uint16_t *comp_k, const uint16_t *comp_v, long long n_comp,
