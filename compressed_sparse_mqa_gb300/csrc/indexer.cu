@@ -10,11 +10,11 @@
 // fl(s + c) is the binary32 rounding of the exact score.  The ranking decision
 // is therefore taken on the correctly rounded binary32 score.
 //
-// Select.  Scores map to order-preserving u32 keys held in registers (16 or 32
-// per thread; larger row counts re-read them from memory).  A radix select over
-// 8-bit digits with one shared histogram per pass (plain shared atomics) finds
-// the k-th largest key, stopping early once the boundary digit holds exactly
-// the rows still needed.  Rows above the boundary, then
+// Select.  Scores map to order-preserving u32 keys held in registers (8, 16 or
+// 32 per thread; larger row counts re-read them from memory).  A radix select
+// over 11-bit digits with one shared histogram per pass (plain shared atomics)
+// finds the k-th largest key, stopping early once the boundary digit holds
+// exactly the rows still needed.  Rows above the boundary, then
 // boundary rows in ascending index order, are written in ascending index order
 // using warp ballots and one scan over (item, warp) counts.
 //
@@ -26,6 +26,7 @@
 // visible rows into shared memory and selects.
 #include "ds4a_common.cuh"
 #include "ds4a_internal.h"
+#include "select.cuh"
 
 namespace ds4a {
 namespace {
@@ -41,9 +42,10 @@ constexpr size_t kWsHeader = 256;                 // ticket lives here
 constexpr int kSmemKeyCap = 16384;                // prefill: keys staged in shared memory
 
 struct SelectSmem {
-    uint32_t hist[256];
+    uint32_t hist[sel::kMaxBins];
     uint32_t cnt[kMaxItems * kWarps];
     uint32_t scan[kWarps];
+    uint32_t res[3];
     uint32_t bin;
     uint32_t above;
     uint32_t count_bin;
@@ -146,17 +148,6 @@ DS4A_DEVINL uint32_t block_excl_scan(uint32_t v, uint32_t *scratch, uint32_t &to
     return before + incl - v;
 }
 
-// In-place exclusive scan of cnt[0..m), m <= 2 * kThreads.
-DS4A_DEVINL void scan_counts(uint32_t *cnt, int m, uint32_t *scratch) {
-    const int e0 = 2 * threadIdx.x, e1 = e0 + 1;
-    const uint32_t a = e0 < m ? cnt[e0] : 0u, b = e1 < m ? cnt[e1] : 0u;
-    uint32_t tot;
-    const uint32_t ex = block_excl_scan(a + b, scratch, tot);
-    if (e0 < m) cnt[e0] = ex;
-    if (e1 < m) cnt[e1] = ex + a;
-    __syncthreads();
-}
-
 // Histogram increment (b = 256 adds nothing).  Plain shared atomics: cheaper
 // here than aggregating equal digits across the warp first.
 DS4A_DEVINL void hist_add(uint32_t *hist, uint32_t b) {
@@ -201,69 +192,17 @@ DS4A_DEVINL uint32_t ld_key(const uint32_t *src, int i) {
 // Keys in registers: item `it` of thread t is index it * kThreads + t.  n > k.
 template <int ITEMS, bool GLOBAL>
 __device__ void select_regs(const uint32_t *src, int n, int k, int32_t *out, SelectSmem &sm) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const unsigned lt = (1u << lane) - 1u;
+    const int tid = threadIdx.x;
     uint32_t key[ITEMS];
 #pragma unroll
     for (int it = 0; it < ITEMS; ++it) {
         const int i = it * kThreads + tid;
         key[it] = i < n ? ld_key<GLOBAL>(src, i) : 0u;
     }
-    uint32_t prefix = 0, mask = 0, kk = static_cast<uint32_t>(k), count_eq = 0;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        if (tid < 256) sm.hist[tid] = 0;
-        __syncthreads();
-#pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-            const bool part = (it * kThreads + tid) < n && (key[it] & mask) == prefix;
-            hist_add(sm.hist, part ? (key[it] >> shift) & 255u : 256u);
-        }
-        __syncthreads();
-        find_bin(sm, kk);
-        __syncthreads();
-        kk -= sm.above;
-        prefix |= sm.bin << shift;
-        mask |= 255u << shift;
-        count_eq = sm.count_bin;
-        if (count_eq == kk) break;   // every boundary row is kept: no tie ranking needed
-    }
-    const bool all_eq = count_eq == kk;
-    uint32_t take_eq = 0u;
-    if (!all_eq) {
-        // rank the boundary rows in index order; keep the first kk
-#pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-            const bool eq = (it * kThreads + tid) < n && (key[it] & mask) == prefix;
-            const unsigned b = __ballot_sync(0xffffffffu, eq);
-            if (lane == 0) sm.cnt[it * kWarps + warp] = __popc(b);
-        }
-        __syncthreads();
-        scan_counts(sm.cnt, ITEMS * kWarps, sm.scan);
-#pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-            const bool eq = (it * kThreads + tid) < n && (key[it] & mask) == prefix;
-            const unsigned b = __ballot_sync(0xffffffffu, eq);
-            if (eq && sm.cnt[it * kWarps + warp] + __popc(b & lt) < kk) take_eq |= 1u << it;
-        }
-        __syncthreads();
-    }
-    // final flags, their warp ballots kept in registers, one scan of (item, warp) counts
-    unsigned fb[ITEMS];
-    uint32_t fbits = 0;
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const uint32_t km = key[it] & mask;
-        const bool f = (it * kThreads + tid) < n &&
-                       (km > prefix || (km == prefix && (all_eq || ((take_eq >> it) & 1u))));
-        fb[it] = __ballot_sync(0xffffffffu, f);
-        fbits |= static_cast<uint32_t>(f) << it;
-        if (lane == 0) sm.cnt[it * kWarps + warp] = __popc(fb[it]);
-    }
-    __syncthreads();
-    scan_counts(sm.cnt, ITEMS * kWarps, sm.scan);
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it)
-        if ((fbits >> it) & 1u) out[sm.cnt[it * kWarps + warp] + __popc(fb[it] & lt)] = it * kThreads + tid;
+    uint32_t prefix, mask, kk;
+    const bool all_eq = sel::find_threshold<kThreads, ITEMS>(key, n, k, sm.hist, sm.scan, sm.res, prefix, mask, kk);
+    const uint32_t flags = sel::topk_flags<kThreads, ITEMS>(key, n, prefix, mask, kk, all_eq, sm.cnt, sm.scan);
+    sel::emit<kThreads, ITEMS>(flags, out, sm.cnt, sm.scan);
 }
 
 // Any n > k: keys re-read from memory each pass; thread t emits the contiguous range [t*C, t*C + C).
@@ -316,6 +255,8 @@ template <bool GLOBAL>
 __device__ void select_topk(const uint32_t *src, int n, int k, int32_t *out, int32_t *out_n, SelectSmem &sm) {
     if (n <= k) {
         for (int i = threadIdx.x; i < k; i += kThreads) out[i] = i < n ? i : -1;
+    } else if (n <= kThreads * 8) {
+        select_regs<8, GLOBAL>(src, n, k, out, sm);
     } else if (n <= kThreads * 16) {
         select_regs<16, GLOBAL>(src, n, k, out, sm);
     } else if (n <= kThreads * kMaxItems) {
@@ -368,12 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
         load_rows(a.k_idx, a.d_idx, base, j1, L);
         score_loaded(qf, L, base, j1, keys + base);
     }
-    __threadfence();
+    // one acquire-release atomic per CTA: releases this CTA's keys (ordered before it
+    // by the barrier) and, for the last CTA, acquires everyone else's
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+    if (threadIdx.x == 0) {
+        unsigned int old;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;\n" : "=r"(old) : "l"(ticket) : "memory");
+        s_last = old == gridDim.x - 1;
+    }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     select_topk<true>(keys, static_cast<int>(n_vis), a.k, a.out_idx, a.out_n, sm);
     if (threadIdx.x == 0) *ticket = 0u;
 }

@@ -23,6 +23,7 @@
 //    to exact scores for every row and an exact radix select.
 #include "ds4a_common.cuh"
 #include "ds4a_internal.h"
+#include "select.cuh"
 #include "tcgen05.cuh"
 
 namespace ds4a {
@@ -208,30 +209,12 @@ struct SelSmem {
     uint32_t band_key[kBandCap];
     uint32_t sel_bits[kSelMaxItems * kSelThreads / 32];
     float red[kSelWarps];
-    uint32_t bin, above, count_bin, band_n, n_in;
+    uint32_t res[3], band_n, n_in;
     float eps;
 };
 
 DS4A_DEVINL float key_to_float(uint32_t key) {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
-
-DS4A_DEVINL uint32_t sel_block_excl_scan(uint32_t v, uint32_t *scratch) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    __syncthreads();
-    if (lane == 31) scratch[warp] = incl;
-    __syncthreads();
-    uint32_t before = 0;
-#pragma unroll
-    for (int w = 0; w < kSelWarps; ++w)
-        if (w < warp) before += scratch[w];
-    return before + incl - v;
 }
 
 DS4A_DEVINL float sel_block_max(float v, float *red) {
@@ -244,42 +227,6 @@ DS4A_DEVINL float sel_block_max(float v, float *red) {
 #pragma unroll
     for (int w = 1; w < kSelWarps; ++w) m = fmaxf(m, red[w]);
     return m;
-}
-
-// One radix pass over `bits` bits at `shift` among keys with (key & mask) == prefix:
-// finds the digit holding the kk-th largest; sets sm.bin, sm.above, sm.count_bin.
-template <int ITEMS>
-DS4A_DEVINL void radix_pass(const uint32_t (&key)[ITEMS], int n, uint32_t prefix, uint32_t mask, int shift,
-                            int bits, uint32_t kk, SelSmem &sm) {
-    const int tid = threadIdx.x;
-    const int nb = 1 << bits;
-    for (int b = tid; b < nb; b += kSelThreads) sm.hist[b] = 0;
-    __syncthreads();
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        if (it * kSelThreads + tid < n && (key[it] & mask) == prefix)
-            atomicAdd(&sm.hist[(key[it] >> shift) & (nb - 1)], 1u);
-    }
-    __syncthreads();
-    // thread t covers bins nb-1-8t .. nb-8-8t (largest first)
-    const int per = nb / kSelThreads;   // 8 for 2048 bins, 4 for 1024
-    uint32_t lsum = 0;
-    for (int e = 0; e < per; ++e) lsum += sm.hist[nb - 1 - per * tid - e];
-    const uint32_t before = sel_block_excl_scan(lsum, sm.scan);
-    if (before < kk && before + lsum >= kk) {
-        uint32_t acc = before;
-        for (int e = 0; e < per; ++e) {
-            const uint32_t c = sm.hist[nb - 1 - per * tid - e];
-            if (acc + c >= kk) {
-                sm.bin = static_cast<uint32_t>(nb - 1 - per * tid - e);
-                sm.above = acc;
-                sm.count_bin = c;
-                break;
-            }
-            acc += c;
-        }
-    }
-    __syncthreads();
 }
 
 // TwoSum-exact score of one row, computed by a group of 16 threads (all 32 lanes of
@@ -310,32 +257,6 @@ DS4A_DEVINL uint32_t exact_key16(const uint16_t *q, const uint16_t *krow, int d_
         c = (c + c2) + err;
     }
     return float_key(s + c);
-}
-
-// Ascending emission of the rows whose flag is set (flags per item bit), using
-// warp ballots and one scan over (item, warp) counts.
-template <int ITEMS>
-DS4A_DEVINL void emit(uint32_t flags, int32_t *out, SelSmem &sm) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const unsigned b = __ballot_sync(0xffffffffu, (flags >> it) & 1u);
-        if (lane == 0) sm.cnt[it * kSelWarps + warp] = __popc(b);
-    }
-    __syncthreads();
-    // exclusive scan of ITEMS * kSelWarps counts (<= 256 = one per thread)
-    const int m = ITEMS * kSelWarps;
-    const uint32_t v = tid < m ? sm.cnt[tid] : 0u;
-    const uint32_t ex = sel_block_excl_scan(v, sm.scan);
-    __syncthreads();
-    if (tid < m) sm.cnt[tid] = ex;
-    __syncthreads();
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const unsigned b = __ballot_sync(0xffffffffu, (flags >> it) & 1u);
-        if ((flags >> it) & 1u) out[sm.cnt[it * kSelWarps + warp] + __popc(b & lt)] = it * kSelThreads + tid;
-    }
 }
 
 template <int ITEMS>
@@ -381,11 +302,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) indexer_select_kernel(SelArgs 
 
     // bracket the k-th largest approximate score: bits 31..21, then 20..10
     uint32_t kk = static_cast<uint32_t>(a.k);
-    radix_pass<ITEMS>(key, n, 0u, 0u, 21, 11, kk, sm);
-    uint32_t prefix = sm.bin << 21, mask = 0xFFE00000u;
-    kk -= sm.above;
-    radix_pass<ITEMS>(key, n, prefix, mask, 10, 11, kk, sm);
-    prefix |= sm.bin << 10;
+    sel::radix_pass<kSelThreads, ITEMS>(key, n, 0u, 0u, 21, 11, kk, sm.hist, sm.scan, sm.res);
+    uint32_t prefix = sm.res[0] << 21, mask = 0xFFE00000u;
+    kk -= sm.res[1];
+    sel::radix_pass<kSelThreads, ITEMS>(key, n, prefix, mask, 10, 11, kk, sm.hist, sm.scan, sm.res);
+    prefix |= sm.res[0] << 10;
     const uint32_t lo_key = prefix, hi_key = prefix | 0x3FFu;
     const float t_lo = key_to_float(lo_key), t_hi = key_to_float(hi_key);
     const float big = fmaxf(fabsf(t_lo), fabsf(t_hi));
@@ -415,7 +336,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) indexer_select_kernel(SelArgs 
             }
         }
     }
-    if (my_in) atomicAdd(&sm.n_in, my_in);
+    my_in = __reduce_add_sync(0xffffffffu, my_in);
+    if (lane == 0 && my_in) atomicAdd(&sm.n_in, my_in);
     __syncthreads();
     const uint32_t band_n = sm.band_n, n_in = sm.n_in;
     const bool fits = band_n <= kBandCap && n_in <= static_cast<uint32_t>(a.k) &&
@@ -448,7 +370,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) indexer_select_kernel(SelArgs 
             const int j = it * kSelThreads + tid;
             if (j < n && ((sm.sel_bits[j >> 5] >> (j & 31)) & 1u)) flags |= 1u << it;
         }
-        emit<ITEMS>(flags, out, sm);
+        sel::emit<kSelThreads, ITEMS>(flags, out, sm.cnt, sm.scan);
         return;
     }
 
@@ -464,48 +386,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) indexer_select_kernel(SelArgs 
         const int j = it * kSelThreads + tid;
         key[it] = j < n ? reinterpret_cast<const uint32_t *>(row)[j] : 0u;
     }
-    kk = static_cast<uint32_t>(a.k);
-    prefix = 0u;
-    mask = 0u;
-    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
-    for (int p = 0; p < 3; ++p) {
-        radix_pass<ITEMS>(key, n, prefix, mask, shifts[p], widths[p], kk, sm);
-        kk -= sm.above;
-        prefix |= sm.bin << shifts[p];
-        mask |= ((1u << widths[p]) - 1u) << shifts[p];
-    }
-    // rows above the k-th key, then ties in index order up to kk of them
-    const unsigned lt = (1u << lane) - 1u;
-    uint32_t eqf = 0;
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const int j = it * kSelThreads + tid;
-        if (j < n && key[it] == prefix) eqf |= 1u << it;
-    }
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const unsigned b = __ballot_sync(0xffffffffu, (eqf >> it) & 1u);
-        if (lane == 0) sm.cnt[it * kSelWarps + warp] = __popc(b);
-    }
-    __syncthreads();
-    {
-        const int m = ITEMS * kSelWarps;
-        const uint32_t v = tid < m ? sm.cnt[tid] : 0u;
-        const uint32_t ex = sel_block_excl_scan(v, sm.scan);
-        __syncthreads();
-        if (tid < m) sm.cnt[tid] = ex;
-        __syncthreads();
-    }
-    flags = 0;
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const int j = it * kSelThreads + tid;
-        const unsigned b = __ballot_sync(0xffffffffu, (eqf >> it) & 1u);
-        const bool tie_kept = ((eqf >> it) & 1u) && sm.cnt[it * kSelWarps + warp] + __popc(b & lt) < kk;
-        if (j < n && (key[it] > prefix || tie_kept)) flags |= 1u << it;
-    }
-    __syncthreads();
-    emit<ITEMS>(flags, out, sm);
+    const bool all_eq = sel::find_threshold<kSelThreads, ITEMS>(key, n, a.k, sm.hist, sm.scan, sm.res, prefix, mask, kk);
+    flags = sel::topk_flags<kSelThreads, ITEMS>(key, n, prefix, mask, kk, all_eq, sm.cnt, sm.scan);
+    sel::emit<kSelThreads, ITEMS>(flags, out, sm.cnt, sm.scan);
 }
 
 template <int DI>

@@ -1,0 +1,154 @@
+// select.cuh -- block-wide pieces of the indexer's exact top-k select: a radix
+// pass over order-preserving u32 keys held in registers, block scans, and the
+// ascending-index emission of flagged rows.  Item `it` of thread t is row
+// it * NT + t (coalesced loads, index order = (item, warp, lane)).
+#pragma once
+
+#include <stdint.h>
+
+#include "ds4a_common.cuh"
+
+namespace ds4a {
+namespace sel {
+
+constexpr int kMaxBins = 2048;   // 11-bit digits
+
+// Exclusive scan of one value per thread across the block (NT threads).
+template <int NT>
+DS4A_DEVINL uint32_t block_excl_scan(uint32_t v, uint32_t *scratch /* NT/32 */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    __syncthreads();
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w)
+        if (w < warp) before += scratch[w];
+    return before + incl - v;
+}
+
+// One radix pass: among keys with (key & mask) == prefix, histogram the `bits`-bit
+// digit at `shift` and find the digit holding the kk-th largest key.  Writes
+// res[0] = digit, res[1] = keys in larger digits, res[2] = keys in the digit.
+template <int NT, int ITEMS>
+DS4A_DEVINL void radix_pass(const uint32_t (&key)[ITEMS], int n, uint32_t prefix, uint32_t mask, int shift,
+                            int bits, uint32_t kk, uint32_t *hist, uint32_t *scratch, uint32_t *res) {
+    const int tid = threadIdx.x;
+    const int nb = 1 << bits;
+    for (int b = tid; b < nb; b += NT) hist[b] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it)
+        if (it * NT + tid < n && (key[it] & mask) == prefix) atomicAdd(&hist[(key[it] >> shift) & (nb - 1)], 1u);
+    __syncthreads();
+    const int per = nb / NT;   // bins per thread, largest first
+    uint32_t lsum = 0;
+    for (int e = 0; e < per; ++e) lsum += hist[nb - 1 - per * tid - e];
+    const uint32_t before = block_excl_scan<NT>(lsum, scratch);
+    if (before < kk && before + lsum >= kk) {
+        uint32_t acc = before;
+        for (int e = 0; e < per; ++e) {
+            const uint32_t c = hist[nb - 1 - per * tid - e];
+            if (acc + c >= kk) {
+                res[0] = static_cast<uint32_t>(nb - 1 - per * tid - e);
+                res[1] = acc;
+                res[2] = c;
+                break;
+            }
+            acc += c;
+        }
+    }
+    __syncthreads();
+}
+
+// Exact k-th largest of n > k keys: up to three passes (11, 11, 10 bits),
+// stopping once the boundary digit holds exactly the rows still needed.
+// On return *prefix/*mask describe the boundary, *kk is the number of boundary
+// rows still to keep, and the result is `true` when every boundary row is kept.
+template <int NT, int ITEMS>
+DS4A_DEVINL bool find_threshold(const uint32_t (&key)[ITEMS], int n, int k, uint32_t *hist, uint32_t *scratch,
+                                uint32_t *res, uint32_t &prefix, uint32_t &mask, uint32_t &kk) {
+    prefix = 0u;
+    mask = 0u;
+    kk = static_cast<uint32_t>(k);
+    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+    for (int p = 0; p < 3; ++p) {
+        radix_pass<NT, ITEMS>(key, n, prefix, mask, shifts[p], widths[p], kk, hist, scratch, res);
+        kk -= res[1];
+        prefix |= res[0] << shifts[p];
+        mask |= ((1u << widths[p]) - 1u) << shifts[p];
+        if (res[2] == kk) return true;
+    }
+    return false;
+}
+
+// Write the rows whose flag bit is set, in ascending row order, to out[].
+template <int NT, int ITEMS>
+DS4A_DEVINL void emit(uint32_t flags, int32_t *out, uint32_t *cnt /* ITEMS*NT/32 <= NT */, uint32_t *scratch) {
+    static_assert(ITEMS * (NT / 32) <= NT, "one count per thread");
+    constexpr int kW = NT / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const unsigned b = __ballot_sync(0xffffffffu, (flags >> it) & 1u);
+        if (lane == 0) cnt[it * kW + warp] = __popc(b);
+    }
+    __syncthreads();
+    const uint32_t v = cnt[tid < ITEMS * kW ? tid : 0];
+    const uint32_t ex = block_excl_scan<NT>(tid < ITEMS * kW ? v : 0u, scratch);
+    if (tid < ITEMS * kW) cnt[tid] = ex;
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const unsigned b = __ballot_sync(0xffffffffu, (flags >> it) & 1u);
+        if ((flags >> it) & 1u) out[cnt[it * kW + warp] + __popc(b & lt)] = it * NT + threadIdx.x;
+    }
+}
+
+// Flags of the exact top-k given the boundary: rows above it, and boundary rows
+// in ascending index order up to kk of them (all of them when `all_eq`).
+template <int NT, int ITEMS>
+DS4A_DEVINL uint32_t topk_flags(const uint32_t (&key)[ITEMS], int n, uint32_t prefix, uint32_t mask, uint32_t kk,
+                                bool all_eq, uint32_t *cnt, uint32_t *scratch) {
+    constexpr int kW = NT / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    uint32_t gt = 0, eq = 0;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        if (it * NT + tid < n) {
+            const uint32_t km = key[it] & mask;
+            gt |= static_cast<uint32_t>(km > prefix) << it;
+            eq |= static_cast<uint32_t>(km == prefix) << it;
+        }
+    }
+    if (all_eq) return gt | eq;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const unsigned b = __ballot_sync(0xffffffffu, (eq >> it) & 1u);
+        if (lane == 0) cnt[it * kW + warp] = __popc(b);
+    }
+    __syncthreads();
+    const uint32_t v = cnt[tid < ITEMS * kW ? tid : 0];
+    const uint32_t ex = block_excl_scan<NT>(tid < ITEMS * kW ? v : 0u, scratch);
+    if (tid < ITEMS * kW) cnt[tid] = ex;
+    __syncthreads();
+    uint32_t take = 0;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const unsigned b = __ballot_sync(0xffffffffu, (eq >> it) & 1u);
+        if (((eq >> it) & 1u) && cnt[it * kW + warp] + __popc(b & lt) < kk) take |= 1u << it;
+    }
+    __syncthreads();   // cnt is reused by emit
+    return gt | take;
+}
+
+}  // namespace sel
+}  // namespace ds4a
