@@ -32,7 +32,6 @@ namespace {
 constexpr int kTM = 128;                 // queries per tile (MMA M)
 constexpr int kTN = 256;                 // rows per tile (MMA N)
 constexpr int kGemmThreads = 128;
-constexpr uint32_t kMaxPolls = 1u << 26;  // bounded mbarrier wait
 
 struct TcScoreArgs {
     const uint16_t *q_idx;
@@ -106,7 +105,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
     bool ok = true;
     auto epilogue = [&](int it) {
         const int buf = it & 1;
-        if (!tc::mbar_wait(&s_bar[buf], (it >> 1) & 1, kMaxPolls)) ok = false;
+        if (!tc::mbar_wait(&s_bar[buf], (it >> 1) & 1)) ok = false;
         tc::fence_after_sync();
         const int row = warp * 32 + lane;
         const int q = m0 + row;

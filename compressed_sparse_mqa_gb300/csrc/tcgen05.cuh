@@ -58,20 +58,35 @@ DS4A_DEVINL void mbar_init(uint64_t *bar, uint32_t count) {
 }
 DS4A_DEVINL void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory"); }
 
-// Bounded wait for the phase with the given parity to complete.  Returns false
-// if it did not within `max_iter` polls.
-DS4A_DEVINL bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t max_iter) {
+DS4A_DEVINL uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+// Each try_wait may suspend the thread in hardware (woken when the phase
+// completes) for up to this long, so waiting warps do not spin on issue slots
+// that the warps doing the work need.
+constexpr uint32_t kSuspendHintNs = 20000;
+
+// Bounded wait for the phase with the given parity to complete.  The bound is
+// wall-clock time (try_wait may itself suspend for a while, so a poll count is
+// no bound); returns false if the phase did not complete within `limit_ns`.
+DS4A_DEVINL bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = 1000000000ull) {
     const uint32_t a = smem_u32(bar);
-    for (uint32_t it = 0; it < max_iter; ++it) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
         uint32_t done;
         asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
             : "=r"(done)
-            : "r"(a), "r"(parity)
+            : "r"(a), "r"(parity), "r"(kSuspendHintNs)
             : "memory");
         if (done) return true;
+        const uint64_t now = globaltimer_ns();
+        if (it == 0) t0 = now;
+        else if (now - t0 > limit_ns) return false;
     }
-    return false;
 }
 
 DS4A_DEVINL void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
