@@ -584,16 +584,16 @@ cudaError_t launch_attn_prefill(const uint16_t *q, int T, int H, int D, const ui
                                 const uint16_t *comp_k, const uint16_t *comp_v, long long n_comp,
                                 const int32_t *sel, int k_stride, long long q_pos0, int ratio,
                                 float scale, uint16_t *out, const Ctx &c) {
-    // the largest key list of any query: its window plus its selected (or visible) rows
-    long long max_keys = window;
+    // the most selected (or visible) compressed rows of any query
+    long long max_sel = 0;
     if (ratio > 0) {
-        if (sel) max_keys += k_stride;
+        if (sel) max_sel = k_stride;
         else {
             const long long nv = (q_pos0 + T) / ratio;
-            max_keys += nv < n_comp ? nv : n_comp;
+            max_sel = nv < n_comp ? nv : n_comp;
         }
     }
-    if (attn_prefill_tc_ok(H, D, max_keys))
+    if (attn_prefill_tc_ok(q, T, H, D, n_prior, window, max_sel, n_comp))
         return launch_attn_prefill_tc(q, T, raw_k, raw_v, n_prior, window, comp_k, comp_v, n_comp, sel, k_stride,
                                       q_pos0, ratio, scale, out, c);
     PrefillArgs a{q, raw_k, raw_v, comp_k, comp_v, sel, out, c.err, n_comp, q_pos0,

@@ -1,4 +1,3 @@
-constexpr long long kWinTag = 1LL << 62;
 // attention_tc.cu -- prefill attention on the 5th-generation tensor cores.
 //
 // "DS4 (DwarfStar 4)", Architecture (64 query heads share one KV head, 128-token
@@ -14,25 +13,39 @@ constexpr long long kWinTag = 1LL << 62;
 //   O^T[d][head]  += sum_key V[key][d] P^T[key][head]   (A = V tile, MN-major; B = P^T, MN-major)
 // so both products run as M = 128 tiles.
 //
-// Warp roles (one persistent CTA per SM, each taking a contiguous block of queries):
-//   warps 8-10  producers: gather the key/value rows of each 128-key tile with
-//               16-byte cp.async into a 5-stage ring of 128-byte-swizzled tiles
-//               (about 160 KB in flight), in the order the MMAs consume them:
-//               K0, K1, V0, K2, V1, ..., V(n-1); the query block Q rides with K0.
-//               Each producer warp moves a third of every tile.
-//   warp 11     MMA issuer (one thread): S^T_c into one of two TMEM buffers, then
-//               O^T += V^T_(c-1) P^T_(c-1); tcgen05.commit releases ring stages
-//               and signals the softmax warps.
-//   warps 0-7   softmax + epilogue: warp w reads TMEM lane quadrant w%4 (keys)
-//               and heads 32*(w/4) .. +31.  Per tile: the per-head max across
-//               the 128 lanes (redux.sync on order-preserving keys, then the 4
-//               quadrants through shared memory), a lazy online softmax (O^T in
-//               TMEM is rescaled only when a head's max grows by more than 2^8),
-//               P^T (fp16) to shared memory.  Per query: the per-head sums, then
-//               O^T / l from TMEM to the output.
+// A query's key list is tile-aligned: its window tiles (raw rows), then its
+// compressed-row tiles, each padded with zero rows.
+//
+// Warp roles (one persistent CTA per SM, each taking a contiguous block of queries;
+// registers are rebalanced with setmaxnreg: 128 for softmax, 56 for the rest):
+//   warps 0-7    softmax + epilogue: warp w reads TMEM lane quadrant w%4 (keys)
+//                and heads 32*(w/4) .. +31; each warp keeps the running
+//                references of its 32 heads in shared memory.  Per tile: x = s*scale - m
+//                for its 32 scores, and one barrier-reduction per head half asks
+//                whether any x exceeds 8 (log2 units); only then is the exact
+//                tile max taken (redux.sync, then the 4 quadrants through shared
+//                memory) and O^T in TMEM rescaled.  P^T (fp16) goes to one of two
+//                shared buffers.  Per query: the per-head sums, then O^T / l from
+//                TMEM to the output.
+//   warp 8       row tables: the 32 lanes resolve the row of every key slot of
+//                the next query (window rows, then sel entries) into one of two
+//                shared tables, with a validity bit per slot.
+//   warp 9       MMA issuer (one thread): S^T_c into one of two TMEM buffers, then
+//                O^T += V^T_(c-1) P^T_(c-1); tcgen05.commit releases ring stages
+//                and signals the softmax warps.
+//   warps 10-23  TMA producers: fill a 5-stage ring of 128-byte-swizzled 32 KB
+//                tiles in the order the MMAs consume them: K0, K1, V0, K2, V1,
+//                ..., V(n-1).  A tile of scattered rows is 64 tile::gather4 loads
+//                (4 rows x 128 B each) shared out over the 14 warps -- a TMA
+//                instruction holds its issuing warp for a while, so the gather
+//                rate grows with the number of issuing warps; a full window tile
+//                is two plain 2-D tile loads.  The query block Q rides with K0.
+//                Completion is counted in bytes on each stage's mbarrier.
 // All hand-offs are mbarriers with time-bounded waits; a wait that gives up
 // records DS4A_ERR_TIMEOUT.  Warps that share a named barrier never leave their
 // loops early: after a failed wait they skip the work but keep the structure.
+#include <cuda.h>
+
 #include "ds4a_common.cuh"
 #include "ds4a_internal.h"
 #include "tcgen05.cuh"
@@ -43,52 +56,64 @@ namespace {
 constexpr int kH = 64;                      // heads (MMA N)
 constexpr int kD = 128;                     // head dim
 constexpr int kTK = 128;                    // keys per tile (MMA M)
-constexpr int kMaxTiles = 6;                // keys per query <= 768
+constexpr int kMaxTiles = 6;                // tiles per query
 constexpr int kNS = 5;                      // ring stages
-constexpr int kLag = kNS - 2;               // stages issued ahead of the oldest retired one
 constexpr int kSoftWarps = 8;
-constexpr int kProdWarps = 3;
-constexpr int kProdWarp = 8;                // first producer warp
-constexpr int kMmaWarp = kProdWarp + kProdWarps;
-constexpr int kThreads = 32 * (kSoftWarps + kProdWarps + 1);
+constexpr int kTblWarp = kSoftWarps;        // row tables
+constexpr int kMmaWarp = kTblWarp + 1;
+constexpr int kIssWarp0 = kMmaWarp + 1;     // first TMA producer warp
+constexpr int kIss = 14;                    // TMA producer warps
+constexpr int kWarps = kIssWarp0 + kIss;    // 24 = 6 warpgroups
+constexpr int kThreads = 32 * kWarps;
+constexpr int kLaunchRegs = 65536 / kThreads / 8 * 8;   // 80
+constexpr int kSoftRegs = 128, kOtherRegs = 56;
 constexpr int kTileBytes = kTK * kD * 2;    // 32 KB: [2 atoms][128 rows][128 B]
 constexpr int kQBytes = kH * kD * 2;        // 16 KB: [2 atoms][64 rows][128 B]
 constexpr int kPBytes = kTK * kH * 2;       // 16 KB: [128 key rows][128 B]
+constexpr int kGathers = kTK / 4 * 2;       // gather4 loads per tile (row groups x atom halves)
+constexpr int kMaskWords = kMaxTiles * 4;   // validity bits per query, 32 slots a word
 constexpr uint32_t kTmemCols = 256;         // S0 | S1 | O0 | O1, 64 columns each
 constexpr uint32_t kColS = 0, kColO = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescale = 8.f;             // lazy rescale threshold (log2 units)
 
+static_assert(kWarps % 4 == 0 && kSoftWarps % 4 == 0, "the register split is per warpgroup");
+static_assert(kSoftWarps * kSoftRegs + (kWarps - kSoftWarps) * kOtherRegs <= kWarps * kLaunchRegs,
+              "the register split exceeds what the block is launched with");
+
 struct Bars {
     uint64_t full[kNS], empty[kNS];
     uint64_t s_full[2], s_empty[2];
-    uint64_t p_full, p_empty;
+    uint64_t p_full[2], p_empty[2];
     uint64_t o_full[2], o_empty[2];
     uint64_t q_empty;
+    uint64_t tbl_full[2], tbl_empty[2];
 };
 
 struct SmemLayout {
     static constexpr int q = 0;
-    static constexpr int p = q + kQBytes;
-    static constexpr int ring = p + kPBytes;
-    static constexpr int tbl = ring + kNS * kTileBytes;                 // long long [768]
-    static constexpr int red = tbl + kMaxTiles * kTK * 8;               // float [2][4][64] max, [4][64] sum
-    static constexpr int bars = red + 3 * 4 * kH * 4;
+    static constexpr int p = q + kQBytes;                               // 2 buffers
+    static constexpr int ring = p + 2 * kPBytes;
+    static constexpr int tbl = ring + kNS * kTileBytes;                 // int [2][768] gather rows
+    static constexpr int mask = tbl + 2 * kMaxTiles * kTK * 4;          // uint32 [2][24] slot validity
+    static constexpr int red = mask + 2 * kMaskWords * 4;               // float [4][64] max, [4][64] sum, [64] 1/l
+    static constexpr int bars = red + (2 * 4 * kH + kH) * 4;
     static constexpr int end = bars + static_cast<int>(sizeof(Bars));
 };
 constexpr size_t kSmemBytes = SmemLayout::end + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 struct Args {
-    const uint16_t *q;
-    const uint16_t *raw_k;
-    const uint16_t *raw_v;
-    const uint16_t *comp_k;
-    const uint16_t *comp_v;
+    CUtensorMap map_raw_k, map_raw_v, map_comp_k, map_comp_v;   // one-row boxes (gathers)
+    CUtensorMap map_win_k, map_win_v;                           // 128-row boxes (window tiles)
+    CUtensorMap map_q;                                          // 64-row boxes
     const int32_t *sel;
     uint16_t *out;
     unsigned int *err;
-    long long n_comp;
+    int n_comp;      // compressed rows (< 2^31 - 1)
     long long q_pos0;
+    int n_raw;       // rows of the raw maps (n_prior + T): the zero-fill row
+    int comp_oob;    // rows of the compressed maps: the zero-fill row
     int T;
     int n_prior;
     int window;
@@ -116,6 +141,13 @@ DS4A_DEVINL void st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
         "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
         "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
 }
+DS4A_DEVINL void st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
+}
 DS4A_DEVINL void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 DS4A_DEVINL uint32_t redux_max_u32(uint32_t v) {
@@ -129,45 +161,99 @@ DS4A_DEVINL float key_to_float(uint32_t key) {
 DS4A_DEVINL void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(bar)) : "memory");
 }
-DS4A_DEVINL void softmax_barrier() { asm volatile("bar.sync 1, %0;\n" ::"n"(kSoftWarps * 32) : "memory"); }
-DS4A_DEVINL void producer_barrier() { asm volatile("bar.sync 2, %0;\n" ::"n"(kProdWarps * 32) : "memory"); }
+// named barriers 1 and 2: the four softmax warps of one head half (128 threads)
+DS4A_DEVINL void half_barrier(int half) { asm volatile("bar.sync %0, 128;\n" ::"r"(1 + half) : "memory"); }
+// the same barrier, returning whether any of the 128 threads passed pred = true
+DS4A_DEVINL bool half_any(int half, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(1 + half)
+        : "memory");
+    return r != 0;
+}
+template <int N> DS4A_DEVINL void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N)); }
+template <int N> DS4A_DEVINL void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N)); }
 
-// The key list of query i: its window rows, then its compressed rows.
+// lane l receives the sum over the warp's 32 lanes of v[l] (a butterfly that
+// halves the live values at each step: 31 shuffles in all)
+DS4A_DEVINL float transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? v[i] : v[i + s];
+            const float keep = upper ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0];
+}
+
+DS4A_DEVINL void expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(tc::smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+// 2-D TMA tile load (x = column, y = row) completing on bar
+DS4A_DEVINL void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(tc::smem_u32(dst)),
+                 "l"(map), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
+                 : "memory");
+}
+// four rows r.x .. r.w, columns x .. x+63, to 4 consecutive 128-byte rows at dst
+DS4A_DEVINL void tma_gather4(uint32_t dst, const CUtensorMap *map, int x, int4 r, uint64_t *bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
+                 "l"(map), "r"(x), "r"(r.x), "r"(r.y), "r"(r.z), "r"(r.w), "r"(tc::smem_u32(bar))
+                 : "memory");
+}
+DS4A_DEVINL void prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(map) : "memory");
+}
+
+// The key list of query i: its window rows padded to whole tiles, then its
+// compressed rows padded to whole tiles.
 struct QueryKeys {
-    long long raw0;   // raw index of the first window row
-    int n_w;
-    int n_sel;
-    int n_tiles;
+    int raw0;         // raw index of the first window row
+    int n_w;          // window rows
+    int n_sel;        // compressed-row slots
+    int n_wt;         // window tiles
+    int n_tiles;      // window tiles + compressed-row tiles
 };
 DS4A_DEVINL QueryKeys query_keys(const Args &a, int i) {
     QueryKeys k;
     const long long p = a.q_pos0 + i;
     const long long first = p - a.window + 1 > 0 ? p - a.window + 1 : 0;
-    k.raw0 = first - (a.q_pos0 - a.n_prior);
+    k.raw0 = static_cast<int>(first - (a.q_pos0 - a.n_prior));
     k.n_w = static_cast<int>(p - first + 1);
     k.n_sel = 0;
     if (a.ratio > 0) {
         if (a.sel) k.n_sel = a.k_stride;
         else {
             const long long nv = (p + 1) / a.ratio;
-            k.n_sel = static_cast<int>(nv < a.n_comp ? nv : a.n_comp);
+            k.n_sel = static_cast<int>(nv < a.n_comp ? nv : static_cast<long long>(a.n_comp));
         }
     }
-    k.n_tiles = (k.n_w + k.n_sel + kTK - 1) / kTK;
+    k.n_wt = (k.n_w + kTK - 1) / kTK;
+    k.n_tiles = k.n_wt + (k.n_sel + kTK - 1) / kTK;
     return k;
 }
-// element offset of key kx's row (window rows tagged), -1 for padding (past the
-// list, negative sel entries, or out-of-range rows, which are also recorded)
-DS4A_DEVINL long long key_offset(const Args &a, int i, const QueryKeys &k, int kx, bool record) {
-    if (kx < k.n_w) return kWinTag | ((k.raw0 + kx) * kD);
-    if (kx >= k.n_w + k.n_sel) return -1;
-    const long long j = a.sel ? static_cast<long long>(__ldg(a.sel + static_cast<size_t>(i) * a.k_stride + (kx - k.n_w)))
-                              : static_cast<long long>(kx - k.n_w);
+// row of key slot kx in its tensor (raw rows in the window tiles, compressed
+// rows after them); -1 for padding, a negative sel entry or an out-of-range one
+// (which is also recorded)
+DS4A_DEVINL int slot_row(const Args &a, int i, const QueryKeys &k, int kx, bool record) {
+    const int w = kx - k.n_wt * kTK;
+    if (w < 0) return kx < k.n_w ? k.raw0 + kx : -1;
+    if (w >= k.n_sel) return -1;
+    const int j = a.sel ? __ldg(a.sel + static_cast<size_t>(i) * a.k_stride + w) : w;
     if (j >= a.n_comp) {
         if (record) record_error(a.err, DS4A_ERR_DEVICE_INDEX);
         return -1;
     }
-    return j >= 0 ? j * kD : -1;
+    return j >= 0 ? j : -1;
 }
 // ring event e (0 .. 2n-1) of a query with n tiles: K0, K1, V0, K2, V1, ..., V(n-1)
 DS4A_DEVINL void ring_event(int e, int n, bool &is_v, int &tile) {
@@ -177,32 +263,39 @@ DS4A_DEVINL void ring_event(int e, int n, bool &is_v, int &tile) {
     else { is_v = true; tile = e / 2 - 1; }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(Args a) {
+
+__global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(const __grid_constant__ Args a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char *q_s = smem + SmemLayout::q;
     unsigned char *p_s = smem + SmemLayout::p;
     unsigned char *ring = smem + SmemLayout::ring;
-    long long *tbl = reinterpret_cast<long long *>(smem + SmemLayout::tbl);
-    float *red_max = reinterpret_cast<float *>(smem + SmemLayout::red);   // [2][4][64]
-    float *red_sum = red_max + 2 * 4 * kH;                                // [4][64]
+    int *tbl = reinterpret_cast<int *>(smem + SmemLayout::tbl);
+    uint32_t *mask = reinterpret_cast<uint32_t *>(smem + SmemLayout::mask);
+    float *red_max = reinterpret_cast<float *>(smem + SmemLayout::red);   // [4][64]
+    float *red_sum = red_max + 4 * kH;                                    // [4][64]
+    float *red_inv = red_sum + 4 * kH;                                    // [64]
     Bars &bar = *reinterpret_cast<Bars *>(smem + SmemLayout::bars);
     __shared__ uint32_t s_tmem;
+    __shared__ __align__(16) float s_alpha[kSoftWarps][32];
+    __shared__ __align__(16) float s_mh[kSoftWarps][32];   // running reference per head (log2 units)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
         for (int s = 0; s < kNS; ++s) {
-            tc::mbar_init(&bar.full[s], kProdWarps);
+            tc::mbar_init(&bar.full[s], kIss);
             tc::mbar_init(&bar.empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&bar.s_full[b], 1);
             tc::mbar_init(&bar.s_empty[b], kSoftWarps);
+            tc::mbar_init(&bar.p_full[b], kSoftWarps);
+            tc::mbar_init(&bar.p_empty[b], 1);
             tc::mbar_init(&bar.o_full[b], 1);
             tc::mbar_init(&bar.o_empty[b], kSoftWarps);
+            tc::mbar_init(&bar.tbl_full[b], 32);
+            tc::mbar_init(&bar.tbl_empty[b], kIss + kSoftWarps);
         }
-        tc::mbar_init(&bar.p_full, kSoftWarps);
-        tc::mbar_init(&bar.p_empty, 1);
         tc::mbar_init(&bar.q_empty, 1);
         tc::mbar_fence_init();
     }
@@ -225,167 +318,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(Args a) {
         return ok;
     };
 
-    if (warp >= kProdWarp && warp < kMmaWarp) {
-        // ---------------- producers: K/V tiles (and Q) into the ring ----------------
-        const int pt = (warp - kProdWarp) * 32 + lane;   // 0 .. 95
-        constexpr int kPT = kProdWarps * 32;
-        long long g = 0;
-        int pending = 0, t = 0;
-        auto retire = [&](long long ev) {
-            tc::fence_proxy_async();   // this lane's cp.async and zero stores -> tensor-core reads
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar.full[ev % kNS]);
-        };
-        for (int i = q_begin; i < q_end; ++i, ++t) {
-            const QueryKeys k = query_keys(a, i);
-            // the query's row table: every sel load issued before any is used
-            constexpr int kPer = (kMaxTiles * kTK + kPT - 1) / kPT;
-            long long offs[kPer];
-#pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-                const int kx = pt + j * kPT;
-                offs[j] = kx < k.n_tiles * kTK ? key_offset(a, i, k, kx, true) : -1;
-            }
-#pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-                const int kx = pt + j * kPT;
-                if (kx < k.n_tiles * kTK) tbl[kx] = offs[j];
-            }
-            producer_barrier();
-            for (int e = 0; e < 2 * k.n_tiles; ++e, ++g) {
-                const int s = static_cast<int>(g % kNS);
-                if (g >= kNS) wait(&bar.empty[s], static_cast<uint32_t>((g / kNS) - 1) & 1u);
-                bool is_v;
-                int c;
-                ring_event(e, k.n_tiles, is_v, c);
-                if (e == 0 && t > 0) {
-                    // The MMAs of the previous query need every stage issued so far:
-                    // retire them all before waiting for those MMAs to free the Q block.
-                    cp_async_wait<0>();
-                    for (; pending > 0; --pending) retire(g - pending);
-                    wait(&bar.q_empty, static_cast<uint32_t>(t - 1) & 1u);
-                }
-                if (!ok) continue;
-                if (e == 0) {
-                    for (int idx = pt; idx < kH * (kD / 8); idx += kPT) {
-                        const int r = idx >> 4, ch = idx & 15;
-                        cp_async16(q_s + (ch >> 3) * (kH * 128) + tc::sw128_chunk(r, ch & 7),
-                                   a.q + (static_cast<size_t>(i) * kH + r) * kD + ch * 8);
-                    }
-                }
-                unsigned char *dst = ring + s * kTileBytes;
-                const uint16_t *raw = is_v ? a.raw_v : a.raw_k;
-                const uint16_t *comp = is_v ? a.comp_v : a.comp_k;
-                // all of this thread's sources first (table loads in flight together),
-                // then the copies back to back
-                constexpr int kChunksPer = (kTK * (kD / 8) + kPT - 1) / kPT;
-                const uint16_t *src[kChunksPer];
-#pragma unroll
-                for (int j = 0; j < kChunksPer; ++j) {
-                    const int idx = pt + j * kPT;
-                    src[j] = nullptr;
-                    if (idx < kTK * (kD / 8)) {
-                        const int r = idx >> 4, ch = idx & 15;
-                        const long long o = tbl[c * kTK + r];
-                        if (o >= 0) src[j] = (o & kWinTag) ? raw + ((o & ~kWinTag) + ch * 8) : comp + (o + ch * 8);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < kChunksPer; ++j) {
-                    const int idx = pt + j * kPT;
-                    if (idx < kTK * (kD / 8)) {
-                        const int r = idx >> 4, ch = idx & 15;
-                        unsigned char *d = dst + (ch >> 3) * (kTK * 128) + tc::sw128_chunk(r, ch & 7);
-                        if (src[j]) cp_async16(d, src[j]);
-                        else *reinterpret_cast<uint4 *>(d) = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                cp_async_commit();
-                if (++pending > kLag) {
-                    cp_async_wait<kLag>();
-                    retire(g - kLag);
-                    --pending;
-                }
-            }
-            producer_barrier();   // the table is rewritten by the next query
-        }
-        cp_async_wait<0>();
-        for (; pending > 0; --pending) retire(g - pending);
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            constexpr uint32_t kIdS = tc::idesc_f16_f32(kTK, kH, false, false);
-            constexpr uint32_t kIdO = tc::idesc_f16_f32(kTK, kH, true, true);
-            long long g = 0, gs = 0, gp = 0;
-            int t = 0;
-            for (int i = q_begin; i < q_end && ok; ++i, ++t) {
-                const QueryKeys k = query_keys(a, i);
-                const int n = k.n_tiles;
-                const uint32_t obuf = static_cast<uint32_t>(t & 1);
-                auto issue_pv = [&](int c) {
-                    const long long ev = g++;
-                    const int s = static_cast<int>(ev % kNS);
-                    wait(&bar.full[s], static_cast<uint32_t>(ev / kNS) & 1u);
-                    wait(&bar.p_full, static_cast<uint32_t>(gp) & 1u);
-                    if (c == 0 && t >= 2) wait(&bar.o_empty[obuf], static_cast<uint32_t>((t >> 1) - 1) & 1u);
-                    if (!ok) return;
-                    tc::fence_after_sync();
-                    const uint32_t va = tc::smem_u32(ring + s * kTileBytes), pb = tc::smem_u32(p_s);
-#pragma unroll
-                    for (int st = 0; st < kTK / 16; ++st) {
-                        const uint64_t da = tc::desc_sw128(va + st * 2048, kTK * 128, 1024);
-                        const uint64_t db = tc::desc_sw128(pb + st * 16 * 128, 8192, 1024);
-                        tc::mma_f16(tmem + kColO + obuf * kH, da, db, kIdO, (c > 0 || st > 0) ? 1u : 0u);
-                    }
-                    tc::commit(&bar.p_empty);
-                    tc::commit(&bar.empty[s]);
-                    if (c == n - 1) tc::commit(&bar.o_full[obuf]);
-                    ++gp;
-                };
-                for (int c = 0; c < n && ok; ++c) {
-                    const long long ev = g++;
-                    const int s = static_cast<int>(ev % kNS);
-                    wait(&bar.full[s], static_cast<uint32_t>(ev / kNS) & 1u);
-                    const uint32_t sb = static_cast<uint32_t>(gs & 1);
-                    if (gs >= 2) wait(&bar.s_empty[sb], static_cast<uint32_t>((gs >> 1) - 1) & 1u);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    const uint32_t ka = tc::smem_u32(ring + s * kTileBytes), qb = tc::smem_u32(q_s);
-#pragma unroll
-                    for (int st = 0; st < kD / 16; ++st) {
-                        const uint64_t da = tc::desc_sw128(ka + (st / 4) * (kTK * 128) + (st % 4) * 32, 16, 1024);
-                        const uint64_t db = tc::desc_sw128(qb + (st / 4) * (kH * 128) + (st % 4) * 32, 16, 1024);
-                        tc::mma_f16(tmem + kColS + sb * kH, da, db, kIdS, st > 0 ? 1u : 0u);
-                    }
-                    tc::commit(&bar.s_full[sb]);
-                    tc::commit(&bar.empty[s]);
-                    if (c == n - 1) tc::commit(&bar.q_empty);
-                    ++gs;
-                    if (c >= 1) issue_pv(c - 1);
-                }
-                if (ok) issue_pv(n - 1);
-            }
-        }
-        __syncwarp();
-    }
-    else {
+    if (warp < kSoftWarps) {
+        setmaxnreg_inc<kSoftRegs>();
         // ---------------- softmax + epilogue (warps 0-7) ----------------
         const int quad = warp & 3, half = warp >> 2;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t kNegInfKey = float_key(-INFINITY);
-        long long gs = 0, gp = 0;
+        const float c2 = a.scale_log2;
+        uint32_t gs = 0, gp = 0;
         int t = 0;
         for (int i = q_begin; i < q_end; ++i, ++t) {
             const QueryKeys k = query_keys(a, i);
             const int n = k.n_tiles;
             const uint32_t obuf = static_cast<uint32_t>(t & 1);
+            // validity of this warp's 32 keys in each tile, from the row table's bits
+            const int b = t & 1;
+            wait(&bar.tbl_full[b], static_cast<uint32_t>(t >> 1) & 1u);
             uint32_t vbits = 0;
-            for (int c = 0; c < n; ++c)
-                if (key_offset(a, i, k, c * kTK + quad * 32 + lane, false) >= 0) vbits |= 1u << c;
-            float mh = -INFINITY;   // running reference of head half*32 + lane (log2 units)
-            float l_lane[32];
+            for (int c = 0; c < n; ++c) vbits |= ((mask[b * kMaskWords + c * 4 + quad] >> lane) & 1u) << c;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar.tbl_empty[b]);
+            float l_lane[32];   // this lane's key: partial softmax sums of the 32 heads
 #pragma unroll
             for (int h = 0; h < 32; ++h) l_lane[h] = 0.f;
+            float *mh = s_mh[warp];   // this warp's copy of the references of its 32 heads
+            mh[lane] = -INFINITY;
+            __syncwarp();
             for (int c = 0; c < n; ++c) {
                 const uint32_t sb = static_cast<uint32_t>(gs & 1);
                 wait(&bar.s_full[sb], static_cast<uint32_t>(gs >> 1) & 1u);
@@ -397,84 +355,130 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(Args a) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar.s_empty[sb]);
                 const bool valid = (vbits >> c) & 1u;
-                // tile max of each head across the 128 lanes: warp, then the 4 quadrants
-                float *rm = red_max + (gs & 1) * (4 * kH);
+                float mx = -INFINITY;
 #pragma unroll
-                for (int h = 0; h < 32; ++h) {
-                    const uint32_t m = redux_max_u32(valid ? float_key(__uint_as_float(r[h])) : kNegInfKey);
-                    if (lane == h) rm[quad * kH + half * 32 + h] = key_to_float(m);
+                for (int h4 = 0; h4 < 8; ++h4) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(mh + h4 * 4);
+                    mx = fmaxf(mx, fmaf(__uint_as_float(r[h4 * 4 + 0]), c2, -m4.x));
+                    mx = fmaxf(mx, fmaf(__uint_as_float(r[h4 * 4 + 1]), c2, -m4.y));
+                    mx = fmaxf(mx, fmaf(__uint_as_float(r[h4 * 4 + 2]), c2, -m4.z));
+                    mx = fmaxf(mx, fmaf(__uint_as_float(r[h4 * 4 + 3]), c2, -m4.w));
                 }
-                softmax_barrier();
-                float tm = rm[half * 32 + lane];
+                if (!valid) mx = -INFINITY;
+                if (half_any(half, mx > kRescale)) {
+                    // some head grew past its reference: the exact tile max of each head
+                    // across the 128 keys (warp, then the 4 quadrants), new references
 #pragma unroll
-                for (int qd = 1; qd < 4; ++qd) tm = fmaxf(tm, rm[qd * kH + half * 32 + lane]);
-                const float target = tm * a.scale_log2;   // scale > 0: the max commutes with it
-                float alpha = 1.f;
-                bool grow = false;
-                if (mh == -INFINITY) {
-                    mh = target;
-                } else if (target > mh + kRescale) {
-                    alpha = exp2f(mh - target);
-                    mh = target;
-                    grow = true;
-                }
-                const bool any_grow = __any_sync(0xffffffffu, grow);
-                // the PV of the previous tile has finished with P^T and with O^T
-                if (gp >= 1) wait(&bar.p_empty, static_cast<uint32_t>(gp - 1) & 1u);
-                tc::fence_after_sync();
-                if (any_grow) {
+                    for (int h = 0; h < 32; ++h) {
+                        const uint32_t m = redux_max_u32(valid ? float_key(__uint_as_float(r[h])) : kNegInfKey);
+                        if (lane == h) red_max[quad * kH + half * 32 + h] = key_to_float(m);
+                    }
+                    half_barrier(half);
+                    bool rescale = false;
+                    float my_new = 0.f;   // the new reference of head `lane`
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) l_lane[h] *= __shfl_sync(0xffffffffu, alpha, h);
-                    if (c > 0) {
-                        uint32_t o[32];
-                        const uint32_t oa = tmem + lane_base + kColO + obuf * kH + half * 32;
-                        ld_x32(oa, o);
-                        tc::wait_ld();
+                    for (int h4 = 0; h4 < 8; ++h4) {
+                        float4 m4 = *reinterpret_cast<const float4 *>(red_max + half * 32 + h4 * 4);
 #pragma unroll
-                        for (int h = 0; h < 32; ++h)
-                            o[h] = __float_as_uint(__uint_as_float(o[h]) * __shfl_sync(0xffffffffu, alpha, h));
-                        st_x32(oa, o);
+                        for (int qd = 1; qd < 4; ++qd) {
+                            const float4 o4 = *reinterpret_cast<const float4 *>(red_max + qd * kH + half * 32 + h4 * 4);
+                            m4.x = fmaxf(m4.x, o4.x);
+                            m4.y = fmaxf(m4.y, o4.y);
+                            m4.z = fmaxf(m4.z, o4.z);
+                            m4.w = fmaxf(m4.w, o4.w);
+                        }
+                        const float tm[4] = {m4.x, m4.y, m4.z, m4.w};
+                        const float4 old4 = *reinterpret_cast<const float4 *>(mh + h4 * 4);
+                        const float old[4] = {old4.x, old4.y, old4.z, old4.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int h = h4 * 4 + u;
+                            const float target = tm[u] * c2;   // scale > 0: the max commutes with it
+                            float alpha = 1.f, m_new = old[u];
+                            if (old[u] == -INFINITY) {
+                                m_new = target;
+                                alpha = 0.f;   // nothing accumulated yet
+                            } else if (target > old[u] + kRescale) {
+                                alpha = exp2f(old[u] - target);
+                                m_new = target;
+                            }
+                            rescale |= alpha != 1.f;
+                            l_lane[h] *= alpha;
+                            if (lane == h) {
+                                s_alpha[warp][h] = alpha;
+                                my_new = m_new;
+                            }
+                        }
+                    }
+                    __syncwarp();   // every lane has read the old references
+                    mh[lane] = my_new;
+                    __syncwarp();
+                    if (c > 0 && rescale) {
+                        // O^T holds the earlier tiles once the previous PV is done
+                        wait(&bar.p_empty[(gp - 1) & 1], static_cast<uint32_t>((gp - 1) >> 1) & 1u);
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int part = 0; part < 2; ++part) {   // 16 columns at a time
+                            uint32_t o[16];
+                            const uint32_t oa = tmem + lane_base + kColO + obuf * kH + half * 32 + part * 16;
+                            tc::ld_x16(oa, o);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int h4 = 0; h4 < 4; ++h4) {
+                                const float4 al = *reinterpret_cast<const float4 *>(&s_alpha[warp][part * 16 + h4 * 4]);
+                                o[h4 * 4 + 0] = __float_as_uint(__uint_as_float(o[h4 * 4 + 0]) * al.x);
+                                o[h4 * 4 + 1] = __float_as_uint(__uint_as_float(o[h4 * 4 + 1]) * al.y);
+                                o[h4 * 4 + 2] = __float_as_uint(__uint_as_float(o[h4 * 4 + 2]) * al.z);
+                                o[h4 * 4 + 3] = __float_as_uint(__uint_as_float(o[h4 * 4 + 3]) * al.w);
+                            }
+                            st_x16(oa, o);
+                        }
                         wait_st();
                     }
                 }
                 // p = 2^(s * scale - m) -> the P^T row (key) of this lane, 32 heads
-                const int key = quad * 32 + lane;
                 uint32_t pk[16];
 #pragma unroll
-                for (int h = 0; h < 32; h += 2) {
-                    const float m0 = __shfl_sync(0xffffffffu, mh, h), m1 = __shfl_sync(0xffffffffu, mh, h + 1);
-                    const float p0 = valid ? exp2f(__uint_as_float(r[h]) * a.scale_log2 - m0) : 0.f;
-                    const float p1 = valid ? exp2f(__uint_as_float(r[h + 1]) * a.scale_log2 - m1) : 0.f;
-                    l_lane[h] += p0;
-                    l_lane[h + 1] += p1;
-                    pk[h / 2] = pack_half2(p0, p1);
+                for (int h4 = 0; h4 < 8; ++h4) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(mh + h4 * 4);
+                    const float m[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; u += 2) {
+                        const int h = h4 * 4 + u;
+                        const float p0 = valid ? exp2f(fmaf(__uint_as_float(r[h]), c2, -m[u])) : 0.f;
+                        const float p1 = valid ? exp2f(fmaf(__uint_as_float(r[h + 1]), c2, -m[u + 1])) : 0.f;
+                        l_lane[h] += p0;
+                        l_lane[h + 1] += p1;
+                        pk[h / 2] = pack_half2(p0, p1);
+                    }
                 }
+                const uint32_t pb = static_cast<uint32_t>(gp & 1);
+                // the PV two tiles back has finished with this P buffer
+                if (gp >= 2) wait(&bar.p_empty[pb], static_cast<uint32_t>((gp >> 1) - 1) & 1u);
+                unsigned char *pbuf = p_s + pb * kPBytes;
+                const int key = quad * 32 + lane;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const int ch = half * 4 + q4;
-                    *reinterpret_cast<uint4 *>(p_s + key * 128 + ((ch ^ (key & 7)) << 4)) =
+                    *reinterpret_cast<uint4 *>(pbuf + key * 128 + ((ch ^ (key & 7)) << 4)) =
                         make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
                 }
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar.p_full);
+                if (lane == 0) mbar_arrive(&bar.p_full[pb]);
                 ++gs;
                 ++gp;
             }
             // ---- per-head sums, then O^T / l to the output ----
-#pragma unroll
-            for (int h = 0; h < 32; ++h) {
-                float s = l_lane[h];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == h) red_sum[quad * kH + half * 32 + h] = s;
-            }
-            softmax_barrier();
+            const float part = transpose_sum32(l_lane, lane);   // head half*32 + lane, this warp's keys
+            red_sum[quad * kH + half * 32 + lane] = part;
+            half_barrier(half);
             float lsum = red_sum[half * 32 + lane];
 #pragma unroll
             for (int qd = 1; qd < 4; ++qd) lsum += red_sum[qd * kH + half * 32 + lane];
-            const float inv = 1.f / lsum;
+            if (quad == 0) red_inv[half * 32 + lane] = 1.f / lsum;
+            half_barrier(half);
             wait(&bar.o_full[obuf], static_cast<uint32_t>(t >> 1) & 1u);
             tc::fence_after_sync();
             uint32_t o[32];
@@ -485,8 +489,168 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(Args a) {
             if (lane == 0) mbar_arrive(&bar.o_empty[obuf]);
             uint16_t *dst = a.out + (static_cast<size_t>(i) * kH + half * 32) * kD + quad * 32 + lane;
 #pragma unroll
-            for (int h = 0; h < 32; ++h) dst[h * kD] = f2h(__uint_as_float(o[h]) * __shfl_sync(0xffffffffu, inv, h));
-            softmax_barrier();   // red_sum is rewritten by the next query
+            for (int h4 = 0; h4 < 8; ++h4) {
+                const float4 iv = *reinterpret_cast<const float4 *>(red_inv + half * 32 + h4 * 4);
+                dst[(h4 * 4 + 0) * kD] = f2h(__uint_as_float(o[h4 * 4 + 0]) * iv.x);
+                dst[(h4 * 4 + 1) * kD] = f2h(__uint_as_float(o[h4 * 4 + 1]) * iv.y);
+                dst[(h4 * 4 + 2) * kD] = f2h(__uint_as_float(o[h4 * 4 + 2]) * iv.z);
+                dst[(h4 * 4 + 3) * kD] = f2h(__uint_as_float(o[h4 * 4 + 3]) * iv.w);
+            }
+        }
+    } else {
+        setmaxnreg_dec<kOtherRegs>();
+        // one lane waits for the warp, so that warp-wide steps stay converged
+        auto warp_wait = [&](uint64_t *b, uint32_t parity) {
+            bool r = true;
+            if (lane == 0) r = wait(b, parity);
+            r = __shfl_sync(0xffffffffu, r, 0);
+            ok = ok && r;
+            return r;
+        };
+        if (warp == kTblWarp) {
+            // ---------------- row tables (double-buffered, one query each) ----------------
+            constexpr int kBatch = 8;
+            int t = 0;
+            for (int i = q_begin; i < q_end; ++i, ++t) {
+                const int b = t & 1;
+                if (t >= 2 && !warp_wait(&bar.tbl_empty[b], static_cast<uint32_t>((t >> 1) - 1) & 1u)) continue;
+                const QueryKeys k = query_keys(a, i);
+                int *tb = tbl + b * (kMaxTiles * kTK);
+                uint32_t *mk = mask + b * kMaskWords;
+                const int n_words = k.n_tiles * 4;
+                for (int w0 = 0; w0 < n_words; w0 += kBatch) {
+                    int rows[kBatch];
+#pragma unroll
+                    for (int j = 0; j < kBatch; ++j)
+                        rows[j] = w0 + j < n_words ? slot_row(a, i, k, lane + 32 * (w0 + j), true) : -1;
+#pragma unroll
+                    for (int j = 0; j < kBatch; ++j) {
+                        if (w0 + j < n_words) {   // warp-uniform
+                            const int kx = lane + 32 * (w0 + j);
+                            tb[kx] = rows[j] >= 0 ? rows[j] : (kx < k.n_wt * kTK ? a.n_raw : a.comp_oob);
+                            const uint32_t m = __ballot_sync(0xffffffffu, rows[j] >= 0);
+                            if (lane == 0) mk[w0 + j] = m;
+                        }
+                    }
+                }
+                mbar_arrive(&bar.tbl_full[b]);
+            }
+        } else if (warp == kMmaWarp) {
+            // ---------------- MMA issuer ----------------
+            if (lane == 0) {
+                constexpr uint32_t kIdS = tc::idesc_f16_f32(kTK, kH, false, false);
+                constexpr uint32_t kIdO = tc::idesc_f16_f32(kTK, kH, true, true);
+                uint32_t g = 0, gs = 0, gp = 0;
+                int t = 0;
+                for (int i = q_begin; i < q_end && ok; ++i, ++t) {
+                    const QueryKeys k = query_keys(a, i);
+                    const int n = k.n_tiles;
+                    const uint32_t obuf = static_cast<uint32_t>(t & 1);
+                    auto issue_pv = [&](int c) {
+                        const uint32_t ev = g++;
+                        const int s = static_cast<int>(ev % kNS);
+                        const uint32_t pb = static_cast<uint32_t>(gp & 1);
+                        wait(&bar.full[s], static_cast<uint32_t>(ev / kNS) & 1u);
+                        wait(&bar.p_full[pb], static_cast<uint32_t>(gp >> 1) & 1u);
+                        if (c == 0 && t >= 2) wait(&bar.o_empty[obuf], static_cast<uint32_t>((t >> 1) - 1) & 1u);
+                        if (!ok) return;
+                        tc::fence_after_sync();
+                        const uint32_t va = tc::smem_u32(ring + s * kTileBytes);
+                        const uint32_t pa = tc::smem_u32(p_s + pb * kPBytes);
+#pragma unroll
+                        for (int st = 0; st < kTK / 16; ++st) {
+                            const uint64_t da = tc::desc_sw128(va + st * 2048, kTK * 128, 1024);
+                            const uint64_t db = tc::desc_sw128(pa + st * 16 * 128, 8192, 1024);
+                            tc::mma_f16(tmem + kColO + obuf * kH, da, db, kIdO, (c > 0 || st > 0) ? 1u : 0u);
+                        }
+                        tc::commit(&bar.p_empty[pb]);
+                        tc::commit(&bar.empty[s]);
+                        if (c == n - 1) tc::commit(&bar.o_full[obuf]);
+                        ++gp;
+                    };
+                    for (int c = 0; c < n && ok; ++c) {
+                        const uint32_t ev = g++;
+                        const int s = static_cast<int>(ev % kNS);
+                        wait(&bar.full[s], static_cast<uint32_t>(ev / kNS) & 1u);
+                        const uint32_t sb = static_cast<uint32_t>(gs & 1);
+                        if (gs >= 2) wait(&bar.s_empty[sb], static_cast<uint32_t>((gs >> 1) - 1) & 1u);
+                        if (!ok) break;
+                        tc::fence_after_sync();
+                        const uint32_t ka = tc::smem_u32(ring + s * kTileBytes), qb = tc::smem_u32(q_s);
+#pragma unroll
+                        for (int st = 0; st < kD / 16; ++st) {
+                            const uint64_t da = tc::desc_sw128(ka + (st / 4) * (kTK * 128) + (st % 4) * 32, 16, 1024);
+                            const uint64_t db = tc::desc_sw128(qb + (st / 4) * (kH * 128) + (st % 4) * 32, 16, 1024);
+                            tc::mma_f16(tmem + kColS + sb * kH, da, db, kIdS, st > 0 ? 1u : 0u);
+                        }
+                        tc::commit(&bar.s_full[sb]);
+                        tc::commit(&bar.empty[s]);
+                        if (c == n - 1) tc::commit(&bar.q_empty);
+                        ++gs;
+                        if (c >= 1) issue_pv(c - 1);
+                    }
+                    if (ok) issue_pv(n - 1);
+                }
+            }
+            __syncwarp();
+        } else {
+            // ---------------- TMA producers (warps 10-23) ----------------
+            const int j = warp - kIssWarp0;
+            if (lane == 0) {
+                const int u0 = j * kGathers / kIss, u1 = (j + 1) * kGathers / kIss;   // this warp's gathers
+                const bool q_warp = j == 2 || j == 3;                                 // the two Q halves
+                if (j == 0) {
+                    prefetch_map(&a.map_q);
+                    prefetch_map(&a.map_win_k);
+                    prefetch_map(&a.map_win_v);
+                    prefetch_map(&a.map_comp_k);
+                    prefetch_map(&a.map_comp_v);
+                }
+                uint32_t g = 0;
+                int t = 0;
+                for (int i = q_begin; i < q_end && ok; ++i, ++t) {
+                    const int b = t & 1;
+                    const QueryKeys k = query_keys(a, i);
+                    if (!wait(&bar.tbl_full[b], static_cast<uint32_t>(t >> 1) & 1u)) break;
+                    const int *tb = tbl + b * (kMaxTiles * kTK);
+                    for (int e = 0; e < 2 * k.n_tiles; ++e, ++g) {
+                        const int s = static_cast<int>(g % kNS);
+                        if (g >= kNS) wait(&bar.empty[s], static_cast<uint32_t>((g / kNS) - 1) & 1u);
+                        const bool q_load = e == 0 && q_warp;
+                        // the MMAs of the previous query are done with the Q block
+                        if (q_load && t > 0) wait(&bar.q_empty, static_cast<uint32_t>(t - 1) & 1u);
+                        if (!ok) break;
+                        bool is_v;
+                        int c;
+                        ring_event(e, k.n_tiles, is_v, c);
+                        // a window tile of 128 existing rows is contiguous: two tile loads
+                        const bool win_tile = c < k.n_wt && (c + 1) * kTK <= k.n_w;
+                        uint32_t bytes = q_load ? kQBytes / 2 : 0;
+                        if (win_tile) bytes += j < 2 ? kTileBytes / 2 : 0;
+                        else bytes += static_cast<uint32_t>(u1 - u0) * 512;
+                        expect_tx(&bar.full[s], bytes);
+                        unsigned char *dst = ring + s * kTileBytes;
+                        if (q_load) tma_load_2d(q_s + (j - 2) * (kH * 128), &a.map_q, (j - 2) * 64, i * kH, &bar.full[s]);
+                        if (win_tile) {
+                            if (j < 2)
+                                tma_load_2d(dst + j * (kTK * 128), is_v ? &a.map_win_v : &a.map_win_k, j * 64,
+                                            k.raw0 + c * kTK, &bar.full[s]);
+                        } else {
+                            const CUtensorMap *map = c < k.n_wt ? (is_v ? &a.map_raw_v : &a.map_raw_k)
+                                                                : (is_v ? &a.map_comp_v : &a.map_comp_k);
+                            const uint32_t d0 = tc::smem_u32(dst);
+                            for (int u = u0; u < u1; ++u) {
+                                const int grp = u >> 1, hf = u & 1;
+                                const int4 r4 = *reinterpret_cast<const int4 *>(tb + c * kTK + grp * 4);
+                                tma_gather4(d0 + hf * (kTK * 128) + grp * 512, map, hf * 64, r4, &bar.full[s]);
+                            }
+                        }
+                    }
+                    // this warp's gathers of the query have taken their rows
+                    mbar_arrive(&bar.tbl_empty[b]);
+                }
+            }
+            __syncwarp();
         }
     }
     if (!ok) record_error(a.err, DS4A_ERR_TIMEOUT);
@@ -495,10 +659,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(Args a) {
     if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// the driver's tensor-map encoder, looked up once through the runtime
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// rows x 128 fp16 values, row-major; boxes of 64 columns x box_rows rows, 128-byte swizzle
+bool encode_rows(CUtensorMap *m, const uint16_t *ptr, long long rows, uint32_t box_rows) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+    const cuuint32_t box[2] = {64, box_rows}, es[2] = {1, 1};
+    return encode_tiled()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(ptr), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
-bool attn_prefill_tc_ok(int H, int D, long long max_keys) {
-    return H == kH && D == kD && max_keys <= kMaxTiles * kTK;
+bool attn_prefill_tc_ok(const uint16_t *q, int T, int H, int D, int n_prior, int window, long long max_sel,
+                        long long n_comp) {
+    const long long tiles = (window + kTK - 1) / kTK + (max_sel + kTK - 1) / kTK;
+    // TMA needs 16-byte aligned bases; row coordinates are 32-bit
+    return H == kH && D == kD && tiles <= kMaxTiles && (reinterpret_cast<uintptr_t>(q) & 15) == 0 &&
+           static_cast<long long>(n_prior) + T < (1LL << 31) - 1 && n_comp < (1LL << 31) - 1 &&
+           static_cast<long long>(T) * kH < (1LL << 31) && encode_tiled() != nullptr;
 }
 
 cudaError_t launch_attn_prefill_tc(const uint16_t *q, int T, const uint16_t *raw_k, const uint16_t *raw_v,
@@ -514,8 +711,30 @@ cudaError_t launch_attn_prefill_tc(const uint16_t *q, int T, const uint16_t *raw
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    Args a{q, raw_k, raw_v, comp_k, comp_v, sel, out, c.err, n_comp, q_pos0, T, n_prior, window, k_stride,
-           ratio, scale * kLog2e};
+    Args a{};
+    const long long n_raw = static_cast<long long>(n_prior) + T;
+    // with no compressed rows the compressed maps alias the raw ones and every slot reads the zero row
+    const bool has_comp = n_comp > 0 && comp_k && comp_v;
+    const long long comp_rows = has_comp ? n_comp : n_raw;
+    if (!encode_rows(&a.map_q, q, static_cast<long long>(T) * kH, kH) ||
+        !encode_rows(&a.map_raw_k, raw_k, n_raw, 1) || !encode_rows(&a.map_raw_v, raw_v, n_raw, 1) ||
+        !encode_rows(&a.map_win_k, raw_k, n_raw, kTK) || !encode_rows(&a.map_win_v, raw_v, n_raw, kTK) ||
+        !encode_rows(&a.map_comp_k, has_comp ? comp_k : raw_k, comp_rows, 1) ||
+        !encode_rows(&a.map_comp_v, has_comp ? comp_v : raw_v, comp_rows, 1))
+        return cudaErrorInvalidValue;
+    a.sel = sel;
+    a.out = out;
+    a.err = c.err;
+    a.n_comp = has_comp ? static_cast<int>(n_comp) : 0;
+    a.q_pos0 = q_pos0;
+    a.n_raw = static_cast<int>(n_raw);
+    a.comp_oob = static_cast<int>(comp_rows);
+    a.T = T;
+    a.n_prior = n_prior;
+    a.window = window;
+    a.k_stride = k_stride;
+    a.ratio = ratio;
+    a.scale_log2 = scale * kLog2e;
     const int grid = T < c.num_sms ? T : c.num_sms;
     return launch(attn_prefill_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, c, 1, a);
 }
