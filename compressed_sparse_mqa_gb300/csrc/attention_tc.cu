@@ -132,15 +132,6 @@ DS4A_DEVINL void ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
-DS4A_DEVINL void st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
-        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
-        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
-}
 DS4A_DEVINL void st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
@@ -150,14 +141,6 @@ DS4A_DEVINL void st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
 }
 DS4A_DEVINL void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
-DS4A_DEVINL uint32_t redux_max_u32(uint32_t v) {
-    uint32_t r;
-    asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;\n" : "=r"(r) : "r"(v));
-    return r;
-}
-DS4A_DEVINL float key_to_float(uint32_t key) {
-    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
 DS4A_DEVINL void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(bar)) : "memory");
 }
@@ -175,6 +158,29 @@ DS4A_DEVINL bool half_any(int half, bool pred) {
 }
 template <int N> DS4A_DEVINL void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N)); }
 template <int N> DS4A_DEVINL void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N)); }
+
+// 2^x with the hardware approximation (flush-to-zero): the softmax numerators
+// are rounded to fp16 right after, far coarser than its error
+DS4A_DEVINL float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// lane l receives the max over the warp's 32 lanes of v[l] (see transpose_sum32)
+DS4A_DEVINL float transpose_max32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? v[i] : v[i + s];
+            const float keep = upper ? v[i + s] : v[i];
+            v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, s));
+        }
+    }
+    return v[0];
+}
 
 // lane l receives the sum over the warp's 32 lanes of v[l] (a butterfly that
 // halves the live values at each step: 31 shuffles in all)
@@ -323,7 +329,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(const __gr
         // ---------------- softmax + epilogue (warps 0-7) ----------------
         const int quad = warp & 3, half = warp >> 2;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t kNegInfKey = float_key(-INFINITY);
         const float c2 = a.scale_log2;
         uint32_t gs = 0, gp = 0;
         int t = 0;
@@ -366,53 +371,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(const __gr
                 }
                 if (!valid) mx = -INFINITY;
                 if (half_any(half, mx > kRescale)) {
-                    // some head grew past its reference: the exact tile max of each head
-                    // across the 128 keys (warp, then the 4 quadrants), new references
+                    // Some head grew past its reference: the exact tile max of each head
+                    // over the 128 keys.  A transposing butterfly leaves lane l with the
+                    // max of head l over this warp's 32 keys; the 4 quadrants meet in
+                    // shared memory; lane l then updates the reference of head l.
+                    float v[32];
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) {
-                        const uint32_t m = redux_max_u32(valid ? float_key(__uint_as_float(r[h])) : kNegInfKey);
-                        if (lane == h) red_max[quad * kH + half * 32 + h] = key_to_float(m);
-                    }
+                    for (int h = 0; h < 32; ++h) v[h] = valid ? __uint_as_float(r[h]) : -INFINITY;
+                    red_max[quad * kH + half * 32 + lane] = transpose_max32(v, lane);
                     half_barrier(half);
-                    bool rescale = false;
-                    float my_new = 0.f;   // the new reference of head `lane`
+                    float tm = red_max[half * 32 + lane];
 #pragma unroll
-                    for (int h4 = 0; h4 < 8; ++h4) {
-                        float4 m4 = *reinterpret_cast<const float4 *>(red_max + half * 32 + h4 * 4);
+                    for (int qd = 1; qd < 4; ++qd) tm = fmaxf(tm, red_max[qd * kH + half * 32 + lane]);
+                    const float target = tm * c2;   // scale > 0: the max commutes with it
+                    const float old = mh[lane];
+                    float alpha = 1.f;
+                    if (old == -INFINITY) {
+                        mh[lane] = target;
+                        alpha = 0.f;   // nothing accumulated yet
+                    } else if (target > old + kRescale) {
+                        alpha = ex2(old - target);
+                        mh[lane] = target;
+                    }
+                    s_alpha[warp][lane] = alpha;
+                    const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+                    __syncwarp();
+                    if (rescale) {
 #pragma unroll
-                        for (int qd = 1; qd < 4; ++qd) {
-                            const float4 o4 = *reinterpret_cast<const float4 *>(red_max + qd * kH + half * 32 + h4 * 4);
-                            m4.x = fmaxf(m4.x, o4.x);
-                            m4.y = fmaxf(m4.y, o4.y);
-                            m4.z = fmaxf(m4.z, o4.z);
-                            m4.w = fmaxf(m4.w, o4.w);
-                        }
-                        const float tm[4] = {m4.x, m4.y, m4.z, m4.w};
-                        const float4 old4 = *reinterpret_cast<const float4 *>(mh + h4 * 4);
-                        const float old[4] = {old4.x, old4.y, old4.z, old4.w};
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int h = h4 * 4 + u;
-                            const float target = tm[u] * c2;   // scale > 0: the max commutes with it
-                            float alpha = 1.f, m_new = old[u];
-                            if (old[u] == -INFINITY) {
-                                m_new = target;
-                                alpha = 0.f;   // nothing accumulated yet
-                            } else if (target > old[u] + kRescale) {
-                                alpha = exp2f(old[u] - target);
-                                m_new = target;
-                            }
-                            rescale |= alpha != 1.f;
-                            l_lane[h] *= alpha;
-                            if (lane == h) {
-                                s_alpha[warp][h] = alpha;
-                                my_new = m_new;
-                            }
+                        for (int h4 = 0; h4 < 8; ++h4) {
+                            const float4 al = *reinterpret_cast<const float4 *>(&s_alpha[warp][h4 * 4]);
+                            l_lane[h4 * 4 + 0] *= al.x;
+                            l_lane[h4 * 4 + 1] *= al.y;
+                            l_lane[h4 * 4 + 2] *= al.z;
+                            l_lane[h4 * 4 + 3] *= al.w;
                         }
                     }
-                    __syncwarp();   // every lane has read the old references
-                    mh[lane] = my_new;
-                    __syncwarp();
                     if (c > 0 && rescale) {
                         // O^T holds the earlier tiles once the previous PV is done
                         wait(&bar.p_empty[(gp - 1) & 1], static_cast<uint32_t>((gp - 1) >> 1) & 1u);
@@ -445,8 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(const __gr
 #pragma unroll
                     for (int u = 0; u < 4; u += 2) {
                         const int h = h4 * 4 + u;
-                        const float p0 = valid ? exp2f(fmaf(__uint_as_float(r[h]), c2, -m[u])) : 0.f;
-                        const float p1 = valid ? exp2f(fmaf(__uint_as_float(r[h + 1]), c2, -m[u + 1])) : 0.f;
+                        const float p0 = valid ? ex2(fmaf(__uint_as_float(r[h]), c2, -m[u])) : 0.f;
+                        const float p1 = valid ? ex2(fmaf(__uint_as_float(r[h + 1]), c2, -m[u + 1])) : 0.f;
                         l_lane[h] += p0;
                         l_lane[h + 1] += p1;
                         pk[h / 2] = pack_half2(p0, p1);
