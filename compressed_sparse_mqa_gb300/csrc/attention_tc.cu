@@ -247,20 +247,6 @@ DS4A_DEVINL QueryKeys query_keys(const Args &a, int i) {
     k.n_tiles = k.n_wt + (k.n_sel + kTK - 1) / kTK;
     return k;
 }
-// row of key slot kx in its tensor (raw rows in the window tiles, compressed
-// rows after them); -1 for padding, a negative sel entry or an out-of-range one
-// (which is also recorded)
-DS4A_DEVINL int slot_row(const Args &a, int i, const QueryKeys &k, int kx, bool record) {
-    const int w = kx - k.n_wt * kTK;
-    if (w < 0) return kx < k.n_w ? k.raw0 + kx : -1;
-    if (w >= k.n_sel) return -1;
-    const int j = a.sel ? __ldg(a.sel + static_cast<size_t>(i) * a.k_stride + w) : w;
-    if (j >= a.n_comp) {
-        if (record) record_error(a.err, DS4A_ERR_DEVICE_INDEX);
-        return -1;
-    }
-    return j >= 0 ? j : -1;
-}
 // ring event e (0 .. 2n-1) of a query with n tiles: K0, K1, V0, K2, V1, ..., V(n-1)
 DS4A_DEVINL void ring_event(int e, int n, bool &is_v, int &tile) {
     if (e == 0) { is_v = false; tile = 0; }
@@ -502,7 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(const __gr
         };
         if (warp == kTblWarp) {
             // ---------------- row tables (double-buffered, one query each) ----------------
-            constexpr int kBatch = 8;
+            // The sel entries of a query come in as int4 (four slots a lane), every
+            // load in flight before any is used; the validity bits are then read
+            // back from the finished table.
+            constexpr int kVec = kMaxTiles * kTK / 4 / 32;
             int t = 0;
             for (int i = q_begin; i < q_end; ++i, ++t) {
                 const int b = t & 1;
@@ -510,21 +499,49 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(const __gr
                 const QueryKeys k = query_keys(a, i);
                 int *tb = tbl + b * (kMaxTiles * kTK);
                 uint32_t *mk = mask + b * kMaskWords;
-                const int n_words = k.n_tiles * 4;
-                for (int w0 = 0; w0 < n_words; w0 += kBatch) {
-                    int rows[kBatch];
+                const int w_slots = k.n_wt * kTK;   // window slots
+                const int n_slots = k.n_tiles * kTK;
+                const int32_t *sp = a.sel ? a.sel + static_cast<size_t>(i) * a.k_stride : nullptr;
+                const bool vec = sp && (reinterpret_cast<uintptr_t>(sp) & 15) == 0 && (k.n_sel & 3) == 0;
+                int4 v[kVec];
 #pragma unroll
-                    for (int j = 0; j < kBatch; ++j)
-                        rows[j] = w0 + j < n_words ? slot_row(a, i, k, lane + 32 * (w0 + j), true) : -1;
-#pragma unroll
-                    for (int j = 0; j < kBatch; ++j) {
-                        if (w0 + j < n_words) {   // warp-uniform
-                            const int kx = lane + 32 * (w0 + j);
-                            tb[kx] = rows[j] >= 0 ? rows[j] : (kx < k.n_wt * kTK ? a.n_raw : a.comp_oob);
-                            const uint32_t m = __ballot_sync(0xffffffffu, rows[j] >= 0);
-                            if (lane == 0) mk[w0 + j] = m;
+                for (int m = 0; m < kVec; ++m) {
+                    const int w = (lane + 32 * m) * 4;   // first of this lane's four compressed slots
+                    if (sp && w < k.n_sel) {
+                        if (vec) {
+                            v[m] = __ldg(reinterpret_cast<const int4 *>(sp + w));
+                        } else {
+                            v[m].x = __ldg(sp + w);
+                            v[m].y = w + 1 < k.n_sel ? __ldg(sp + w + 1) : -1;
+                            v[m].z = w + 2 < k.n_sel ? __ldg(sp + w + 2) : -1;
+                            v[m].w = w + 3 < k.n_sel ? __ldg(sp + w + 3) : -1;
                         }
+                    } else {
+                        v[m] = make_int4(w, w + 1, w + 2, w + 3);   // no sel: the visible rows in order
                     }
+                }
+                // window slots: consecutive raw rows, the zero row past the window
+                for (int kx = lane; kx < w_slots; kx += 32) tb[kx] = kx < k.n_w ? k.raw0 + kx : a.n_raw;
+#pragma unroll
+                for (int m = 0; m < kVec; ++m) {
+                    const int w = (lane + 32 * m) * 4;
+                    if (w_slots + w < n_slots) {
+                        const int e[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+                        int r[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const bool in_list = w + u < k.n_sel;
+                            if (in_list && e[u] >= a.n_comp) record_error(a.err, DS4A_ERR_DEVICE_INDEX);
+                            r[u] = in_list && e[u] >= 0 && e[u] < a.n_comp ? e[u] : a.comp_oob;
+                        }
+                        *reinterpret_cast<int4 *>(tb + w_slots + w) = make_int4(r[0], r[1], r[2], r[3]);
+                    }
+                }
+                __syncwarp();
+                for (int wd = 0; wd < k.n_tiles * 4; ++wd) {   // warp-uniform
+                    const int kx = wd * 32 + lane;
+                    const uint32_t m = __ballot_sync(0xffffffffu, tb[kx] != (kx < w_slots ? a.n_raw : a.comp_oob));
+                    if (lane == 0) mk[wd] = m;
                 }
                 mbar_arrive(&bar.tbl_full[b]);
             }
