@@ -8,8 +8,8 @@
 // 1. indexer_scores_tc_kernel: tcgen05.mma (M = 128 queries, N = 256 rows,
 //    K = d_idx, fp16 in, fp32 accumulate in tensor memory, two accumulator
 //    buffers so the epilogue of one tile overlaps the MMAs of the next) writes
-//    approximate scores s~ to the workspace, and the squared norm of every key
-//    row.
+//    approximate scores s~ to the workspace, and the largest squared key norm
+//    of every 256-row tile.
 // 2. indexer_select_kernel: per query, the approximate scores s~ differ from the
 //    exact scores s by at most eps = 2^-12 |q| max_j |k_j| (a bound far above the
 //    tensor cores' fp32 accumulation error over d_idx <= 128 exact products).  Two
@@ -37,7 +37,7 @@ struct TcScoreArgs {
     const uint16_t *q_idx;
     const uint16_t *k_idx;
     float *scores;     // [n_q][ld]
-    float *knorm2;     // [ld]
+    float *tile_kmax2; // [n_ntiles] largest squared key norm of each 256-row tile
     unsigned int *err;
     long long n_rows;
     int n_q;
@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
     unsigned char *sb[2] = {smem + kABytes, smem + kABytes + kBBytes};
     __shared__ uint32_t s_tmem;
     __shared__ __align__(8) uint64_t s_bar[2];
+    __shared__ uint32_t s_kmax2;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int m0 = blockIdx.x * kTM;
@@ -142,9 +143,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
             }
             tc::commit(&s_bar[buf]);
         }
-        // squared norms of the key rows (one M tile computes them)
+        // largest squared norm of the tile's key rows (one M tile computes them)
         if (blockIdx.x == 0) {
             const long long row0 = static_cast<long long>(ns + it * a.n_split) * kTN;
+            if (tid == 0) s_kmax2 = 0u;
+            __syncthreads();
+            float m2 = 0.f;
             for (int r = tid; r < kTN; r += kGemmThreads) {
                 float acc = 0.f;
 #pragma unroll
@@ -157,8 +161,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
                         acc = fmaf(x, x, acc);
                     }
                 }
-                if (row0 + r < a.n_rows) a.knorm2[row0 + r] = acc;
+                if (row0 + r < a.n_rows) m2 = fmaxf(m2, acc);
             }
+            // non-negative floats order like their bit patterns
+            atomicMax(&s_kmax2, __float_as_uint(warp_max(m2)));
+            __syncthreads();
+            if (tid == 0) a.tile_kmax2[ns + it * a.n_split] = __uint_as_float(s_kmax2);
         }
         if (it >= 1) {
             epilogue(it - 1);
@@ -179,9 +187,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
 
 // ---- per-query select on approximate scores with an exact band ------------------------------
 
-constexpr int kSelThreads = 256;
-constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelMaxItems = 32;          // n_vis <= 8192
+constexpr int kSelMaxRows = 8192;
 constexpr int kBandCap = 1024;
 constexpr int kBins = 2048;               // 11-bit digits
 
@@ -189,7 +195,7 @@ struct SelArgs {
     const uint16_t *q_idx;
     const uint16_t *k_idx;
     float *scores;          // [n_q][ld] approximate scores (overwritten by exact keys on fallback)
-    const float *knorm2;
+    const float *tile_kmax2;   // largest squared key norm of each 256-row tile
     int32_t *out_idx;
     int32_t *out_n;
     long long n_rows;
@@ -200,32 +206,20 @@ struct SelArgs {
     int ld;
 };
 
+template <int NT>
 struct SelSmem {
     uint32_t hist[kBins];
-    uint32_t cnt[kSelMaxItems * kSelWarps];
-    uint32_t scan[kSelWarps];
+    uint32_t cnt[NT];
+    uint32_t scan[NT / 32];
     int band_idx[kBandCap];
     uint32_t band_key[kBandCap];
-    uint32_t sel_bits[kSelMaxItems * kSelThreads / 32];
-    float red[kSelWarps];
+    uint32_t sel_bits[kSelMaxRows / 32];
     uint32_t res[3], band_n, n_in;
     float eps;
 };
 
 DS4A_DEVINL float key_to_float(uint32_t key) {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
-
-DS4A_DEVINL float sel_block_max(float v, float *red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = warp_max(v);
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float m = red[0];
-#pragma unroll
-    for (int w = 1; w < kSelWarps; ++w) m = fmaxf(m, red[w]);
-    return m;
 }
 
 // TwoSum-exact score of one row, computed by a group of 16 threads (all 32 lanes of
@@ -258,9 +252,10 @@ DS4A_DEVINL uint32_t exact_key16(const uint16_t *q, const uint16_t *krow, int d_
     return float_key(s + c);
 }
 
-template <int ITEMS>
-__global__ void __launch_bounds__(kSelThreads, 2) indexer_select_kernel(SelArgs a) {
-    __shared__ SelSmem sm;
+template <int NT, int ITEMS, int MIN_BLOCKS>
+__global__ void __launch_bounds__(NT, MIN_BLOCKS) indexer_select_kernel(SelArgs a) {
+    constexpr int kSelThreads = NT;
+    __shared__ SelSmem<NT> sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();
     pdl_trigger();
@@ -276,25 +271,25 @@ __global__ void __launch_bounds__(kSelThreads, 2) indexer_select_kernel(SelArgs 
     const uint16_t *q = a.q_idx + static_cast<size_t>(i) * a.d_idx;
     float *row = a.scores + static_cast<size_t>(i) * a.ld;
 
-    // error bound of the approximate scores
-    float kmax2 = 0.f;
-    for (int j = tid; j < n; j += kSelThreads) kmax2 = fmaxf(kmax2, a.knorm2[j]);
-    kmax2 = sel_block_max(kmax2, sm.red);
+    uint32_t key[ITEMS];
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int j = it * kSelThreads + tid;
+        key[it] = j < n ? float_key(row[j]) : 0u;
+    }
+    // error bound of the approximate scores: |q| times the largest key norm of
+    // the tiles holding the visible rows
     if (warp == 0) {
         float qn2 = 0.f;
         for (int c = lane; c < a.d_idx; c += 32) {
             const float x = h2f(q[c]);
             qn2 = fmaf(x, x, qn2);
         }
+        float kmax2 = 0.f;
+        for (int t = lane; t * kTN < n; t += 32) kmax2 = fmaxf(kmax2, a.tile_kmax2[t]);
         qn2 = warp_sum(qn2);
+        kmax2 = warp_max(kmax2);
         if (lane == 0) sm.eps = ldexpf(sqrtf(qn2 * kmax2) * 1.01f, -12) + 1e-30f;
-    }
-
-    uint32_t key[ITEMS];
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const int j = it * kSelThreads + tid;
-        key[it] = j < n ? float_key(row[j]) : 0u;
     }
     __syncthreads();
     const float eps = sm.eps;
@@ -390,18 +385,20 @@ __global__ void __launch_bounds__(kSelThreads, 2) indexer_select_kernel(SelArgs 
     sel::emit<kSelThreads, ITEMS>(flags, out, sm.cnt, sm.scan);
 }
 
+constexpr int kSelNT = 256, kSelMinBlocks = 4;   // threads per query, CTAs per SM (<= 64 registers)
+
 template <int DI>
 constexpr size_t gemm_smem() { return (DI / 64) * (kTM + 2 * kTN) * 128 + 1024; }
 
 }  // namespace
 
 bool indexer_prefill_tc_ok(int n_q, long long n_rows, int d_idx) {
-    return n_q >= 64 && (d_idx == 64 || d_idx == 128) && n_rows <= kSelThreads * kSelMaxItems;
+    return n_q >= 64 && (d_idx == 64 || d_idx == 128) && n_rows <= kSelMaxRows;
 }
 
 size_t indexer_prefill_tc_ws_bytes(int n_q, long long n_rows) {
     const long long ld = (n_rows + kTN - 1) / kTN * kTN;
-    return 256 + static_cast<size_t>(ld) * sizeof(float) + static_cast<size_t>(n_q) * ld * sizeof(float);
+    return 256 + static_cast<size_t>(n_q) * ld * sizeof(float);
 }
 
 cudaError_t launch_indexer_prefill_tc(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
@@ -421,14 +418,14 @@ cudaError_t launch_indexer_prefill_tc(const uint16_t *q_idx, int n_q, const uint
         configured_device = dev;
     }
     const int ld = static_cast<int>((n_rows + kTN - 1) / kTN * kTN);
-    unsigned char *base = static_cast<unsigned char *>(ws) + 256;
-    float *knorm2 = reinterpret_cast<float *>(base);
-    float *scores = reinterpret_cast<float *>(base + static_cast<size_t>(ld) * sizeof(float));
+    // workspace: 256-byte header holding the tile norms (<= 32 tiles), then the scores
+    float *tile_kmax2 = static_cast<float *>(ws);
+    float *scores = reinterpret_cast<float *>(static_cast<unsigned char *>(ws) + 256);
     TcScoreArgs g;
     g.q_idx = q_idx;
     g.k_idx = k_idx;
     g.scores = scores;
-    g.knorm2 = knorm2;
+    g.tile_kmax2 = tile_kmax2;
     g.err = c.err;
     g.n_rows = n_rows;
     g.n_q = n_q;
@@ -443,11 +440,11 @@ cudaError_t launch_indexer_prefill_tc(const uint16_t *q_idx, int n_q, const uint
                         ? launch(indexer_scores_tc_kernel<128>, grid, dim3(kGemmThreads), gemm_smem<128>(), c, 1, g)
                         : launch(indexer_scores_tc_kernel<64>, grid, dim3(kGemmThreads), gemm_smem<64>(), c, 1, g);
     if (e != cudaSuccess) return e;
-    SelArgs s{q_idx, k_idx, scores, knorm2, out_idx, out_n, n_rows, q_pos0, d_idx, ratio, k, ld};
+    SelArgs s{q_idx, k_idx, scores, tile_kmax2, out_idx, out_n, n_rows, q_pos0, d_idx, ratio, k, ld};
     const long long n_max = n_rows;
-    if (n_max <= 8 * kSelThreads) return launch(indexer_select_kernel<8>, dim3(n_q), dim3(kSelThreads), 0, c, 1, s);
-    if (n_max <= 16 * kSelThreads) return launch(indexer_select_kernel<16>, dim3(n_q), dim3(kSelThreads), 0, c, 1, s);
-    return launch(indexer_select_kernel<32>, dim3(n_q), dim3(kSelThreads), 0, c, 1, s);
+    if (n_max <= 8 * kSelNT) return launch(indexer_select_kernel<kSelNT, 8, kSelMinBlocks>, dim3(n_q), dim3(kSelNT), 0, c, 1, s);
+    if (n_max <= 16 * kSelNT) return launch(indexer_select_kernel<kSelNT, 16, kSelMinBlocks>, dim3(n_q), dim3(kSelNT), 0, c, 1, s);
+    return launch(indexer_select_kernel<kSelNT, kSelMaxRows / kSelNT, kSelMinBlocks>, dim3(n_q), dim3(kSelNT), 0, c, 1, s);
 }
 
 }  // namespace ds4a
