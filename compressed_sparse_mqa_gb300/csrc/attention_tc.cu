@@ -30,12 +30,13 @@
 //   warp 8       row tables: the 32 lanes resolve the row of every key slot of
 //                the next query (window rows, then sel entries) into one of two
 //                shared tables, with a validity bit per slot.
-//   warp 9       MMA issuer (one thread): S^T_c into one of two TMEM buffers, then
-//                O^T += V^T_(c-1) P^T_(c-1); tcgen05.commit releases ring stages
-//                and signals the softmax warps.
+//   warp 9       MMA issuer (one thread): S^T_0, S^T_1, then S^T_(c+2) (into the
+//                TMEM buffer the softmax has just read S^T_c from) and
+//                O^T += V^T_c P^T_c for each tile c; tcgen05.commit releases ring
+//                stages and signals the softmax warps.
 //   warps 10-23  TMA producers: fill a 5-stage ring of 128-byte-swizzled 32 KB
-//                tiles in the order the MMAs consume them: K0, K1, V0, K2, V1,
-//                ..., V(n-1).  A tile of scattered rows is 64 tile::gather4 loads
+//                tiles in the order the MMAs consume them: K0, K1, K2, V0, K3,
+//                V1, ..., V(n-2), V(n-1).  A tile of scattered rows is 64 tile::gather4 loads
 //                (4 rows x 128 B each) shared out over the 14 warps -- a TMA
 //                instruction holds its issuing warp for a while, so the gather
 //                rate grows with the number of issuing warps; a full window tile
@@ -247,12 +248,14 @@ DS4A_DEVINL QueryKeys query_keys(const Args &a, int i) {
     k.n_tiles = k.n_wt + (k.n_sel + kTK - 1) / kTK;
     return k;
 }
-// ring event e (0 .. 2n-1) of a query with n tiles: K0, K1, V0, K2, V1, ..., V(n-1)
+// ring event e (0 .. 2n-1) of a query with n tiles, in the order the MMAs take
+// them: K0, K1, then K(c+2), V(c) for c = 0 .. n-3, then V(n-2), V(n-1)
 DS4A_DEVINL void ring_event(int e, int n, bool &is_v, int &tile) {
-    if (e == 0) { is_v = false; tile = 0; }
-    else if (e == 2 * n - 1) { is_v = true; tile = n - 1; }
-    else if (e & 1) { is_v = false; tile = (e + 1) / 2; }
-    else { is_v = true; tile = e / 2 - 1; }
+    if (e == 2 * n - 1) { is_v = true; tile = n - 1; }
+    else if (e == 2 * n - 2 && n >= 2) { is_v = true; tile = n - 2; }
+    else if (e < 2) { is_v = false; tile = e; }
+    else if (e & 1) { is_v = true; tile = (e - 2) / 2; }
+    else { is_v = false; tile = (e - 2) / 2 + 2; }
 }
 
 
@@ -578,13 +581,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(const __gr
                         if (c == n - 1) tc::commit(&bar.o_full[obuf]);
                         ++gp;
                     };
-                    for (int c = 0; c < n && ok; ++c) {
+                    // S^T_c = K_c Q^T into S buffer c % 2 (free once the softmax has read S_(c-2))
+                    auto issue_s = [&](int c) {
                         const uint32_t ev = g++;
                         const int s = static_cast<int>(ev % kNS);
                         wait(&bar.full[s], static_cast<uint32_t>(ev / kNS) & 1u);
                         const uint32_t sb = static_cast<uint32_t>(gs & 1);
                         if (gs >= 2) wait(&bar.s_empty[sb], static_cast<uint32_t>((gs >> 1) - 1) & 1u);
-                        if (!ok) break;
+                        if (!ok) return;
                         tc::fence_after_sync();
                         const uint32_t ka = tc::smem_u32(ring + s * kTileBytes), qb = tc::smem_u32(q_s);
 #pragma unroll
@@ -597,9 +601,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(const __gr
                         tc::commit(&bar.empty[s]);
                         if (c == n - 1) tc::commit(&bar.q_empty);
                         ++gs;
-                        if (c >= 1) issue_pv(c - 1);
+                    };
+                    // the scores run two tiles ahead of the PV products: S_(c+2) is on the
+                    // tensor pipe while the softmax of tile c is still being computed
+                    issue_s(0);
+                    if (n > 1) issue_s(1);
+                    for (int c = 0; c < n && ok; ++c) {
+                        if (c + 2 < n) issue_s(c + 2);
+                        if (ok) issue_pv(c);
                     }
-                    if (ok) issue_pv(n - 1);
                 }
             }
             __syncwarp();
