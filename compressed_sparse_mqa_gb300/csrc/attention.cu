@@ -593,7 +593,7 @@ cudaError_t launch_attn_prefill(const uint16_t *q, int T, int H, int D, const ui
             max_sel = nv < n_comp ? nv : n_comp;
         }
     }
-    if (attn_prefill_tc_ok(q, T, H, D, n_prior, window, max_sel, n_comp))
+    if (attn_prefill_tc_ok(q, out, T, H, D, n_prior, window, max_sel, n_comp))
         return launch_attn_prefill_tc(q, T, raw_k, raw_v, n_prior, window, comp_k, comp_v, n_comp, sel, k_stride,
                                       q_pos0, ratio, scale, out, c);
     PrefillArgs a{q, raw_k, raw_v, comp_k, comp_v, sel, out, c.err, n_comp, q_pos0,

@@ -469,15 +469,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_tc_kernel(const __gr
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar.o_empty[obuf]);
-            uint16_t *dst = a.out + (static_cast<size_t>(i) * kH + half * 32) * kD + quad * 32 + lane;
+            // Stage the warp's 32 heads x 32 d through the part of the P buffer that
+            // only this warp writes (rows 32*quad .., bytes 64*half ..; every PV of the
+            // query has finished with it), then write 16 bytes per lane.
+            unsigned char *stg = p_s + (gp & 1) * kPBytes;
+            auto stg_chunk = [&](int h, int c16) {   // 16-byte chunk c16 (0..3) of head h's 64 bytes
+                const int key = quad * 32 + h;
+                return stg + key * 128 + (((half * 4 + c16) ^ (key & 7)) << 4);
+            };
 #pragma unroll
             for (int h4 = 0; h4 < 8; ++h4) {
                 const float4 iv = *reinterpret_cast<const float4 *>(red_inv + half * 32 + h4 * 4);
-                dst[(h4 * 4 + 0) * kD] = f2h(__uint_as_float(o[h4 * 4 + 0]) * iv.x);
-                dst[(h4 * 4 + 1) * kD] = f2h(__uint_as_float(o[h4 * 4 + 1]) * iv.y);
-                dst[(h4 * 4 + 2) * kD] = f2h(__uint_as_float(o[h4 * 4 + 2]) * iv.z);
-                dst[(h4 * 4 + 3) * kD] = f2h(__uint_as_float(o[h4 * 4 + 3]) * iv.w);
+                const float inv[4] = {iv.x, iv.y, iv.z, iv.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint16_t *>(stg_chunk(h4 * 4 + u, lane >> 3) + (lane & 7) * 2) =
+                        f2h(__uint_as_float(o[h4 * 4 + u]) * inv[u]);
             }
+            __syncwarp();
+            uint16_t *dst = a.out + (static_cast<size_t>(i) * kH + half * 32) * kD + quad * 32;
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int h = k4 * 8 + (lane >> 2), c16 = lane & 3;
+                *reinterpret_cast<uint4 *>(dst + h * kD + c16 * 8) = *reinterpret_cast<const uint4 *>(stg_chunk(h, c16));
+            }
+            __syncwarp();
         }
     } else {
         setmaxnreg_dec<kOtherRegs>();
@@ -709,11 +725,13 @@ bool encode_rows(CUtensorMap *m, const uint16_t *ptr, long long rows, uint32_t b
 
 }  // namespace
 
-bool attn_prefill_tc_ok(const uint16_t *q, int T, int H, int D, int n_prior, int window, long long max_sel,
-                        long long n_comp) {
+bool attn_prefill_tc_ok(const uint16_t *q, const uint16_t *out, int T, int H, int D, int n_prior, int window,
+                        long long max_sel, long long n_comp) {
     const long long tiles = (window + kTK - 1) / kTK + (max_sel + kTK - 1) / kTK;
-    // TMA needs 16-byte aligned bases; row coordinates are 32-bit
+    // TMA needs 16-byte aligned bases, the output is written 16 bytes at a time;
+    // row coordinates are 32-bit
     return H == kH && D == kD && tiles <= kMaxTiles && (reinterpret_cast<uintptr_t>(q) & 15) == 0 &&
+           (reinterpret_cast<uintptr_t>(out) & 15) == 0 &&
            static_cast<long long>(n_prior) + T < (1LL << 31) - 1 && n_comp < (1LL << 31) - 1 &&
            static_cast<long long>(T) * kH < (1LL << 31) && encode_tiled() != nullptr;
 }

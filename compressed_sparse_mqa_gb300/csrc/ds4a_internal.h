@@ -36,10 +36,10 @@ cudaError_t launch_attn_decode(const uint16_t *q, int H, int D, const uint16_t *
                                int n_sel, float scale, uint16_t *out, const Ctx &c);
 
 // tensor-core prefill attention (64 heads, head_dim 128, <= 768 keys per query)
-// the tensor-core prefill path takes H = 64, D = 128, 16-byte aligned queries and
+// the tensor-core prefill path takes H = 64, D = 128, 16-byte aligned queries and outputs, and
 // key lists of at most 6 tiles of 128 (window tiles + selected-row tiles)
-bool attn_prefill_tc_ok(const uint16_t *q, int T, int H, int D, int n_prior, int window, long long max_sel,
-                        long long n_comp);
+bool attn_prefill_tc_ok(const uint16_t *q, const uint16_t *out, int T, int H, int D, int n_prior, int window,
+                        long long max_sel, long long n_comp);
 cudaError_t launch_attn_prefill_tc(const uint16_t *q, int T, const uint16_t *raw_k, const uint16_t *raw_v,
                                    int n_prior, int window, const uint16_t *comp_k, const uint16_t *comp_v,
                                    long long n_comp, const int32_t *sel, int k_stride, long long q_pos0,
