@@ -36,6 +36,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kGroup = 16;                        // threads per scored row
 constexpr int kRowsPerPass = kThreads / kGroup;   // 32
 constexpr int kRowsPerCta = 2 * kRowsPerPass;     // decode slice: 64 rows
+constexpr int kStagedRows = 1024;                 // decode: rows per CTA scored before the dependency wait
 constexpr int kMaxDIdx = 256;
 constexpr int kMaxItems = 32;                     // register select: n <= 512 * 32
 constexpr size_t kWsHeader = 256;                 // ticket lives here
@@ -293,19 +294,30 @@ DS4A_DEVINL long long visible_rows(const IndexerArgs &a, int i) {
 __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs a, int rows_per_cta) {
     __shared__ SelectSmem sm;
     __shared__ bool s_last;
+    __shared__ uint32_t s_keys[kStagedRows];
     const long long n_vis = visible_rows(a, 0);
     const long long j0 = static_cast<long long>(blockIdx.x) * rows_per_cta;
     const long long j1 = min(n_vis, j0 + rows_per_cta);
-    RowLoads L;
-    load_rows(a.k_idx, a.d_idx, j0, j1, L);   // key rows: cache state, independent of the previous kernel
-    pdl_wait();
-    pdl_trigger();
+    // The query and the key rows are inputs no kernel of this library writes, so the
+    // first kStagedRows rows of the slice are scored into shared memory before
+    // waiting on the previous kernel; only the workspace and the output (which the
+    // previous kernel may still be using) are written after the wait.
+    const long long js = min(j1, j0 + kStagedRows);
     float qf[2][8];
     load_query(a.q_idx, a.d_idx, qf);
+    for (long long base = j0; base < js; base += kRowsPerCta) {
+        RowLoads L;
+        load_rows(a.k_idx, a.d_idx, base, js, L);
+        score_loaded(qf, L, base, js, s_keys + (base - j0));
+    }
+    pdl_wait();
+    pdl_trigger();
     unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws);
     uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + kWsHeader);
-    score_loaded(qf, L, j0, j1, keys + j0);
-    for (long long base = j0 + kRowsPerCta; base < j1; base += kRowsPerCta) {
+    __syncthreads();
+    for (long long j = j0 + threadIdx.x; j < js; j += kThreads) keys[j] = s_keys[j - j0];
+    for (long long base = js; base < j1; base += kRowsPerCta) {
+        RowLoads L;
         load_rows(a.k_idx, a.d_idx, base, j1, L);
         score_loaded(qf, L, base, j1, keys + base);
     }
