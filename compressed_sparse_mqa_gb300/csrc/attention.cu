@@ -23,8 +23,8 @@
 // one cluster barrier publishes the stores, and each CTA merges its own heads
 // by log-sum-exp from local shared memory.  A relaxed cluster arrive at kernel
 // start, waited on just before the first remote store, guarantees every peer
-// is running.  Window rows are cache state and are gathered before waiting on
-// the previous kernel.  No workspace, no second launch, no spin.
+// is running.  Window rows are cache state and, with the query, are gathered
+// before waiting on the previous kernel.  No workspace, no second launch, no spin.
 // Prefill: one CTA per query walks the query's whole row list (the shapes the
 // tensor-core kernel in attention_tc.cu does not take).
 #include <cooperative_groups.h>
@@ -374,10 +374,11 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
         issue_loads<D>(a.src, sm.off[0], sm.k[0], sm.v[0]);
         cp_async_commit();
     }
-    pdl_wait();
-    pdl_trigger();
+    // the query is an input no kernel of this library writes: loaded before the wait too
     uint32_t qa[D / 16][4];
     load_q_frags<D>(a.q, a.H, h0, qa);
+    pdl_wait();
+    pdl_trigger();
     WarpState<D> st;
     init_state<D>(st);
     attend_range<D>(a.src, v0, v1, qa, has_heads, kh, a.scale_log2, sm, st, pre);
