@@ -111,9 +111,12 @@ def test_c5_full_43_layer_stack():
 
 # ---- smaller prefill chunks, checked on every output ---------------------------------------
 
+# (128, 0, 40000, ...): three compressed-row tiles without sel; (4, 1024, ...): a key list of
+# 9 tiles, past the tensor-core kernel's 6, so the mma.sync kernel takes it
 @pytest.mark.parametrize("ratio,topk,P,T,W", [(4, 16, 200, 96, 32), (4, 512, 2100, 130, 128),
                                               (128, 0, 300, 200, 128), (0, 0, 50, 77, 128),
-                                              (4, 16, 0, 40, 32), (128, 0, 1000, 257, 64)])
+                                              (4, 16, 0, 40, 32), (128, 0, 1000, 257, 64),
+                                              (128, 0, 40000, 64, 128), (4, 1024, 8000, 64, 128)])
 def test_prefill_small_full(ratio, topk, P, T, W):
     inst = synth.prefill_instance(seed=11, layer=ratio, H=64, D=128, window=W, ratio=ratio, d_idx=128,
                                   topk=topk, P=P, T=T, sigma_w=configs.SIGMA_W)
