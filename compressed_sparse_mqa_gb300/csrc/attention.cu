@@ -18,12 +18,13 @@
 // head group are combined through shared memory at the end.
 //
 // Decode: one query, rows split across one thread-block cluster of 16 CTAs (8
-// if 16 cannot be scheduled).  Each CTA stores its (m, l, O) of head h straight
-// into the shared memory of the CTA that owns h (distributed shared memory),
-// one cluster barrier publishes the stores, and each CTA merges its own heads
-// by log-sum-exp from local shared memory.  A relaxed cluster arrive at kernel
-// start, waited on just before the first remote store, guarantees every peer
-// is running.  Window rows are cache state and, with the query, are gathered
+// if 16 cannot be scheduled).  Each CTA sends its (m, l, O) of head h straight
+// into the shared memory of the CTA that owns h with asynchronous remote stores
+// (st.async) that count their bytes on the owner's receive mbarrier; each CTA
+// waits only for the bytes destined to it, then merges its own heads by
+// log-sum-exp from local shared memory.  A cluster arrive at kernel start (after
+// the receive barrier is armed), waited on just before the first remote store,
+// guarantees every peer is running and ready.  Window rows are cache state and, with the query, are gathered
 // before waiting on the previous kernel.  No workspace, no second launch, no spin.
 // Prefill: one CTA per query walks the query's whole row list (the shapes the
 // tensor-core kernel in attention_tc.cu does not take).
@@ -327,7 +328,42 @@ DS4A_DEVINL void finish_l(WarpState<D> &st) {
     }
 }
 
-DS4A_DEVINL void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory"); }
+// shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
+DS4A_DEVINL uint32_t cluster_addr(const void *local, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n"
+                 : "=r"(r)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
+    return r;
+}
+// asynchronous store of two floats into another CTA's shared memory, counted in
+// bytes on that CTA's mbarrier
+DS4A_DEVINL void st_async_f2(uint32_t raddr, float x, float y, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];\n" ::"r"(raddr),
+                 "f"(x), "f"(y), "r"(rbar)
+                 : "memory");
+}
+DS4A_DEVINL void tc_mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))),
+                 "r"(count));
+}
+// bounded wait (about a second of wall time) for phase 0 of a receive barrier
+DS4A_DEVINL bool recv_wait(uint64_t *bar) {
+    const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t done;
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(done)
+                     : "r"(b)
+                     : "memory");
+        if (done) return true;
+        uint64_t now;
+        asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(now));
+        if (it == 0) t0 = now;
+        else if (now - t0 > 1000000000ull) return false;
+    }
+}
 DS4A_DEVINL void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
 DS4A_DEVINL void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
 
@@ -355,10 +391,25 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
     float *recv = reinterpret_cast<float *>(smem_raw + recv_offset<D>());
+    __shared__ __align__(8) uint64_t s_recv_bar;
     cg::cluster_group cluster = cg::this_cluster();
     const int cs = static_cast<int>(cluster.num_blocks());
     const int rank = static_cast<int>(cluster.block_rank());
-    cluster_arrive_relaxed();   // this CTA is running; waited on before the first remote store
+    // heads [hb, hb + nh) are merged here: every CTA of the cluster sends (O, m, l) of
+    // each of them, (D + 2) floats, into this CTA's receive buffer
+    const int hpc = (a.H + cs - 1) / cs;
+    const int hb = rank * hpc;
+    const int nh = max(0, min(a.H, hb + hpc) - hb);
+    if (threadIdx.x == 0) {
+        tc_mbar_init(&s_recv_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(
+                         static_cast<uint32_t>(__cvta_generic_to_shared(&s_recv_bar))),
+                     "r"(static_cast<uint32_t>(cs * nh * (D + 2) * 4))
+                     : "memory");
+    }
+    // this CTA is running and its receive barrier is armed; waited on before the first remote store
+    cluster_arrive_release();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int h0 = (warp & 3) * 16, kh = warp >> 2;
@@ -385,8 +436,8 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
     combine_halves<D>(st, reinterpret_cast<float *>(smem_raw));
     finish_l<D>(st);
 
-    // push (O, m, l) of each head to the CTA that owns it: recv[src rank][local head][D + 4]
-    const int hpc = (a.H + cs - 1) / cs;
+    // push (O, m, l) of each head to the CTA that owns it, recv[src rank][local head][D + 4],
+    // with asynchronous remote stores that complete on the owner's receive barrier
     cluster_wait();
     if (warp < 4 && has_heads) {
 #pragma unroll
@@ -394,23 +445,19 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
             const int h = h0 + g + 8 * r;
             if (h < a.H) {
                 const int owner = h / hpc;
-                float *dst = cluster.map_shared_rank(recv, owner) + (rank * hpc + (h - owner * hpc)) * (D + 4);
+                const uint32_t dst = cluster_addr(recv + (rank * hpc + (h - owner * hpc)) * (D + 4), owner);
+                const uint32_t bar = cluster_addr(&s_recv_bar, owner);
 #pragma unroll
                 for (int dn = 0; dn < D / 8; ++dn)
-                    *reinterpret_cast<float2 *>(dst + dn * 8 + 2 * t) = make_float2(st.o[dn][2 * r], st.o[dn][2 * r + 1]);
-                if (t == 0) {
-                    dst[D] = st.m[r];
-                    dst[D + 1] = st.l[r];
-                }
+                    st_async_f2(dst + (dn * 8 + 2 * t) * 4, st.o[dn][2 * r], st.o[dn][2 * r + 1], bar);
+                if (t == 0) st_async_f2(dst + D * 4, st.m[r], st.l[r], bar);
             }
         }
     }
-    cluster_arrive_release();
-    cluster_wait();
+    // every byte destined for this CTA has landed
+    if (!recv_wait(&s_recv_bar)) record_error(a.src.err, DS4A_ERR_TIMEOUT);
 
     // merge this CTA's heads from local shared memory
-    const int hb = rank * hpc;
-    const int nh = max(0, min(a.H, hb + hpc) - hb);
     for (int idx = threadIdx.x; idx < nh * (D / 4); idx += kThreads) {
         const int hh = idx / (D / 4), d = (idx % (D / 4)) * 4;
         float M = -INFINITY;
