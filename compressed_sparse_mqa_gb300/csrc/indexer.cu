@@ -45,6 +45,7 @@ constexpr int kSmemKeyCap = 16384;                // prefill: keys staged in sha
 struct SelectSmem {
     uint32_t hist[sel::kMaxBins];
     uint32_t cnt[kMaxItems * kWarps];
+    uint32_t eq_bits[kMaxItems * kWarps];
     uint32_t scan[kWarps];
     uint32_t res[3];
     uint32_t bin;
@@ -202,8 +203,7 @@ __device__ void select_regs(const uint32_t *src, int n, int k, int32_t *out, Sel
     }
     uint32_t prefix, mask, kk;
     const bool all_eq = sel::find_threshold<kThreads, ITEMS>(key, n, k, sm.hist, sm.scan, sm.res, prefix, mask, kk);
-    const uint32_t flags = sel::topk_flags<kThreads, ITEMS>(key, n, prefix, mask, kk, all_eq, sm.cnt, sm.scan);
-    sel::emit<kThreads, ITEMS>(flags, out, sm.cnt, sm.scan);
+    sel::emit_topk_bits<kThreads, ITEMS>(key, n, prefix, mask, kk, all_eq, sm.cnt, sm.eq_bits, sm.scan, out);
 }
 
 // Any n > k: keys re-read from memory each pass; thread t emits the contiguous range [t*C, t*C + C).

@@ -150,5 +150,55 @@ DS4A_DEVINL uint32_t topk_flags(const uint32_t (&key)[ITEMS], int n, uint32_t pr
     return gt | take;
 }
 
+// Flags of the exact top-k, written out in ascending row order, for keys in the
+// item-major layout: a warp's ballot of one item is the bit word of 32 consecutive
+// rows, so the "above the boundary" and "on the boundary" rows become two bitmasks
+// in shared memory; thread t then takes rows t*ITEMS .. t*ITEMS + ITEMS-1 of them
+// (row order = thread order), ranks its boundary rows and its kept rows with one
+// block scan each, and writes its kept rows.  gt_bits, eq_bits: ITEMS*NT/32 words.
+template <int NT, int ITEMS>
+DS4A_DEVINL void emit_topk_bits(const uint32_t (&key)[ITEMS], int n, uint32_t prefix, uint32_t mask, uint32_t kk,
+                                bool all_eq, uint32_t *gt_bits, uint32_t *eq_bits, uint32_t *scratch,
+                                int32_t *out) {
+    static_assert(ITEMS <= 32 && 32 % ITEMS == 0, "a thread's rows lie in one bit word");
+    constexpr int kW = NT / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const bool valid = it * NT + tid < n;
+        const uint32_t km = key[it] & mask;
+        const unsigned g = __ballot_sync(0xffffffffu, valid && km > prefix);
+        const unsigned e = __ballot_sync(0xffffffffu, valid && km == prefix);
+        if (lane == 0) {
+            gt_bits[it * kW + warp] = g;
+            eq_bits[it * kW + warp] = e;
+        }
+    }
+    __syncthreads();
+    const int w = tid * ITEMS / 32, sh = tid * ITEMS % 32;
+    const uint32_t seg = ITEMS == 32 ? 0xFFFFFFFFu : ((1u << (ITEMS & 31)) - 1u);
+    const uint32_t g = (gt_bits[w] >> sh) & seg;
+    uint32_t e = (eq_bits[w] >> sh) & seg;
+    if (!all_eq) {
+        const uint32_t before = block_excl_scan<NT>(static_cast<uint32_t>(__popc(e)), scratch);
+        // keep the first kk - before boundary rows of this thread (lowest rows first)
+        const int keep = before >= kk ? 0 : static_cast<int>(min(static_cast<uint32_t>(__popc(e)), kk - before));
+        uint32_t t = e, kept = 0;
+        for (int j = 0; j < keep; ++j) {
+            const uint32_t low = t & (0u - t);
+            kept |= low;
+            t ^= low;
+        }
+        e = kept;
+    }
+    uint32_t sel_bits = g | e;
+    uint32_t pos = block_excl_scan<NT>(static_cast<uint32_t>(__popc(sel_bits)), scratch);
+    while (sel_bits) {
+        const int b = __ffs(sel_bits) - 1;
+        out[pos++] = tid * ITEMS + b;
+        sel_bits &= sel_bits - 1u;
+    }
+}
+
 }  // namespace sel
 }  // namespace ds4a
