@@ -358,13 +358,15 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) indexer_select_kernel(SelArgs 
             }
             if (rank < need) atomicOr(&sm.sel_bits[jb >> 5], 1u << (jb & 31));
         }
-        __syncthreads();
+        // the certainly kept rows join the band's kept rows in the row bitmask
+        // (a warp's ballot of one item is the word of its 32 consecutive rows)
 #pragma unroll
         for (int it = 0; it < ITEMS; ++it) {
-            const int j = it * kSelThreads + tid;
-            if (j < n && ((sm.sel_bits[j >> 5] >> (j & 31)) & 1u)) flags |= 1u << it;
+            const unsigned b = __ballot_sync(0xffffffffu, (flags >> it) & 1u);
+            if (lane == 0 && b) atomicOr(&sm.sel_bits[it * (kSelThreads / 32) + warp], b);
         }
-        sel::emit<kSelThreads, ITEMS>(flags, out, sm.cnt, sm.scan);
+        __syncthreads();
+        sel::emit_bits<kSelThreads, ITEMS>(sm.sel_bits, sm.scan, out);
         return;
     }
 
@@ -381,8 +383,7 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) indexer_select_kernel(SelArgs 
         key[it] = j < n ? reinterpret_cast<const uint32_t *>(row)[j] : 0u;
     }
     const bool all_eq = sel::find_threshold<kSelThreads, ITEMS>(key, n, a.k, sm.hist, sm.scan, sm.res, prefix, mask, kk);
-    flags = sel::topk_flags<kSelThreads, ITEMS>(key, n, prefix, mask, kk, all_eq, sm.cnt, sm.scan);
-    sel::emit<kSelThreads, ITEMS>(flags, out, sm.cnt, sm.scan);
+    sel::emit_topk_bits<kSelThreads, ITEMS>(key, n, prefix, mask, kk, all_eq, sm.cnt, sm.sel_bits, sm.scan, out);
 }
 
 constexpr int kSelNT = 256, kSelMinBlocks = 4;   // threads per query, CTAs per SM (<= 64 registers)

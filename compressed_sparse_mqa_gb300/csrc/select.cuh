@@ -200,5 +200,21 @@ DS4A_DEVINL void emit_topk_bits(const uint32_t (&key)[ITEMS], int n, uint32_t pr
     }
 }
 
+// Rows whose bit is set in `bits` (row r is bit r%32 of word r/32), in ascending
+// order, to out[]: thread t takes rows t*ITEMS .. t*ITEMS + ITEMS-1 and one block
+// scan places them.
+template <int NT, int ITEMS>
+DS4A_DEVINL void emit_bits(const uint32_t *bits, uint32_t *scratch, int32_t *out) {
+    static_assert(ITEMS <= 32 && 32 % ITEMS == 0, "a thread's rows lie in one bit word");
+    const int tid = threadIdx.x;
+    const uint32_t seg = ITEMS == 32 ? 0xFFFFFFFFu : ((1u << (ITEMS & 31)) - 1u);
+    uint32_t m = (bits[tid * ITEMS / 32] >> (tid * ITEMS % 32)) & seg;
+    uint32_t pos = block_excl_scan<NT>(static_cast<uint32_t>(__popc(m)), scratch);
+    while (m) {
+        out[pos++] = tid * ITEMS + __ffs(m) - 1;
+        m &= m - 1u;
+    }
+}
+
 }  // namespace sel
 }  // namespace ds4a
