@@ -37,18 +37,13 @@ struct CompressArgs {
     int ratio;
 };
 
-// Pool tokens [t0, t1) of block b (t1 - t0 <= ratio).  If `resume`, continue
-// from the stored running state.  If t1 closes the block, write row b, else
-// store the running state.
-__device__ void pool_segment(const CompressArgs &a, long long b, long long t0, long long t1,
-                             bool resume, float *s_w, float *s_red) {
+// Scores s_i = w . k_i of tokens [t0, t1) into s_w: one warp per token, lanes
+// over 8-dim chunks.  Reads only the caller's inputs (k, w).
+__device__ void segment_scores(const CompressArgs &a, long long t0, long long t1, float *s_w) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int D = a.D;
     const int n = static_cast<int>(t1 - t0);
     const uint16_t *kb = a.k + (t0 - a.pos) * D;
-    const uint16_t *vb = a.v + (t0 - a.pos) * D;
-
-    // scores s_i = w . k_i: one warp per token, lanes over 8-dim chunks
     for (int i = warp; i < n; i += kThreads / 32) {
         float acc = 0.f;
         for (int ch = lane; ch < D / 8; ch += 32) {
@@ -61,6 +56,18 @@ __device__ void pool_segment(const CompressArgs &a, long long b, long long t0, l
         if (lane == 0) s_w[i] = acc;
     }
     __syncthreads();
+}
+
+// Pool tokens [t0, t1) of block b (t1 - t0 <= ratio) whose scores are in s_w.  If
+// `resume`, continue from the stored running state.  If t1 closes the block,
+// write row b, else store the running state.
+__device__ void pool_segment(const CompressArgs &a, long long b, long long t0, long long t1,
+                             bool resume, float *s_w, float *s_red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int D = a.D;
+    const int n = static_cast<int>(t1 - t0);
+    const uint16_t *kb = a.k + (t0 - a.pos) * D;
+    const uint16_t *vb = a.v + (t0 - a.pos) * D;
 
     // segment max
     float m = -INFINITY;
@@ -109,24 +116,44 @@ __device__ void pool_segment(const CompressArgs &a, long long b, long long t0, l
 __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
     __shared__ float s_w[kMaxRatio];
     __shared__ float s_red[kThreads / 32];
-    pdl_wait();
-    pdl_trigger();
     const long long r = a.ratio;
     const long long end = a.pos + a.n_new;
     const long long b_first = a.pos / r, b_last = (end - 1) / r;
     const bool first_open = (a.pos % r) != 0;
     const bool last_open = (end % r) != 0;
     const long long fc_lo = b_first + (first_open ? 1 : 0);
+    // this CTA's segments: [t0a, t1a) of block ba (resumed if CTA 0 continues the
+    // open block), then for CTA 0 possibly the block this call leaves open
+    long long ba, t0a, t1a;
+    bool resume_a;
     if (blockIdx.x == 0) {
         if (first_open) {
-            const long long t1 = (b_first + 1) * r < end ? (b_first + 1) * r : end;
-            pool_segment(a, b_first, a.pos, t1, true, s_w, s_red);
+            ba = b_first;
+            t0a = a.pos;
+            t1a = (b_first + 1) * r < end ? (b_first + 1) * r : end;
+            resume_a = true;
+        } else {
+            ba = b_last;
+            t0a = b_last * r;
+            t1a = end;
+            resume_a = false;
         }
-        if (last_open && !(first_open && b_last == b_first))
-            pool_segment(a, b_last, b_last * r, end, false, s_w, s_red);
     } else {
-        const long long b = fc_lo + blockIdx.x - 1;
-        pool_segment(a, b, b * r, (b + 1) * r, false, s_w, s_red);
+        ba = fc_lo + blockIdx.x - 1;
+        t0a = ba * r;
+        t1a = (ba + 1) * r;
+        resume_a = false;
+    }
+    const bool has_a = blockIdx.x != 0 || first_open || last_open;
+    // The scores read only the caller's inputs: computed before waiting on the
+    // previous kernel; the running state and the outputs are touched after it.
+    if (has_a) segment_scores(a, t0a, t1a, s_w);
+    pdl_wait();
+    pdl_trigger();
+    if (has_a) pool_segment(a, ba, t0a, t1a, resume_a, s_w, s_red);
+    if (blockIdx.x == 0 && first_open && last_open && b_last != b_first) {
+        segment_scores(a, b_last * r, end, s_w);
+        pool_segment(a, b_last, b_last * r, end, false, s_w, s_red);
     }
 }
 
