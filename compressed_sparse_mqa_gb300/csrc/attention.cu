@@ -18,7 +18,9 @@
 // head group are combined through shared memory at the end.
 //
 // Decode: one query, rows split across one thread-block cluster of 16 CTAs (8
-// if 16 cannot be scheduled).  Each CTA sends its (m, l, O) of head h straight
+// if 16 cannot be scheduled).  Inside a CTA the 8 warps split by head group x
+// half of d instead (compute_tile_dsplit): both halves compute the same scores,
+// and no partial state has to be combined across warps.  Each CTA sends its (m, l, O) of head h straight
 // into the shared memory of the CTA that owns h with asynchronous remote stores
 // (st.async) that count their bytes on the owner's receive mbarrier; each CTA
 // waits only for the bytes destined to it, then merges its own heads by
@@ -38,7 +40,7 @@ namespace cg = cooperative_groups;
 namespace ds4a {
 namespace {
 
-constexpr int kThreads = 256;    // 8 warps: 4 head groups x 2 key halves
+constexpr int kThreads = 256;    // 8 warps: 4 head groups x 2 key halves (decode: x 2 halves of d)
 constexpr int kBN = 64;           // rows per tile
 constexpr int kHalf = kBN / 2;    // keys per warp per tile
 constexpr float kLog2e = 1.4426950408889634f;
@@ -318,6 +320,140 @@ DS4A_DEVINL void combine_halves(WarpState<D> &st, float *xch) {
     __syncthreads();
 }
 
+// ---- decode tile engine: warps split by head group x half of d ------------------------------
+// Warp w owns heads 16(w%4) .. +15 and output columns d in [(w/4) D/2, (w/4 + 1) D/2): it
+// computes S for all the tile's keys (the two d halves of a head group compute the same S
+// and the same softmax state), and O += P V for its half of d only.  Nothing has to be
+// combined across warps afterwards.
+
+template <int D>
+struct WarpStateH {
+    float o[D / 16][4];   // rows g and g+8 of the warp's 16 heads, D/2 columns
+    float m[2];
+    float l[2];
+};
+
+template <int D>
+DS4A_DEVINL void compute_tile_dsplit(const uint32_t (&qa)[D / 16][4], const uint16_t *kt, const uint16_t *vt,
+                                     const long long *off, int nvalid, int dh, float scale_log2,
+                                     WarpStateH<D> &st) {
+    const int lane = threadIdx.x & 31, t = lane & 3;
+    if (nvalid <= 0) return;
+    const int groups = min(kBN / 16, (nvalid + 15) / 16);   // 16-key groups holding list rows
+    const unsigned char *kb = reinterpret_cast<const unsigned char *>(kt);
+    const unsigned char *vb = reinterpret_cast<const unsigned char *>(vt);
+    float s[kBN / 8][4];
+#pragma unroll
+    for (int nt = 0; nt < kBN / 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+    // S = Q K^T over the tile: ldmatrix x4 gives b0/b1 for two key tiles (one 16-key group)
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+        for (int gq = 0; gq < kBN / 16; ++gq) {
+            if (gq < groups) {
+                const int key = gq * 16 + (lane & 7) + ((lane >> 4) << 3);
+                const int ch = 2 * ks + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4(b0, b1, b2, b3, kb + swz<D>(key, ch));
+                mma_16816(s[2 * gq], qa[ks], b0, b1);
+                mma_16816(s[2 * gq + 1], qa[ks], b2, b3);
+            }
+        }
+    }
+    // scale into the log2 domain, mask padding rows, running max
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < kBN / 8; ++nt) {
+        const int kr = nt * 8 + 2 * t;
+        const bool v0 = off[kr] >= 0, v1 = off[kr + 1] >= 0;
+        s[nt][0] = v0 ? s[nt][0] * scale_log2 : -INFINITY;
+        s[nt][1] = v1 ? s[nt][1] * scale_log2 : -INFINITY;
+        s[nt][2] = v0 ? s[nt][2] * scale_log2 : -INFINITY;
+        s[nt][3] = v1 ? s[nt][3] * scale_log2 : -INFINITY;
+        mx[0] = fmaxf(mx[0], fmaxf(s[nt][0], s[nt][1]));
+        mx[1] = fmaxf(mx[1], fmaxf(s[nt][2], s[nt][3]));
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+    }
+    float ref[2], alpha[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const float m_new = fmaxf(st.m[r], mx[r]);
+        ref[r] = m_new == -INFINITY ? 0.f : m_new;
+        alpha[r] = exp2f(st.m[r] - ref[r]);
+        st.m[r] = m_new;
+        st.l[r] *= alpha[r];
+    }
+#pragma unroll
+    for (int dn = 0; dn < D / 16; ++dn) {
+        st.o[dn][0] *= alpha[0];
+        st.o[dn][1] *= alpha[0];
+        st.o[dn][2] *= alpha[1];
+        st.o[dn][3] *= alpha[1];
+    }
+    uint32_t pa[kBN / 16][4];
+#pragma unroll
+    for (int nt = 0; nt < kBN / 8; ++nt) {
+        const float p0 = exp2f(s[nt][0] - ref[0]), p1 = exp2f(s[nt][1] - ref[0]);
+        const float p2 = exp2f(s[nt][2] - ref[1]), p3 = exp2f(s[nt][3] - ref[1]);
+        st.l[0] += p0 + p1;
+        st.l[1] += p2 + p3;
+        const int kk = nt >> 1, hi = nt & 1;
+        pa[kk][hi ? 2 : 0] = pack_half2(p0, p1);
+        pa[kk][hi ? 3 : 1] = pack_half2(p2, p3);
+    }
+    // O += P V over this warp's half of d: ldmatrix.trans x4 gives b0/b1 for two d tiles
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+        if (kk < groups) {
+#pragma unroll
+            for (int dn = 0; dn < D / 16; dn += 2) {
+                const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                const int ch = dh * (D / 16) + dn + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldmatrix_x4_trans(b0, b1, b2, b3, vb + swz<D>(key, ch));
+                mma_16816(st.o[dn], pa[kk], b0, b1);
+                mma_16816(st.o[dn + 1], pa[kk], b2, b3);
+            }
+        }
+    }
+}
+
+// Walk virtual rows [v_begin, v_end) with the d-split engine (as attend_range).
+template <int D>
+__device__ void attend_range_dsplit(const RowSrc &src, int v_begin, int v_end, const uint32_t (&qa)[D / 16][4],
+                                    bool has_heads, int dh, float scale_log2, Smem<D> &sm, WarpStateH<D> &st,
+                                    bool tile0_issued) {
+    const int n_tiles = v_end > v_begin ? (v_end - v_begin + kBN - 1) / kBN : 0;
+    if (n_tiles == 0) return;
+    if (!tile0_issued) {
+        build_table<D>(src, v_begin, v_end, sm.off[0], &sm.nvalid[0]);
+        __syncthreads();
+        issue_loads<D>(src, sm.off[0], sm.k[0], sm.v[0]);
+        cp_async_commit();
+    }
+    for (int it = 0; it < n_tiles; ++it) {
+        __syncthreads();
+        if (it + 1 < n_tiles) {
+            const int b = (it + 1) & 1;
+            build_table<D>(src, v_begin + (it + 1) * kBN, v_end, sm.off[b], &sm.nvalid[b]);
+            __syncthreads();
+            issue_loads<D>(src, sm.off[b], sm.k[b], sm.v[b]);
+        }
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const int b = it & 1;
+        if (has_heads) compute_tile_dsplit<D>(qa, sm.k[b], sm.v[b], sm.off[b], sm.nvalid[b], dh, scale_log2, st);
+    }
+    __syncthreads();
+}
+
 // quad-reduce the per-lane partial sums of l
 template <int D>
 DS4A_DEVINL void finish_l(WarpState<D> &st) {
@@ -412,7 +548,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
     cluster_arrive_release();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int h0 = (warp & 3) * 16, kh = warp >> 2;
+    const int h0 = (warp & 3) * 16, dh = warp >> 2;   // head group, half of d
     const bool has_heads = h0 < a.H;
     const int chunk = (a.n_rows + cs - 1) / cs;
     const int v0 = min(a.n_rows, rank * chunk);
@@ -430,16 +566,24 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
     load_q_frags<D>(a.q, a.H, h0, qa);
     pdl_wait();
     pdl_trigger();
-    WarpState<D> st;
-    init_state<D>(st);
-    attend_range<D>(a.src, v0, v1, qa, has_heads, kh, a.scale_log2, sm, st, pre);
-    combine_halves<D>(st, reinterpret_cast<float *>(smem_raw));
-    finish_l<D>(st);
+    WarpStateH<D> st;
+#pragma unroll
+    for (int dn = 0; dn < D / 16; ++dn)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st.o[dn][e] = 0.f;
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
+    attend_range_dsplit<D>(a.src, v0, v1, qa, has_heads, dh, a.scale_log2, sm, st, pre);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {   // quad-reduce the per-lane partial sums of l
+        st.l[r] += __shfl_xor_sync(0xffffffffu, st.l[r], 1);
+        st.l[r] += __shfl_xor_sync(0xffffffffu, st.l[r], 2);
+    }
 
     // push (O, m, l) of each head to the CTA that owns it, recv[src rank][local head][D + 4],
     // with asynchronous remote stores that complete on the owner's receive barrier
     cluster_wait();
-    if (warp < 4 && has_heads) {
+    if (has_heads) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int h = h0 + g + 8 * r;
@@ -448,9 +592,9 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
                 const uint32_t dst = cluster_addr(recv + (rank * hpc + (h - owner * hpc)) * (D + 4), owner);
                 const uint32_t bar = cluster_addr(&s_recv_bar, owner);
 #pragma unroll
-                for (int dn = 0; dn < D / 8; ++dn)
-                    st_async_f2(dst + (dn * 8 + 2 * t) * 4, st.o[dn][2 * r], st.o[dn][2 * r + 1], bar);
-                if (t == 0) st_async_f2(dst + D * 4, st.m[r], st.l[r], bar);
+                for (int dn = 0; dn < D / 16; ++dn)
+                    st_async_f2(dst + (dh * (D / 2) + dn * 8 + 2 * t) * 4, st.o[dn][2 * r], st.o[dn][2 * r + 1], bar);
+                if (t == 0 && dh == 0) st_async_f2(dst + D * 4, st.m[r], st.l[r], bar);
             }
         }
     }
