@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
     __shared__ uint32_t s_tmem;
     __shared__ __align__(8) uint64_t s_bar[2];
     __shared__ uint32_t s_kmax2;
+    __shared__ float s_stage[kGemmThreads / 32][32 * 33];   // epilogue transpose, padded against bank conflicts
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int m0 = blockIdx.x * kTM;
@@ -104,26 +105,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
     }
 
     bool ok = true;
+    // Epilogue: lane l of warp w holds query row 32w + l.  Each 32 x 32 block goes
+    // through a padded shared tile so that a store instruction writes 128-byte runs
+    // of four rows instead of 16 bytes of 32 rows.
     auto epilogue = [&](int it) {
         const int buf = it & 1;
         if (!tc::mbar_wait(&s_bar[buf], (it >> 1) & 1)) ok = false;
         tc::fence_after_sync();
-        const int row = warp * 32 + lane;
-        const int q = m0 + row;
         const long long col0 = static_cast<long long>(ns + it * a.n_split) * kTN;
-        float *dst = a.scores + static_cast<long long>(q) * a.ld + col0;
+        float *stg = s_stage[warp];
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTN; c0 += 16) {
+        for (int c0 = 0; c0 < kTN; c0 += 32) {
             uint32_t r[16];
-            tc::ld_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + buf * kTN + c0, r);
-            tc::wait_ld();
-            if (ok && q < a.n_q) {
 #pragma unroll
-                for (int j = 0; j < 16; j += 4)
-                    *reinterpret_cast<float4 *>(dst + c0 + j) =
-                        make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                    __uint_as_float(r[j + 3]));
+            for (int h = 0; h < 2; ++h) {
+                tc::ld_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + buf * kTN + c0 + 16 * h, r);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) stg[lane * 33 + 16 * h + j] = __uint_as_float(r[j]);
             }
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int row = 4 * k + (lane >> 3), cg = 4 * (lane & 7);
+                const int q = m0 + warp * 32 + row;
+                const float *src = stg + row * 33 + cg;
+                if (ok && q < a.n_q)
+                    *reinterpret_cast<float4 *>(a.scores + static_cast<long long>(q) * a.ld + col0 + c0 + cg) =
+                        make_float4(src[0], src[1], src[2], src[3]);
+            }
+            __syncwarp();
         }
     };
 
