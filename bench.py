@@ -3,7 +3,7 @@
 
 Headline step: one batch-1 decode token through one ratio-4 layer with the
 indexer at context 32768 (8192 compressed rows, top-512, 128-row raw window, 64
-heads, head_dim 128, fp16): ds4a_compress_append -> ds4a_indexer_topk ->
+heads, head_dim 128, fp16): ds4a_indexer_topk -> ds4a_compress_append ->
 ds4a_attn_decode.  Metric: tokens/s/layer (= steps/s) and the HBM bandwidth the
 step's algorithmic bytes imply.
 
@@ -79,6 +79,13 @@ def max_over_ranks(x: float, world: int) -> float:
     t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(ms: float, steps: int, world: int) -> tuple[float, float]:
+    """The slowest rank's time (ms) for `steps` steps on every rank, and the whole-job
+    rate world * steps / that time (steps per second over all ranks)."""
+    ms = max_over_ranks(ms, world)
+    return ms, world * steps / (ms / 1e3)
 
 
 def graph_size(k: int, cap: int = 1024) -> int:
@@ -178,10 +185,9 @@ def run_ours(args, rank, world, local):
         ms = timing.time_graph(g, reps, stream)
     barrier(world)
     clocks = clk.summary()
-    ms = max_over_ranks(ms, world)
     steps = G * reps
+    ms, value = job_throughput(ms, steps, world)
     s_per_step = ms / 1e3 / steps
-    value = world * steps / (ms / 1e3)
     gbs = step_bytes / s_per_step / 1e9
 
     # ---- per-kernel durations (events around each launch, on the launching stream) -------
