@@ -472,11 +472,12 @@ DS4A_DEVINL uint32_t cluster_addr(const void *local, int rank) {
                  : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
     return r;
 }
-// asynchronous store of two floats into another CTA's shared memory, counted in
-// bytes on that CTA's mbarrier
-DS4A_DEVINL void st_async_f2(uint32_t raddr, float x, float y, uint32_t rbar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];\n" ::"r"(raddr),
-                 "f"(x), "f"(y), "r"(rbar)
+// bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this
+// CTA's shared memory into another CTA's, counted in bytes on that CTA's mbarrier
+DS4A_DEVINL void bulk_copy_to_cta(uint32_t raddr, const void *local, uint32_t bytes, uint32_t rbar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                     raddr),
+                 "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(bytes), "r"(rbar)
                  : "memory");
 }
 DS4A_DEVINL void tc_mbar_init(uint64_t *bar, uint32_t count) {
@@ -521,6 +522,8 @@ constexpr size_t decode_smem() { return recv_offset<D>() + kRecvRows * (D + 4) *
 template <int D>
 constexpr size_t prefill_smem() { return sizeof(Smem<D>); }
 static_assert(4 * 32 * (128 / 2 + 4) * sizeof(float) <= sizeof(Smem<128>), "exchange fits in the tiles");
+static_assert(64 * (128 + 4) * sizeof(float) <= sizeof(Smem<128>) && 64 * (64 + 4) * sizeof(float) <= sizeof(Smem<64>),
+              "the send rows of 64 heads fit in the tiles");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
@@ -532,7 +535,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
     const int cs = static_cast<int>(cluster.num_blocks());
     const int rank = static_cast<int>(cluster.block_rank());
     // heads [hb, hb + nh) are merged here: every CTA of the cluster sends (O, m, l) of
-    // each of them, (D + 2) floats, into this CTA's receive buffer
+    // each of them, a row of D + 4 floats (16-byte multiple), into this CTA's receive buffer
     const int hpc = (a.H + cs - 1) / cs;
     const int hb = rank * hpc;
     const int nh = max(0, min(a.H, hb + hpc) - hb);
@@ -541,7 +544,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(
                          static_cast<uint32_t>(__cvta_generic_to_shared(&s_recv_bar))),
-                     "r"(static_cast<uint32_t>(cs * nh * (D + 2) * 4))
+                     "r"(static_cast<uint32_t>(cs * nh * (D + 4) * 4))
                      : "memory");
     }
     // this CTA is running and its receive barrier is armed; waited on before the first remote store
@@ -580,23 +583,37 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
         st.l[r] += __shfl_xor_sync(0xffffffffu, st.l[r], 2);
     }
 
-    // push (O, m, l) of each head to the CTA that owns it, recv[src rank][local head][D + 4],
-    // with asynchronous remote stores that complete on the owner's receive barrier
-    cluster_wait();
+    // Stage (O, m, l) of each head in this CTA's own shared memory, send[h][D + 4] (the
+    // tiles are free once every warp is past them), then send the rows of each
+    // owner's heads with one bulk copy into recv[this rank] there; the copies
+    // complete on the owner's receive barrier.
+    float *send = reinterpret_cast<float *>(smem_raw);
+    __syncthreads();
     if (has_heads) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int h = h0 + g + 8 * r;
             if (h < a.H) {
-                const int owner = h / hpc;
-                const uint32_t dst = cluster_addr(recv + (rank * hpc + (h - owner * hpc)) * (D + 4), owner);
-                const uint32_t bar = cluster_addr(&s_recv_bar, owner);
+                float *row = send + h * (D + 4);
 #pragma unroll
                 for (int dn = 0; dn < D / 16; ++dn)
-                    st_async_f2(dst + (dh * (D / 2) + dn * 8 + 2 * t) * 4, st.o[dn][2 * r], st.o[dn][2 * r + 1], bar);
-                if (t == 0 && dh == 0) st_async_f2(dst + D * 4, st.m[r], st.l[r], bar);
+                    *reinterpret_cast<float2 *>(row + dh * (D / 2) + dn * 8 + 2 * t) =
+                        make_float2(st.o[dn][2 * r], st.o[dn][2 * r + 1]);
+                if (t == 0 && dh == 0) *reinterpret_cast<float2 *>(row + D) = make_float2(st.m[r], st.l[r]);
             }
         }
+    }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");   // the copies read through the async proxy
+    __syncthreads();
+    cluster_wait();   // every CTA's receive barrier is armed
+    if (threadIdx.x == 0) {
+        for (int o = 0; o < cs; ++o) {
+            const int nho = min(a.H, (o + 1) * hpc) - o * hpc;
+            if (nho > 0)
+                bulk_copy_to_cta(cluster_addr(recv + rank * hpc * (D + 4), o), send + o * hpc * (D + 4),
+                                 static_cast<uint32_t>(nho * (D + 4) * 4), cluster_addr(&s_recv_bar, o));
+        }
+        asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
     }
     // every byte destined for this CTA has landed
     if (!recv_wait(&s_recv_bar)) record_error(a.src.err, DS4A_ERR_TIMEOUT);
@@ -625,6 +642,8 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
         packed.y = pack_half2(acc.z * inv, acc.w * inv);
         *reinterpret_cast<uint2 *>(a.out + (hb + hh) * D + d) = packed;
     }
+    // this CTA's outgoing copies have finished reading its shared memory
+    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
 
 struct PrefillArgs {
