@@ -3,9 +3,10 @@
 
 Headline step: one batch-1 decode token through one ratio-4 layer with the
 indexer at context 32768 (8192 compressed rows, top-512, 128-row raw window, 64
-heads, head_dim 128, fp16): ds4a_indexer_topk -> ds4a_compress_append ->
-ds4a_attn_decode.  Metric: tokens/s/layer (= steps/s) and the HBM bandwidth the
-step's algorithmic bytes imply.
+heads, head_dim 128, fp16): ds4a_indexer_topk_compress (the indexer query and
+the compressor's update for the new token, in one launch) -> ds4a_attn_decode.
+Metric: tokens/s/layer (= steps/s) and the HBM bandwidth the step's algorithmic
+bytes imply.
 
 Inputs are resident in HBM.  The timed steps rotate over enough independent
 copies of the layer state that the working set is more than twice the L2, so
@@ -101,24 +102,32 @@ def rotation_copies(bytes_per_copy: int, l2_bytes: int, minimum: int = 2) -> int
     return max(minimum, math.ceil(2 * l2_bytes / max(bytes_per_copy, 1)) + 1)
 
 
-KERNEL_SOURCES = {"indexer_topk": "indexer.cu", "attn_decode": "attention.cu", "compress_append": "compress.cu"}
+KERNEL_SOURCES = {"indexer_topk_compress": ["indexer.cu", "compress_dev.cuh", "select.cuh"],
+                  "attn_decode": ["attention.cu"]}
 
 
 def kernel_traffic(name: str):
     """DRAM bytes per launch from the committed ncu capture of this kernel, or None
     when the kernel's source has changed since the counters were taken."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "compressed_sparse_mqa_gb300", "csrc", KERNEL_SOURCES.get(name, ""))
-    if not os.path.exists(path) or not os.path.isfile(src):
+    srcs = [os.path.join(ROOT, "compressed_sparse_mqa_gb300", "csrc", f) for f in KERNEL_SOURCES.get(name, [])]
+    if not os.path.exists(path) or not srcs or not all(os.path.isfile(f) for f in srcs):
         return None
     with open(path) as f:
         entry = json.load(f).get(name)
     if not entry:
         return None
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()
-    return entry["dram_bytes_per_launch"] if entry.get("source_sha256") == digest else None
+    return entry["dram_bytes_per_launch"] if entry.get("source_sha256") == source_digest(srcs) else None
+
+
+def source_digest(paths) -> str:
+    """sha256 over the concatenated contents of a kernel's source files."""
+    import hashlib
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def cpu_cores() -> int:
@@ -191,14 +200,11 @@ def run_ours(args, rank, world, local):
     gbs = step_bytes / s_per_step / 1e9
 
     # ---- per-kernel durations (events around each launch, on the launching stream) -------
-    def k_compress(t):
+    def k_prep(t):
         L = layers[t % R]
-        ds4a.ds4a_compress_append(L.ring_k[L.slot:L.slot + 1], L.ring_v[L.slot:L.slot + 1], L.w, L.ratio, L.p,
-                                  L.state, L.comp_k, L.comp_v)
-
-    def k_indexer(t):
-        L = layers[t % R]
-        ds4a.ds4a_indexer_topk(L.q_idx, L.kidx, L.p, L.ratio, L.topk, L.sel, L.sel_n, L.ws)
+        ds4a.ds4a_indexer_topk_compress(L.q_idx, L.kidx, L.p, L.ratio, L.topk, L.sel, L.sel_n, L.ws,
+                                        L.ring_k[L.slot:L.slot + 1], L.ring_v[L.slot:L.slot + 1], L.w, L.state,
+                                        L.comp_k, L.comp_v)
 
     def k_attn(t):
         L = layers[t % R]
@@ -209,14 +215,15 @@ def run_ours(args, rank, world, local):
     # CUDA events around its replays on the launching stream; average per launch
     n_k = 1024
     kt = {}
-    for name, fn in [("compress_append", k_compress), ("indexer_topk", k_indexer), ("attn_decode", k_attn)]:
+    for name, fn in [("indexer_topk_compress", k_prep), ("attn_decode", k_attn)]:
         gk = timing.capture_graph(fn, n_k, stream)
         gk.replay()
         kt[name] = timing.time_graph(gk, 4, stream) / (4 * n_k)
     D, H = base.D, base.H
     kbytes = {
-        "compress_append": 2 * D * 2 + D * 4 + (2 + 2 * D) * 4,
-        "indexer_topk": base.n_vis * base.kidx.shape[1] * 2 + base.kidx.shape[1] * 2 + base.topk * 4 + 4,
+        # indexer keys + query + kept indices, and the compressor's token, score vector and state
+        "indexer_topk_compress": base.n_vis * base.kidx.shape[1] * 2 + base.kidx.shape[1] * 2 + base.topk * 4 + 4
+        + 2 * D * 2 + D * 4 + (2 + 2 * D) * 4,
         "attn_decode": 2 * H * D * 2 + 2 * (base.n_win + base.topk) * D * 2 + base.topk * 4,
     }
     dom = max(kt, key=kt.get)

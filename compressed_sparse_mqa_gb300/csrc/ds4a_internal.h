@@ -23,6 +23,13 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
                            int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
                            int32_t *out_n, void *ws, const Ctx &c);
 
+// one decode query's indexer and the one-token compressor update of the same step,
+// in one launch (the compressor's arguments as launch_compress with n_new = 1, pos = q_pos)
+cudaError_t launch_indexer_compress(const uint16_t *q_idx, const uint16_t *k_idx, long long n_rows, int d_idx,
+                                   long long q_pos, int ratio, int k, int32_t *out_idx, int32_t *out_n, void *ws,
+                                   const uint16_t *k_new, const uint16_t *v_new, int D, const float *score_w,
+                                   float *state, uint16_t *comp_k, uint16_t *comp_v, const Ctx &c);
+
 // tensor-core prefill indexer (many queries): availability, workspace, launch
 bool indexer_prefill_tc_ok(int n_q, long long n_rows, int d_idx);
 size_t indexer_prefill_tc_ws_bytes(int n_q, long long n_rows);

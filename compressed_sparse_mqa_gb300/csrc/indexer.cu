@@ -24,6 +24,7 @@
 // waiting) selects and resets the ticket.  Many queries: the tensor-core path
 // (indexer_tc.cu) when the shapes allow it, else one CTA per query scores its
 // visible rows into shared memory and selects.
+#include "compress_dev.cuh"
 #include "ds4a_common.cuh"
 #include "ds4a_internal.h"
 #include "select.cuh"
@@ -289,12 +290,38 @@ DS4A_DEVINL long long visible_rows(const IndexerArgs &a, int i) {
     return v < a.n_rows ? v : a.n_rows;
 }
 
-// one query: CTA b scores rows [b*rows_per_cta, (b+1)*rows_per_cta) in 64-row
-// slices; the last CTA to finish selects
-__global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs a, int rows_per_cta) {
+// The compressor's update for the one new token of a decode step (n_new = 1): its
+// score reads only the caller's inputs and is taken before the wait; the running
+// state and the pooled row of a completed block are written after it.
+DS4A_DEVINL void compress_one_token(const cmp::CompressArgs &c, float *s_w, float *s_red) {
+    const long long b = c.pos / c.ratio;
+    const bool resume = c.pos % c.ratio != 0;   // the token continues an open block
+    cmp::segment_scores<kThreads>(c, c.pos, c.pos + 1, s_w);
+    pdl_wait();
+    pdl_trigger();
+    cmp::pool_segment<kThreads>(c, b, c.pos, c.pos + 1, resume, s_w, s_red);
+}
+
+// one query: CTA b < n_score scores rows [b*rows_per_cta, (b+1)*rows_per_cta) in
+// 64-row slices; the last of them to finish selects.  With kCompress the grid has
+// one more CTA, which feeds the query's token to the layer's compressor: that
+// update reads nothing the selection writes and vice versa.
+template <bool kCompress>
+__global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs a, int rows_per_cta,
+                                                                     cmp::CompressArgs c) {
     __shared__ SelectSmem sm;
     __shared__ bool s_last;
     __shared__ uint32_t s_keys[kStagedRows];
+    if constexpr (kCompress) {
+        if (blockIdx.x == gridDim.x - 1) {
+            static_assert(sizeof(sm.scan) >= kWarps * sizeof(float), "one float per warp");
+            compress_one_token(c, reinterpret_cast<float *>(s_keys), reinterpret_cast<float *>(sm.scan));
+            return;
+        }
+    } else {
+        (void)c;
+    }
+    const unsigned int n_score = kCompress ? gridDim.x - 1 : gridDim.x;
     const long long n_vis = visible_rows(a, 0);
     const long long j0 = static_cast<long long>(blockIdx.x) * rows_per_cta;
     const long long j1 = min(n_vis, j0 + rows_per_cta);
@@ -327,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     if (threadIdx.x == 0) {
         unsigned int old;
         asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;\n" : "=r"(old) : "l"(ticket) : "memory");
-        s_last = old == gridDim.x - 1;
+        s_last = old == n_score - 1;
     }
     __syncthreads();
     if (!s_last) return;
@@ -378,10 +405,59 @@ size_t indexer_ws_bytes(int n_q, long long n_rows, int k) {
     return bytes;
 }
 
+// One decode query: 64-row slices spread so that the scoring grid is at most one
+// CTA on each of `sms` SMs.
+static unsigned decode_grid(long long q_pos, long long n_rows, int ratio, int sms, int &rows_per_cta) {
+    long long n_vis = (q_pos + 1) / ratio;
+    if (n_vis > n_rows) n_vis = n_rows;
+    const long long slices = (n_vis + kRowsPerCta - 1) / kRowsPerCta;
+    const long long per_cta = slices > sms ? (slices + sms - 1) / sms : 1;
+    rows_per_cta = static_cast<int>(per_cta * kRowsPerCta);
+    long long grid = (n_vis + rows_per_cta - 1) / rows_per_cta;
+    return static_cast<unsigned>(grid < 1 ? 1 : grid);
+}
+
+static cudaError_t configure_indexer(const Ctx &c);
+
 cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
                            int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
                            int32_t *out_n, void *ws, const Ctx &c) {
     if (d_idx > kMaxDIdx || n_rows > 0x7fffffffLL) return cudaErrorInvalidValue;
+    cudaError_t e = configure_indexer(c);
+    if (e != cudaSuccess) return e;
+    IndexerArgs a{q_idx, k_idx, out_idx, out_n, static_cast<unsigned char *>(ws), n_rows, q_pos0,
+                  n_q, d_idx, ratio, k};
+    if (n_q == 1) {
+        int rows_per_cta = 0;
+        const unsigned grid = decode_grid(q_pos0, n_rows, ratio, c.num_sms, rows_per_cta);
+        return launch(indexer_decode_kernel<false>, dim3(grid), dim3(kThreads), 0, c, 1, a, rows_per_cta,
+                      cmp::CompressArgs{});
+    }
+    if (indexer_prefill_tc_ok(n_q, n_rows, d_idx))
+        return launch_indexer_prefill_tc(q_idx, n_q, k_idx, n_rows, d_idx, q_pos0, ratio, k, out_idx, out_n, ws, c);
+    return launch(indexer_query_kernel, dim3(static_cast<unsigned>(n_q)), dim3(kThreads), kQuerySmem, c, 1, a);
+}
+
+cudaError_t launch_indexer_compress(const uint16_t *q_idx, const uint16_t *k_idx, long long n_rows, int d_idx,
+                                   long long q_pos, int ratio, int k, int32_t *out_idx, int32_t *out_n, void *ws,
+                                   const uint16_t *k_new, const uint16_t *v_new, int D, const float *score_w,
+                                   float *state, uint16_t *comp_k, uint16_t *comp_v, const Ctx &c) {
+    if (d_idx > kMaxDIdx || n_rows > 0x7fffffffLL || ratio > cmp::kMaxRatio || D > cmp::kMaxD)
+        return cudaErrorInvalidValue;
+    cudaError_t e = configure_indexer(c);
+    if (e != cudaSuccess) return e;
+    IndexerArgs a{q_idx, k_idx, out_idx, out_n, static_cast<unsigned char *>(ws), n_rows, q_pos,
+                  1, d_idx, ratio, k};
+    const cmp::CompressArgs ca{k_new, v_new, score_w, state, comp_k, comp_v, q_pos, 1, D, ratio};
+    int rows_per_cta = 0;
+    // the scoring CTAs leave one SM for the compressor's CTA
+    const unsigned grid = decode_grid(q_pos, n_rows, ratio, c.num_sms > 1 ? c.num_sms - 1 : 1, rows_per_cta);
+    return launch(indexer_decode_kernel<true>, dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca);
+}
+
+// kernel attributes, once per device and host thread
+static cudaError_t configure_indexer(const Ctx &c) {
+    (void)c;
     static thread_local int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -389,7 +465,10 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
         cudaError_t e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kQuerySmem));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(indexer_decode_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(indexer_decode_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -397,23 +476,7 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    IndexerArgs a{q_idx, k_idx, out_idx, out_n, static_cast<unsigned char *>(ws), n_rows, q_pos0,
-                  n_q, d_idx, ratio, k};
-    if (n_q == 1) {
-        long long n_vis = (q_pos0 + 1) / ratio;
-        if (n_vis > n_rows) n_vis = n_rows;
-        // 64-row slices, spread so that the grid is at most one CTA per SM
-        const long long slices = (n_vis + kRowsPerCta - 1) / kRowsPerCta;
-        const long long per_cta = slices > c.num_sms ? (slices + c.num_sms - 1) / c.num_sms : 1;
-        const int rows_per_cta = static_cast<int>(per_cta * kRowsPerCta);
-        long long grid = (n_vis + rows_per_cta - 1) / rows_per_cta;
-        if (grid < 1) grid = 1;
-        return launch(indexer_decode_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, c, 1, a,
-                      rows_per_cta);
-    }
-    if (indexer_prefill_tc_ok(n_q, n_rows, d_idx))
-        return launch_indexer_prefill_tc(q_idx, n_q, k_idx, n_rows, d_idx, q_pos0, ratio, k, out_idx, out_n, ws, c);
-    return launch(indexer_query_kernel, dim3(static_cast<unsigned>(n_q)), dim3(kThreads), kQuerySmem, c, 1, a);
+    return cudaSuccess;
 }
 
 }  // namespace ds4a

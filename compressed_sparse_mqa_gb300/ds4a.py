@@ -28,7 +28,7 @@ DS4A_ERR_DEVICE_INDEX = 7
 
 EXPORTED = ["ds4a_status_str", "ds4a_last_device_error", "ds4a_compress_append",
             "ds4a_indexer_topk", "ds4a_indexer_workspace_bytes", "ds4a_attn_decode",
-            "ds4a_attn_prefill"]
+            "ds4a_attn_prefill", "ds4a_indexer_topk_compress"]
 
 
 class Ds4aError(RuntimeError):
@@ -49,6 +49,7 @@ def lib() -> ctypes.CDLL:
         L.ds4a_last_device_error.argtypes = [P]
         L.ds4a_compress_append.argtypes = [P, P, I, I, P, I, LL, P, P, P, LL, P]
         L.ds4a_indexer_topk.argtypes = [P, I, P, LL, I, LL, I, I, P, P, P, SZ, P]
+        L.ds4a_indexer_topk_compress.argtypes = [P, P, LL, I, LL, I, I, P, P, P, SZ, P, P, I, P, P, P, P, LL, P]
         L.ds4a_indexer_workspace_bytes.argtypes = [I, LL, I]
         L.ds4a_indexer_workspace_bytes.restype = SZ
         L.ds4a_attn_decode.argtypes = [P, I, I, P, P, I, P, P, LL, P, I, F, P, P, SZ, P]
@@ -132,6 +133,35 @@ def ds4a_indexer_topk(q_idx, k_idx, q_pos0: int, ratio: int, k: int, out_idx, ou
                                  _ptr(out_n, torch.int32, "out_n", optional=True),
                                  _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
     _check(rc, "ds4a_indexer_topk")
+
+
+def ds4a_indexer_topk_compress(q_idx, k_idx, q_pos: int, ratio: int, k: int, out_idx, out_n, ws, k_new, v_new,
+                               score_w, state, comp_k, comp_v, n_rows=None, stream=None):
+    """ds4a_indexer_topk for one query at q_pos (q_idx [d] or [1, d]) and
+    ds4a_compress_append of that position's token (k_new, v_new [1, D] fp16), in one
+    launch; arguments as the two calls."""
+    q2 = q_idx if q_idx.dim() == 2 else q_idx.view(1, -1)
+    if q2.shape[0] != 1:
+        raise ValueError("indexer_topk_compress: one query")
+    d = q2.shape[1]
+    rows = k_idx.shape[0] if n_rows is None else n_rows
+    if k_idx.shape[0] < rows or (k_idx.numel() and k_idx.shape[1] != d):
+        raise ValueError("indexer_topk_compress: k_idx shape")
+    if out_idx.numel() < k:
+        raise ValueError("indexer_topk_compress: out_idx too small")
+    n_new, D = k_new.shape
+    if n_new != 1 or v_new.shape != k_new.shape or comp_k.shape != comp_v.shape or comp_k.shape[1] != D:
+        raise ValueError("indexer_topk_compress: token / compressed-row shapes")
+    if state.numel() < 2 + 2 * D or score_w.numel() != D:
+        raise ValueError("indexer_topk_compress: state / score_w size")
+    rc = lib().ds4a_indexer_topk_compress(
+        _ptr(q2, torch.float16, "q_idx"), _ptr(k_idx, torch.float16, "k_idx") if k_idx.numel() else None, rows, d,
+        q_pos, ratio, k, _ptr(out_idx, torch.int32, "out_idx"), _ptr(out_n, torch.int32, "out_n", optional=True),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _ptr(k_new, torch.float16, "k_new"),
+        _ptr(v_new, torch.float16, "v_new"), D, _ptr(score_w, torch.float32, "score_w"),
+        _ptr(state, torch.float32, "state"), _ptr(comp_k, torch.float16, "comp_k"),
+        _ptr(comp_v, torch.float16, "comp_v"), comp_k.shape[0], _stream(stream))
+    _check(rc, "ds4a_indexer_topk_compress")
 
 
 def ds4a_attn_decode(q, win_k, win_v, comp_k, comp_v, sel, n_sel: int, scale: float, out, stream=None):

@@ -8,9 +8,10 @@ ratio 128 and attend every compressed row.
 The KV state of one layer lives on the device, owned here (allocated through
 torch): the raw window ring [W, D] (token p sits in slot p % W), the compressed
 rows [cap, D], one indexer key per compressed row, and the compressor's running
-state.  A decode step is three library calls on the current stream:
-indexer_topk (ratio-4 layers) -> compress_append (the new token, read from its
-ring slot) -> attn_decode over the ring and the kept rows.
+state.  A decode step is, on the current stream: indexer_topk (ratio-4 layers)
+and compress_append of the new token (read from its ring slot) -- on ratio-4
+layers both in one launch, ds4a_indexer_topk_compress -- then attn_decode over
+the ring and the kept rows.
 """
 from __future__ import annotations
 
@@ -124,14 +125,18 @@ class DecodeLayer:
     def step(self, stream=None):
         """One decode step at position p (all inputs already resident).
 
-        The indexer runs first: it reads only the indexer keys (caller-supplied for
-        every visible row), not the compressor's output, so under programmatic
-        dependent launch its key-row loads overlap the previous layer's attention.
+        The indexer reads only the indexer keys (caller-supplied for every visible
+        row), not the compressor's output, and the compressor reads only the new
+        token: on ratio-4 layers one launch runs both, so the step is two dependent
+        kernels.  Under programmatic dependent launch the indexer's key-row loads
+        overlap the previous layer's attention.
         """
         if self.topk:
-            ds4a.ds4a_indexer_topk(self.q_idx, self.kidx, self.p, self.ratio, self.topk, self.sel, self.sel_n,
-                                   self.ws, stream=stream)
-        if self.ratio:
+            ds4a.ds4a_indexer_topk_compress(self.q_idx, self.kidx, self.p, self.ratio, self.topk, self.sel,
+                                            self.sel_n, self.ws, self.ring_k[self.slot: self.slot + 1],
+                                            self.ring_v[self.slot: self.slot + 1], self.w, self.state, self.comp_k,
+                                            self.comp_v, stream=stream)
+        elif self.ratio:
             ds4a.ds4a_compress_append(self.ring_k[self.slot: self.slot + 1], self.ring_v[self.slot: self.slot + 1],
                                       self.w, self.ratio, self.p, self.state, self.comp_k, self.comp_v,
                                       stream=stream)

@@ -118,6 +118,31 @@ int ds4a_indexer_topk(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, lon
 size_t ds4a_indexer_workspace_bytes(int n_q, long long n_rows, int k);
 
 /*
+ * ds4a_indexer_topk_compress -- one decode step's indexer query and the
+ * compressor update for the step's token, in a single kernel launch.
+ * ("DS4 (DwarfStar 4)", Key Techniques, "KV attention compression": both are
+ * per-token steps of a ratio-4 layer; the indexer reads the caller's indexer
+ * keys, the compressor reads the new token, and neither reads what the other
+ * writes.)
+ *
+ * Same results as ds4a_indexer_topk(q_idx, 1, k_idx, n_rows, d_idx, q_pos,
+ * ratio, k, out_idx, out_n, ws, ws_bytes, stream) followed by
+ * ds4a_compress_append(k_new, v_new, 1, head_dim, score_w, ratio, q_pos, state,
+ * comp_k, comp_v, cap, stream): the same kernels' arithmetic, bit for bit.  One
+ * launch instead of two takes a kernel boundary off a decode step's chain.
+ *
+ *   Indexer arguments as ds4a_indexer_topk with n_q = 1 and q_pos0 = q_pos.
+ *   Compressor arguments as ds4a_compress_append with n_new = 1 and pos = q_pos
+ *   (k_new, v_new: [1, head_dim] fp16, the token at position q_pos).
+ *   Errors: the union of the two calls' checks; nothing is enqueued on error.
+ */
+int ds4a_indexer_topk_compress(const uint16_t *q_idx, const uint16_t *k_idx, long long n_rows, int d_idx,
+                               long long q_pos, int ratio, int k, int32_t *out_idx, int32_t *out_n, void *ws,
+                               size_t ws_bytes, const uint16_t *k_new, const uint16_t *v_new, int head_dim,
+                               const float *score_w, float *state, uint16_t *comp_k, uint16_t *comp_v,
+                               long long cap, void *stream);
+
+/*
  * ds4a_indexer_topk_noalloc -- ds4a_indexer_topk for one query (n_q = 1) with no
  * workspace argument and no allocation.  The pages have no counterpart: this is
  * a convenience of this library.

@@ -78,6 +78,33 @@ def test_indexer_validation(ds4a_lib):
     assert f(None, 0, None, 0, 128, 0, 4, 512, None, None, None, 0, None) == 0            # n_q = 0
 
 
+def test_indexer_topk_compress_validation(ds4a_lib):
+    L = ds4a_lib.lib()
+    f = L.ds4a_indexer_topk_compress
+    nb = L.ds4a_indexer_workspace_bytes(1, 8192, 512)
+
+    def call(**kw):
+        a = dict(q=FAKE, kidx=FAKE, n_rows=8192, d_idx=128, q_pos=32768, ratio=4, k=512, out=FAKE, out_n=FAKE,
+                 ws=FAKE, nb=nb, k_new=FAKE, v_new=FAKE, head_dim=128, w=FAKE, state=FAKE, ck=FAKE, cv=FAKE,
+                 cap=9000)
+        a.update(kw)
+        return f(a["q"], a["kidx"], a["n_rows"], a["d_idx"], a["q_pos"], a["ratio"], a["k"], a["out"], a["out_n"],
+                 a["ws"], a["nb"], a["k_new"], a["v_new"], a["head_dim"], a["w"], a["state"], a["ck"], a["cv"],
+                 a["cap"], None)
+    assert call(k=0) == ARG
+    assert call(ratio=0) == ARG
+    assert call(d_idx=100) == UNSUP
+    assert call(head_dim=100) == UNSUP
+    assert call(ratio=2048) == UNSUP
+    assert call(k_new=None) == ARG
+    assert call(state=None) == ARG
+    assert call(k_new=FAKE + 8) == ARG          # the token rows must be 16-byte aligned
+    assert call(q=FAKE + 4) == ARG
+    assert call(ws=None) == WS
+    assert call(nb=nb - 1) == WS
+    assert call(q_pos=32771, cap=8192) == CAP   # position 32771 completes row 8192 (rows 0 .. 8191 fit)
+
+
 def test_attn_decode_validation(ds4a_lib):
     L = ds4a_lib.lib()
     f = L.ds4a_attn_decode

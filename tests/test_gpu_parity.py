@@ -255,6 +255,45 @@ def test_indexer_repeated_calls_reuse_workspace():
     assert np.array_equal(h(L.sel), first)
 
 
+@pytest.mark.parametrize("p", [1, 3, 202, 203, 8191])
+def test_indexer_topk_compress_matches_the_two_calls(p):
+    """The one-launch indexer query + compressor update for position p gives the same
+    bits as ds4a_indexer_topk followed by ds4a_compress_append: kept rows, count,
+    running state and pooled rows (p = 3, 203, 8191 complete a block; p = 1 sees no row)."""
+    ratio, topk, d_idx, D, seed = 4, 64, 64, 128, 11
+    n_rows = (p + 1) // ratio
+    kidx = torch.from_numpy(synth.normal_f16(seed, 3, synth.T_KIDX, (max(n_rows, 1), d_idx))).cuda()[:n_rows]
+    q_idx = torch.from_numpy(synth.normal_f16(seed, 3, synth.T_QIDX, (d_idx,))).cuda()
+    tok_k = torch.from_numpy(synth.normal_f16(seed, 3, synth.T_KRAW, (p + 1, D))).cuda()
+    tok_v = torch.from_numpy(synth.normal_f16(seed, 3, synth.T_VRAW, (p + 1, D))).cuda()
+    w = torch.from_numpy(synth.normal_f32(seed, 3, synth.T_W, (D,), 1.0 / np.sqrt(D))).cuda()
+    comp_k = torch.zeros(n_rows + 1, D, dtype=torch.float16, device="cuda")
+    comp_v = torch.zeros_like(comp_k)
+    state = torch.zeros(2 + 2 * D, dtype=torch.float32, device="cuda")
+    if p:
+        ds4a.ds4a_compress_append(tok_k[:p], tok_v[:p], w, ratio, 0, state, comp_k, comp_v)
+    nb = ds4a.ds4a_indexer_workspace_bytes(1, n_rows, topk)
+    outs = []
+    for fused in (False, True):
+        ck, cv, st = comp_k.clone(), comp_v.clone(), state.clone()
+        sel = torch.full((topk,), 7, dtype=torch.int32, device="cuda")
+        sel_n = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+        ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+        if fused:
+            ds4a.ds4a_indexer_topk_compress(q_idx, kidx, p, ratio, topk, sel, sel_n, ws, tok_k[p:p + 1],
+                                            tok_v[p:p + 1], w, st, ck, cv)
+        else:
+            ds4a.ds4a_indexer_topk(q_idx, kidx, p, ratio, topk, sel, sel_n, ws)
+            ds4a.ds4a_compress_append(tok_k[p:p + 1], tok_v[p:p + 1], w, ratio, p, st, ck, cv)
+        torch.cuda.synchronize()
+        outs.append([h(x) for x in (sel, sel_n, st, ck, cv, ws)])
+    for name, a, b in zip(["sel", "sel_n", "state", "comp_k", "comp_v", "workspace"], *outs):
+        assert np.array_equal(a, b), name
+    assert int(outs[1][1][0]) == min(topk, n_rows)
+    assert not outs[1][5][:256].any()   # the ticket is back at zero for the next call
+    assert ds4a.ds4a_last_device_error() == 0
+
+
 # ---- compressor: chunk-split invariance and online == blockwise ----------------------------------
 
 @pytest.mark.parametrize("ratio", [4, 128])
