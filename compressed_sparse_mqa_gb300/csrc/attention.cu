@@ -32,6 +32,7 @@
 // tensor-core kernel in attention_tc.cu does not take).
 #include <cooperative_groups.h>
 
+#include "compress_dev.cuh"
 #include "ds4a_common.cuh"
 #include "ds4a_internal.h"
 
@@ -511,6 +512,8 @@ struct DecodeArgs {
     int H;
     int n_rows;        // n_win + n_sel
     float scale_log2;
+    int comp_rank;     // with the compressor: the CTA that runs its update (it attends the row it may write)
+    int comp_first;    // the update completes a block: its row is written before that CTA attends
 };
 
 constexpr int kRecvRows = 80;   // >= cluster size * ceil(H / cluster size) for H <= 64
@@ -525,8 +528,15 @@ static_assert(4 * 32 * (128 / 2 + 4) * sizeof(float) <= sizeof(Smem<128>), "exch
 static_assert(64 * (128 + 4) * sizeof(float) <= sizeof(Smem<128>) && 64 * (64 + 4) * sizeof(float) <= sizeof(Smem<64>),
               "the send rows of 64 heads fit in the tiles");
 
-template <int D>
-__global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
+// kCompress: one CTA (a.comp_rank) also runs the compressor's update for the step's
+// token (n_new = 1, arguments ca): its score before the dependency wait; the
+// running state and, when the token completes a block, the pooled row after it.
+// A completed row is the last row this call attends and a.comp_rank is the CTA
+// that attends it, so that CTA writes the row before it attends its rows; other
+// steps update the state after the partials are sent.  No other CTA reads what
+// the compressor writes.
+template <int D, bool kCompress>
+__global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a, cmp::CompressArgs ca) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
     float *recv = reinterpret_cast<float *>(smem_raw + recv_offset<D>());
@@ -556,8 +566,12 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
     const int chunk = (a.n_rows + cs - 1) / cs;
     const int v0 = min(a.n_rows, rank * chunk);
     const int v1 = min(a.n_rows, v0 + chunk);
+    const bool comp_here = kCompress && rank == a.comp_rank;
+    __shared__ float s_cw[1], s_cred[kThreads / 32];   // compressor: the token's score, per-warp maxima
+    if (comp_here) cmp::segment_scores<kThreads>(ca, ca.pos, ca.pos + 1, s_cw);
     // a first tile of window rows only (cache state) is gathered before the dependency wait
-    const bool pre = v1 > v0 && min(v1, v0 + kBN) <= a.src.n_w;
+    // (not by a CTA that writes a compressed row before it attends)
+    const bool pre = v1 > v0 && min(v1, v0 + kBN) <= a.src.n_w && !(comp_here && a.comp_first);
     if (pre) {
         build_table<D>(a.src, v0, v1, sm.off[0], &sm.nvalid[0]);
         __syncthreads();
@@ -569,6 +583,11 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
     load_q_frags<D>(a.q, a.H, h0, qa);
     pdl_wait();
     pdl_trigger();
+    if (comp_here && a.comp_first) {
+        cmp::pool_segment<kThreads>(ca, ca.pos / ca.ratio, ca.pos, ca.pos + 1, ca.pos % ca.ratio != 0, s_cw, s_cred);
+        __threadfence();   // the row is in memory before this CTA's own row loads read it
+        __syncthreads();
+    }
     WarpStateH<D> st;
 #pragma unroll
     for (int dn = 0; dn < D / 16; ++dn)
@@ -615,6 +634,8 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a) {
         }
         asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
     }
+    if (comp_here && !a.comp_first)   // off the critical path: while the partials travel
+        cmp::pool_segment<kThreads>(ca, ca.pos / ca.ratio, ca.pos, ca.pos + 1, ca.pos % ca.ratio != 0, s_cw, s_cred);
     // every byte destined for this CTA has landed
     if (!recv_wait(&s_recv_bar)) record_error(a.src.err, DS4A_ERR_TIMEOUT);
 
@@ -729,16 +750,19 @@ cudaError_t configure(int &cluster) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(decode_smem<D>()));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_decode_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        cudaError_t e = cudaSuccess;
+        for (auto kern : {attn_decode_kernel<D, false>, attn_decode_kernel<D, true>}) {
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(decode_smem<D>()));
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+        }
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(prefill_smem<D>()));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_decode_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
@@ -757,7 +781,7 @@ cudaError_t configure(int &cluster) {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         int n_clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&n_clusters, attn_decode_kernel<D>, &cfg) == cudaSuccess &&
+        if (cudaOccupancyMaxActiveClusters(&n_clusters, attn_decode_kernel<D, false>, &cfg) == cudaSuccess &&
             n_clusters > 0)
             cluster_size = 16;
         cudaGetLastError();
@@ -780,14 +804,45 @@ cudaError_t launch_attn_decode(const uint16_t *q, int H, int D, const uint16_t *
     a.H = H;
     a.n_rows = n_win + n_sel;
     a.scale_log2 = scale * kLog2e;
+    a.comp_rank = -1;
+    a.comp_first = 0;
     int cluster = 16;
     cudaError_t e;
     if (D == 128) {
         if ((e = configure<128>(cluster)) != cudaSuccess) return e;
-        return launch(attn_decode_kernel<128>, dim3(cluster), dim3(kThreads), decode_smem<128>(), c, cluster, a);
+        return launch(attn_decode_kernel<128, false>, dim3(cluster), dim3(kThreads), decode_smem<128>(), c, cluster, a,
+                      cmp::CompressArgs{});
     }
     if ((e = configure<64>(cluster)) != cudaSuccess) return e;
-    return launch(attn_decode_kernel<64>, dim3(cluster), dim3(kThreads), decode_smem<64>(), c, cluster, a);
+    return launch(attn_decode_kernel<64, false>, dim3(cluster), dim3(kThreads), decode_smem<64>(), c, cluster, a,
+                  cmp::CompressArgs{});
+}
+
+cudaError_t launch_compress_attn_decode(const uint16_t *k_new, const uint16_t *v_new, const float *score_w, int ratio,
+                                        long long pos, float *state, const uint16_t *q, int H, int D,
+                                        const uint16_t *win_k, const uint16_t *win_v, int n_win, uint16_t *comp_k,
+                                        uint16_t *comp_v, float scale, uint16_t *out, const Ctx &c) {
+    if (ratio > cmp::kMaxRatio || D > cmp::kMaxD) return cudaErrorInvalidValue;
+    const long long n_vis = (pos + 1) / ratio;   // every visible row, the one this step may complete included
+    DecodeArgs a;
+    a.q = q;
+    a.out = out;
+    a.src = RowSrc{win_k, win_v, comp_k, comp_v, nullptr, c.err, n_vis, n_win};
+    a.H = H;
+    a.n_rows = n_win + static_cast<int>(n_vis);
+    a.scale_log2 = scale * kLog2e;
+    a.comp_first = (pos + 1) % ratio == 0;
+    const cmp::CompressArgs ca{k_new, v_new, score_w, state, comp_k, comp_v, pos, 1, D, ratio};
+    int cluster = 16;
+    cudaError_t e = D == 128 ? configure<128>(cluster) : configure<64>(cluster);
+    if (e != cudaSuccess) return e;
+    // the CTA that attends the last row (the row a completing step writes), as the kernel splits the rows
+    const int chunk = (a.n_rows + cluster - 1) / cluster;
+    a.comp_rank = (a.n_rows - 1) / chunk;
+    if (D == 128)
+        return launch(attn_decode_kernel<128, true>, dim3(cluster), dim3(kThreads), decode_smem<128>(), c, cluster, a,
+                      ca);
+    return launch(attn_decode_kernel<64, true>, dim3(cluster), dim3(kThreads), decode_smem<64>(), c, cluster, a, ca);
 }
 
 cudaError_t launch_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *raw_k,

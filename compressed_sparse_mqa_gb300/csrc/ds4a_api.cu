@@ -189,6 +189,32 @@ int ds4a_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
                                               n_sel, scale, out, c));
 }
 
+int ds4a_compress_attn_decode(const uint16_t *k_new, const uint16_t *v_new, const float *score_w, int ratio,
+                              long long pos, float *state, uint16_t *comp_k, uint16_t *comp_v, long long cap,
+                              const uint16_t *q, int H, int D, const uint16_t *win_k, const uint16_t *win_v,
+                              int n_win, float scale, uint16_t *out, void *stream) {
+    // the checks of ds4a_compress_append (n_new = 1, head_dim = D) and of ds4a_attn_decode
+    // (sel = NULL, n_sel = floor((pos+1)/ratio), n_comp = cap)
+    if (pos < 0 || cap < 0 || ratio < 1) return DS4A_ERR_ARG;
+    int rc = check_heads(H, D);
+    if (rc != DS4A_OK) return rc;
+    if (ratio > 1024) return DS4A_ERR_UNSUPPORTED;
+    if (n_win < 1 || n_win > 4096) return DS4A_ERR_ARG;
+    if (!k_new || !v_new || !score_w || !state || !comp_k || !comp_v || !q || !win_k || !win_v || !out)
+        return DS4A_ERR_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(score_w, 4) || !aligned(state, 4) ||
+        !aligned(comp_k, 16) || !aligned(comp_v, 16) || !aligned(q, 4) || !aligned(win_k, 16) ||
+        !aligned(win_v, 16) || !aligned(out, 16))
+        return DS4A_ERR_ARG;
+    if ((pos + 1) / ratio > cap) return DS4A_ERR_CAPACITY;
+    if (n_win + (pos + 1) / ratio > 0x7fffffffLL) return DS4A_ERR_UNSUPPORTED;
+    ds4a::Ctx c;
+    rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    return from_cuda(ds4a::launch_compress_attn_decode(k_new, v_new, score_w, ratio, pos, state, q, H, D, win_k,
+                                                       win_v, n_win, comp_k, comp_v, scale, out, c));
+}
+
 int ds4a_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *raw_k,
                       const uint16_t *raw_v, int n_prior, int window, const uint16_t *comp_k,
                       const uint16_t *comp_v, long long n_comp, const int32_t *sel, int k_stride,

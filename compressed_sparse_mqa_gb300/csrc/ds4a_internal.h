@@ -42,6 +42,13 @@ cudaError_t launch_attn_decode(const uint16_t *q, int H, int D, const uint16_t *
                                const uint16_t *comp_v, long long n_comp, const int32_t *sel,
                                int n_sel, float scale, uint16_t *out, const Ctx &c);
 
+// the compressor's update for one decode token (as launch_compress with n_new = 1) and attention over the
+// window and every visible compressed row floor((pos+1)/ratio), in one launch
+cudaError_t launch_compress_attn_decode(const uint16_t *k_new, const uint16_t *v_new, const float *score_w, int ratio,
+                                        long long pos, float *state, const uint16_t *q, int H, int D,
+                                        const uint16_t *win_k, const uint16_t *win_v, int n_win, uint16_t *comp_k,
+                                        uint16_t *comp_v, float scale, uint16_t *out, const Ctx &c);
+
 // tensor-core prefill attention (64 heads, head_dim 128, <= 768 keys per query)
 // the tensor-core prefill path takes H = 64, D = 128, 16-byte aligned queries and outputs, and
 // key lists of at most 6 tiles of 128 (window tiles + selected-row tiles)

@@ -28,7 +28,7 @@ DS4A_ERR_DEVICE_INDEX = 7
 
 EXPORTED = ["ds4a_status_str", "ds4a_last_device_error", "ds4a_compress_append",
             "ds4a_indexer_topk", "ds4a_indexer_workspace_bytes", "ds4a_attn_decode",
-            "ds4a_attn_prefill", "ds4a_indexer_topk_compress"]
+            "ds4a_attn_prefill", "ds4a_indexer_topk_compress", "ds4a_compress_attn_decode"]
 
 
 class Ds4aError(RuntimeError):
@@ -50,6 +50,7 @@ def lib() -> ctypes.CDLL:
         L.ds4a_compress_append.argtypes = [P, P, I, I, P, I, LL, P, P, P, LL, P]
         L.ds4a_indexer_topk.argtypes = [P, I, P, LL, I, LL, I, I, P, P, P, SZ, P]
         L.ds4a_indexer_topk_compress.argtypes = [P, P, LL, I, LL, I, I, P, P, P, SZ, P, P, I, P, P, P, P, LL, P]
+        L.ds4a_compress_attn_decode.argtypes = [P, P, P, I, LL, P, P, P, LL, P, I, I, P, P, I, F, P, P]
         L.ds4a_indexer_workspace_bytes.argtypes = [I, LL, I]
         L.ds4a_indexer_workspace_bytes.restype = SZ
         L.ds4a_attn_decode.argtypes = [P, I, I, P, P, I, P, P, LL, P, I, F, P, P, SZ, P]
@@ -162,6 +163,27 @@ def ds4a_indexer_topk_compress(q_idx, k_idx, q_pos: int, ratio: int, k: int, out
         _ptr(state, torch.float32, "state"), _ptr(comp_k, torch.float16, "comp_k"),
         _ptr(comp_v, torch.float16, "comp_v"), comp_k.shape[0], _stream(stream))
     _check(rc, "ds4a_indexer_topk_compress")
+
+
+def ds4a_compress_attn_decode(k_new, v_new, score_w, ratio: int, pos: int, state, comp_k, comp_v, q, win_k, win_v,
+                              scale: float, out, stream=None):
+    """ds4a_compress_append of the token at pos (k_new, v_new [1, D] fp16) and
+    ds4a_attn_decode over the window and every visible compressed row, in one launch;
+    arguments as the two calls."""
+    H, D = q.shape
+    if k_new.shape != (1, D) or v_new.shape != (1, D) or comp_k.shape != comp_v.shape or comp_k.shape[1] != D:
+        raise ValueError("compress_attn_decode: token / compressed-row shapes")
+    if win_k.shape != win_v.shape or win_k.shape[1] != D or out.shape != q.shape:
+        raise ValueError("compress_attn_decode: window / output shapes")
+    if state.numel() < 2 + 2 * D or score_w.numel() != D:
+        raise ValueError("compress_attn_decode: state / score_w size")
+    rc = lib().ds4a_compress_attn_decode(
+        _ptr(k_new, torch.float16, "k_new"), _ptr(v_new, torch.float16, "v_new"),
+        _ptr(score_w, torch.float32, "score_w"), ratio, pos, _ptr(state, torch.float32, "state"),
+        _ptr(comp_k, torch.float16, "comp_k"), _ptr(comp_v, torch.float16, "comp_v"), comp_k.shape[0],
+        _ptr(q, torch.float16, "q"), H, D, _ptr(win_k, torch.float16, "win_k"), _ptr(win_v, torch.float16, "win_v"),
+        win_k.shape[0], scale, _ptr(out, torch.float16, "out"), _stream(stream))
+    _check(rc, "ds4a_compress_attn_decode")
 
 
 def ds4a_attn_decode(q, win_k, win_v, comp_k, comp_v, sel, n_sel: int, scale: float, out, stream=None):

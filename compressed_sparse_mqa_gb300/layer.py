@@ -8,10 +8,11 @@ ratio 128 and attend every compressed row.
 The KV state of one layer lives on the device, owned here (allocated through
 torch): the raw window ring [W, D] (token p sits in slot p % W), the compressed
 rows [cap, D], one indexer key per compressed row, and the compressor's running
-state.  A decode step is, on the current stream: indexer_topk (ratio-4 layers)
-and compress_append of the new token (read from its ring slot) -- on ratio-4
-layers both in one launch, ds4a_indexer_topk_compress -- then attn_decode over
-the ring and the kept rows.
+state.  A decode step is, on the current stream: indexer_topk (ratio-4 layers),
+compress_append of the new token (read from its ring slot) and attn_decode over
+the ring and the kept rows.  Ratio-4 layers run the first two in one launch
+(ds4a_indexer_topk_compress), ratio-128 layers the last two
+(ds4a_compress_attn_decode), so every step is at most two dependent kernels.
 """
 from __future__ import annotations
 
@@ -127,19 +128,22 @@ class DecodeLayer:
 
         The indexer reads only the indexer keys (caller-supplied for every visible
         row), not the compressor's output, and the compressor reads only the new
-        token: on ratio-4 layers one launch runs both, so the step is two dependent
-        kernels.  Under programmatic dependent launch the indexer's key-row loads
+        token: on ratio-4 layers one launch runs both.  A ratio-128 layer attends
+        every row, and the compressor's update runs inside the attention launch.
+        Under programmatic dependent launch the first kernel's input-only loads
         overlap the previous layer's attention.
         """
+        new_k = self.ring_k[self.slot: self.slot + 1]
+        new_v = self.ring_v[self.slot: self.slot + 1]
         if self.topk:
             ds4a.ds4a_indexer_topk_compress(self.q_idx, self.kidx, self.p, self.ratio, self.topk, self.sel,
-                                            self.sel_n, self.ws, self.ring_k[self.slot: self.slot + 1],
-                                            self.ring_v[self.slot: self.slot + 1], self.w, self.state, self.comp_k,
+                                            self.sel_n, self.ws, new_k, new_v, self.w, self.state, self.comp_k,
                                             self.comp_v, stream=stream)
         elif self.ratio:
-            ds4a.ds4a_compress_append(self.ring_k[self.slot: self.slot + 1], self.ring_v[self.slot: self.slot + 1],
-                                      self.w, self.ratio, self.p, self.state, self.comp_k, self.comp_v,
-                                      stream=stream)
+            ds4a.ds4a_compress_attn_decode(new_k, new_v, self.w, self.ratio, self.p, self.state, self.comp_k,
+                                           self.comp_v, self.q, self.ring_k[: self.n_win], self.ring_v[: self.n_win],
+                                           self.scale, self.out, stream=stream)
+            return self.out
         if self.topk:
             ds4a.ds4a_attn_decode(self.q, self.ring_k[: self.n_win], self.ring_v[: self.n_win], self.comp_k,
                                   self.comp_v, self.sel, self.topk, self.scale, self.out, stream=stream)

@@ -196,6 +196,29 @@ int ds4a_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
                      float scale, uint16_t *out, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * ds4a_compress_attn_decode -- one decode step of a layer that attends every
+ * compressed row (no indexer: the ratio-128 layers): the compressor update for
+ * the step's token and the attention, in a single kernel launch.
+ * ("DS4 (DwarfStar 4)", Key Techniques, "KV attention compression".)
+ *
+ * Same results as ds4a_compress_append(k_new, v_new, 1, D, score_w, ratio, pos,
+ * state, comp_k, comp_v, cap, stream) followed by ds4a_attn_decode(q, H, D,
+ * win_k, win_v, n_win, comp_k, comp_v, cap, NULL, floor((pos+1)/ratio), scale,
+ * out, NULL, 0, stream), bit for bit.  When the token completes a block, its
+ * pooled row is the last row attended and the one CTA that attends it writes
+ * it first; otherwise the compressor's state is updated off the critical path.
+ *
+ *   Compressor arguments as ds4a_compress_append with n_new = 1 and head_dim = D
+ *   (k_new, v_new: [1, D] fp16, the token at position pos).
+ *   Attention arguments as ds4a_attn_decode; the window must hold the token at pos.
+ *   Errors: the union of the two calls' checks; nothing is enqueued on error.
+ */
+int ds4a_compress_attn_decode(const uint16_t *k_new, const uint16_t *v_new, const float *score_w, int ratio,
+                              long long pos, float *state, uint16_t *comp_k, uint16_t *comp_v, long long cap,
+                              const uint16_t *q, int H, int D, const uint16_t *win_k, const uint16_t *win_v,
+                              int n_win, float scale, uint16_t *out, void *stream);
+
+/*
  * ds4a_attn_prefill -- causal attention for a prefill chunk of T queries at
  * positions q_pos0 .. q_pos0+T-1.
  *

@@ -105,6 +105,29 @@ def test_indexer_topk_compress_validation(ds4a_lib):
     assert call(q_pos=32771, cap=8192) == CAP   # position 32771 completes row 8192 (rows 0 .. 8191 fit)
 
 
+def test_compress_attn_decode_validation(ds4a_lib):
+    L = ds4a_lib.lib()
+    f = L.ds4a_compress_attn_decode
+
+    def call(**kw):
+        a = dict(k_new=FAKE, v_new=FAKE, w=FAKE, ratio=128, pos=131071, state=FAKE, ck=FAKE, cv=FAKE, cap=1024,
+                 q=FAKE, H=64, D=128, wk=FAKE, wv=FAKE, n_win=128, out=FAKE)
+        a.update(kw)
+        return f(a["k_new"], a["v_new"], a["w"], a["ratio"], a["pos"], a["state"], a["ck"], a["cv"], a["cap"],
+                 a["q"], a["H"], a["D"], a["wk"], a["wv"], a["n_win"], ctypes.c_float(0.088), a["out"], None)
+    assert call(ratio=0) == ARG
+    assert call(pos=-1) == ARG
+    assert call(H=12) == UNSUP
+    assert call(D=96) == UNSUP
+    assert call(ratio=2048) == UNSUP
+    assert call(n_win=0) == ARG
+    assert call(state=None) == ARG
+    assert call(out=None) == ARG
+    assert call(k_new=FAKE + 8) == ARG          # the token rows must be 16-byte aligned
+    assert call(ck=FAKE + 8) == ARG
+    assert call(cap=1023) == CAP                # position 131071 completes row 1023
+
+
 def test_attn_decode_validation(ds4a_lib):
     L = ds4a_lib.lib()
     f = L.ds4a_attn_decode

@@ -294,6 +294,43 @@ def test_indexer_topk_compress_matches_the_two_calls(p):
     assert ds4a.ds4a_last_device_error() == 0
 
 
+@pytest.mark.parametrize("ratio,p,H,D", [(128, 254, 64, 128), (128, 255, 64, 128), (128, 256, 8, 64), (4, 7, 8, 64),
+                                         (4, 1, 64, 128), (128, 131071, 64, 128)])
+def test_compress_attn_decode_matches_the_two_calls(ratio, p, H, D):
+    """The one-launch compressor update + attention over every visible row gives the
+    same bits as ds4a_compress_append followed by ds4a_attn_decode (sel = NULL):
+    output, running state and pooled rows (p + 1 = 256, 8, 131072 complete a block,
+    whose row is then attended; p = 1 at ratio 4 sees no compressed row)."""
+    W, seed = 128, 12
+    n_vis = (p + 1) // ratio
+    tok_k = torch.from_numpy(synth.normal_f16(seed, 4, synth.T_KRAW, (p + 1, D))).cuda()
+    tok_v = torch.from_numpy(synth.normal_f16(seed, 4, synth.T_VRAW, (p + 1, D))).cuda()
+    w = torch.from_numpy(synth.normal_f32(seed, 4, synth.T_W, (D,), 1.0 / np.sqrt(D))).cuda()
+    q = torch.from_numpy(synth.normal_f16(seed, 4, synth.T_Q, (H, D))).cuda()
+    win = slice(max(0, p - W + 1), p + 1)
+    comp_k = torch.zeros(n_vis + 1, D, dtype=torch.float16, device="cuda")
+    comp_v = torch.zeros_like(comp_k)
+    state = torch.zeros(2 + 2 * D, dtype=torch.float32, device="cuda")
+    if p:
+        ds4a.ds4a_compress_append(tok_k[:p], tok_v[:p], w, ratio, 0, state, comp_k, comp_v)
+    scale = 1.0 / np.sqrt(D)
+    outs = []
+    for fused in (False, True):
+        ck, cv, st = comp_k.clone(), comp_v.clone(), state.clone()
+        out = torch.full((H, D), 7, dtype=torch.float16, device="cuda")
+        if fused:
+            ds4a.ds4a_compress_attn_decode(tok_k[p:p + 1], tok_v[p:p + 1], w, ratio, p, st, ck, cv, q, tok_k[win],
+                                           tok_v[win], scale, out)
+        else:
+            ds4a.ds4a_compress_append(tok_k[p:p + 1], tok_v[p:p + 1], w, ratio, p, st, ck, cv)
+            ds4a.ds4a_attn_decode(q, tok_k[win], tok_v[win], ck, cv, None, n_vis, scale, out)
+        torch.cuda.synchronize()
+        outs.append([h(x) for x in (out, st, ck, cv)])
+    for name, a, b in zip(["out", "state", "comp_k", "comp_v"], *outs):
+        assert np.array_equal(a, b), name
+    assert ds4a.ds4a_last_device_error() == 0
+
+
 # ---- compressor: chunk-split invariance and online == blockwise ----------------------------------
 
 @pytest.mark.parametrize("ratio", [4, 128])

@@ -25,7 +25,7 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-@pytest.mark.parametrize("ratio,topk,fused", [(4, 16, False), (4, 16, True), (128, 0, False)])
+@pytest.mark.parametrize("ratio,topk,fused", [(4, 16, False), (4, 16, True), (128, 0, False), (128, 0, True)])
 def test_decode_steps_back_to_back(ratio, topk, fused):
     H, D, W, d_idx, seed = 8, 64, 32, 32, 5
     p0, S = 200 if ratio == 4 else 1020, 12
@@ -58,15 +58,18 @@ def test_decode_steps_back_to_back(ratio, topk, fused):
     for s in range(S):
         p = p0 + s
         n_vis = (p + 1) // ratio
-        if fused:   # the indexer query and the compressor update in one launch
+        if fused and topk:   # the indexer query and the compressor update in one launch
             ds4a.ds4a_indexer_topk_compress(qid[s], kid, p, ratio, topk, sel, sel_n, ws, rk[p:p + 1], rv[p:p + 1],
                                             wd, state, comp_k, comp_v)
-        else:
+        elif not fused:
             if topk:
                 ds4a.ds4a_indexer_topk(qid[s], kid, p, ratio, topk, sel, sel_n, ws)
             ds4a.ds4a_compress_append(rk[p:p + 1], rv[p:p + 1], wd, ratio, p, state, comp_k, comp_v)
         win = slice(p - W + 1, p + 1)
-        if topk:
+        if fused and not topk:   # the compressor update and the attention in one launch
+            ds4a.ds4a_compress_attn_decode(rk[p:p + 1], rv[p:p + 1], wd, ratio, p, state, comp_k, comp_v, qd[s],
+                                           rk[win], rv[win], scale, out[s])
+        elif topk:
             ds4a.ds4a_attn_decode(qd[s], rk[win], rv[win], comp_k, comp_v, sel, topk, scale, out[s])
             sels[s].copy_(sel)   # a stream-ordered copy: the next indexer writes sel again
         else:
