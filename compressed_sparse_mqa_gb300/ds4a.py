@@ -136,11 +136,8 @@ def ds4a_indexer_topk(q_idx, k_idx, q_pos0: int, ratio: int, k: int, out_idx, ou
     _check(rc, "ds4a_indexer_topk")
 
 
-def ds4a_indexer_topk_compress(q_idx, k_idx, q_pos: int, ratio: int, k: int, out_idx, out_n, ws, k_new, v_new,
-                               score_w, state, comp_k, comp_v, n_rows=None, stream=None):
-    """ds4a_indexer_topk for one query at q_pos (q_idx [d] or [1, d]) and
-    ds4a_compress_append of that position's token (k_new, v_new [1, D] fp16), in one
-    launch; arguments as the two calls."""
+def _marshal_indexer_topk_compress(q_idx, k_idx, q_pos: int, ratio: int, k: int, out_idx, out_n, ws, k_new, v_new,
+                                   score_w, state, comp_k, comp_v, n_rows=None, stream=None):
     q2 = q_idx if q_idx.dim() == 2 else q_idx.view(1, -1)
     if q2.shape[0] != 1:
         raise ValueError("indexer_topk_compress: one query")
@@ -155,21 +152,26 @@ def ds4a_indexer_topk_compress(q_idx, k_idx, q_pos: int, ratio: int, k: int, out
         raise ValueError("indexer_topk_compress: token / compressed-row shapes")
     if state.numel() < 2 + 2 * D or score_w.numel() != D:
         raise ValueError("indexer_topk_compress: state / score_w size")
-    rc = lib().ds4a_indexer_topk_compress(
-        _ptr(q2, torch.float16, "q_idx"), _ptr(k_idx, torch.float16, "k_idx") if k_idx.numel() else None, rows, d,
-        q_pos, ratio, k, _ptr(out_idx, torch.int32, "out_idx"), _ptr(out_n, torch.int32, "out_n", optional=True),
-        _ptr(ws, torch.uint8, "ws"), ws.numel(), _ptr(k_new, torch.float16, "k_new"),
-        _ptr(v_new, torch.float16, "v_new"), D, _ptr(score_w, torch.float32, "score_w"),
-        _ptr(state, torch.float32, "state"), _ptr(comp_k, torch.float16, "comp_k"),
-        _ptr(comp_v, torch.float16, "comp_v"), comp_k.shape[0], _stream(stream))
-    _check(rc, "ds4a_indexer_topk_compress")
+    return (_ptr(q2, torch.float16, "q_idx"), _ptr(k_idx, torch.float16, "k_idx") if k_idx.numel() else None, rows,
+            d, q_pos, ratio, k, _ptr(out_idx, torch.int32, "out_idx"), _ptr(out_n, torch.int32, "out_n", optional=True),
+            _ptr(ws, torch.uint8, "ws"), ws.numel(), _ptr(k_new, torch.float16, "k_new"),
+            _ptr(v_new, torch.float16, "v_new"), D, _ptr(score_w, torch.float32, "score_w"),
+            _ptr(state, torch.float32, "state"), _ptr(comp_k, torch.float16, "comp_k"),
+            _ptr(comp_v, torch.float16, "comp_v"), comp_k.shape[0], _stream(stream))
 
 
-def ds4a_compress_attn_decode(k_new, v_new, score_w, ratio: int, pos: int, state, comp_k, comp_v, q, win_k, win_v,
-                              scale: float, out, stream=None):
-    """ds4a_compress_append of the token at pos (k_new, v_new [1, D] fp16) and
-    ds4a_attn_decode over the window and every visible compressed row, in one launch;
-    arguments as the two calls."""
+def ds4a_indexer_topk_compress(q_idx, k_idx, q_pos: int, ratio: int, k: int, out_idx, out_n, ws, k_new, v_new,
+                               score_w, state, comp_k, comp_v, n_rows=None, stream=None):
+    """ds4a_indexer_topk for one query at q_pos (q_idx [d] or [1, d]) and
+    ds4a_compress_append of that position's token (k_new, v_new [1, D] fp16), in one
+    launch; arguments as the two calls."""
+    args = _marshal_indexer_topk_compress(q_idx, k_idx, q_pos, ratio, k, out_idx, out_n, ws, k_new, v_new, score_w,
+                                          state, comp_k, comp_v, n_rows, stream)
+    _check(lib().ds4a_indexer_topk_compress(*args), "ds4a_indexer_topk_compress")
+
+
+def _marshal_compress_attn_decode(k_new, v_new, score_w, ratio: int, pos: int, state, comp_k, comp_v, q, win_k,
+                                  win_v, scale: float, out, stream=None):
     H, D = q.shape
     if k_new.shape != (1, D) or v_new.shape != (1, D) or comp_k.shape != comp_v.shape or comp_k.shape[1] != D:
         raise ValueError("compress_attn_decode: token / compressed-row shapes")
@@ -177,28 +179,40 @@ def ds4a_compress_attn_decode(k_new, v_new, score_w, ratio: int, pos: int, state
         raise ValueError("compress_attn_decode: window / output shapes")
     if state.numel() < 2 + 2 * D or score_w.numel() != D:
         raise ValueError("compress_attn_decode: state / score_w size")
-    rc = lib().ds4a_compress_attn_decode(
-        _ptr(k_new, torch.float16, "k_new"), _ptr(v_new, torch.float16, "v_new"),
-        _ptr(score_w, torch.float32, "score_w"), ratio, pos, _ptr(state, torch.float32, "state"),
-        _ptr(comp_k, torch.float16, "comp_k"), _ptr(comp_v, torch.float16, "comp_v"), comp_k.shape[0],
-        _ptr(q, torch.float16, "q"), H, D, _ptr(win_k, torch.float16, "win_k"), _ptr(win_v, torch.float16, "win_v"),
-        win_k.shape[0], scale, _ptr(out, torch.float16, "out"), _stream(stream))
-    _check(rc, "ds4a_compress_attn_decode")
+    return (_ptr(k_new, torch.float16, "k_new"), _ptr(v_new, torch.float16, "v_new"),
+            _ptr(score_w, torch.float32, "score_w"), ratio, pos, _ptr(state, torch.float32, "state"),
+            _ptr(comp_k, torch.float16, "comp_k"), _ptr(comp_v, torch.float16, "comp_v"), comp_k.shape[0],
+            _ptr(q, torch.float16, "q"), H, D, _ptr(win_k, torch.float16, "win_k"), _ptr(win_v, torch.float16, "win_v"),
+            win_k.shape[0], scale, _ptr(out, torch.float16, "out"), _stream(stream))
+
+
+def ds4a_compress_attn_decode(k_new, v_new, score_w, ratio: int, pos: int, state, comp_k, comp_v, q, win_k, win_v,
+                              scale: float, out, stream=None):
+    """ds4a_compress_append of the token at pos (k_new, v_new [1, D] fp16) and
+    ds4a_attn_decode over the window and every visible compressed row, in one launch;
+    arguments as the two calls."""
+    args = _marshal_compress_attn_decode(k_new, v_new, score_w, ratio, pos, state, comp_k, comp_v, q, win_k, win_v,
+                                         scale, out, stream)
+    _check(lib().ds4a_compress_attn_decode(*args), "ds4a_compress_attn_decode")
+
+
+def _marshal_attn_decode(q, win_k, win_v, comp_k, comp_v, sel, n_sel: int, scale: float, out, stream=None):
+    H, D = q.shape
+    n_win = win_k.shape[0]
+    n_comp = 0 if comp_k is None else comp_k.shape[0]
+    return (_ptr(q, torch.float16, "q"), H, D, _ptr(win_k, torch.float16, "win_k"),
+            _ptr(win_v, torch.float16, "win_v"), n_win,
+            _ptr(comp_k, torch.float16, "comp_k", optional=True),
+            _ptr(comp_v, torch.float16, "comp_v", optional=True), n_comp,
+            _ptr(sel, torch.int32, "sel", optional=True), n_sel, scale,
+            _ptr(out, torch.float16, "out"), None, 0, _stream(stream))
 
 
 def ds4a_attn_decode(q, win_k, win_v, comp_k, comp_v, sel, n_sel: int, scale: float, out, stream=None):
     """q [H, D] fp16; window rows win_k/win_v [n_win, D]; comp rows [n_comp, D]; sel int32 [>= n_sel]
     or None (rows 0..n_sel-1); out [H, D] fp16."""
-    H, D = q.shape
-    n_win = win_k.shape[0]
-    n_comp = 0 if comp_k is None else comp_k.shape[0]
-    rc = lib().ds4a_attn_decode(_ptr(q, torch.float16, "q"), H, D, _ptr(win_k, torch.float16, "win_k"),
-                                _ptr(win_v, torch.float16, "win_v"), n_win,
-                                _ptr(comp_k, torch.float16, "comp_k", optional=True),
-                                _ptr(comp_v, torch.float16, "comp_v", optional=True), n_comp,
-                                _ptr(sel, torch.int32, "sel", optional=True), n_sel, scale,
-                                _ptr(out, torch.float16, "out"), None, 0, _stream(stream))
-    _check(rc, "ds4a_attn_decode")
+    args = _marshal_attn_decode(q, win_k, win_v, comp_k, comp_v, sel, n_sel, scale, out, stream)
+    _check(lib().ds4a_attn_decode(*args), "ds4a_attn_decode")
 
 
 def ds4a_attn_prefill(q, raw_k, raw_v, n_prior: int, window: int, comp_k, comp_v, sel, q_pos0: int,
@@ -215,3 +229,23 @@ def ds4a_attn_prefill(q, raw_k, raw_v, n_prior: int, window: int, comp_k, comp_v
                                  _ptr(sel, torch.int32, "sel", optional=True), k_stride, q_pos0, ratio, scale,
                                  _ptr(out, torch.float16, "out"), None, 0, _stream(stream))
     _check(rc, "ds4a_attn_prefill")
+
+
+_MARSHAL = {"ds4a_attn_decode": _marshal_attn_decode,
+            "ds4a_compress_attn_decode": _marshal_compress_attn_decode,
+            "ds4a_indexer_topk_compress": _marshal_indexer_topk_compress}
+
+
+def bind(name: str, *args, **kwargs):
+    """The C call that the binding function `name` makes for these arguments,
+    marshalled once: returns a zero-argument callable that repeats exactly that call
+    (the same device buffers and stream) and raises Ds4aError on a non-zero status.
+    For a step repeated on persistent tensors (the per-call Python checks run once)."""
+    f = getattr(lib(), name)
+    cargs = tuple(_MARSHAL[name](*args, **kwargs))
+
+    def call():
+        rc = f(*cargs)
+        if rc != DS4A_OK:
+            raise Ds4aError(rc, name)
+    return call

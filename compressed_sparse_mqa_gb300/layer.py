@@ -133,24 +133,38 @@ class DecodeLayer:
         Under programmatic dependent launch the first kernel's input-only loads
         overlap the previous layer's attention.
         """
+        for name, args in self._step_calls():
+            getattr(ds4a, name)(*args, stream=stream)
+        return self.out
+
+    def bind(self, stream=None):
+        """The decode step marshalled once (the layer's tensors are persistent): a
+        zero-argument callable that issues the same launches as step(stream), without
+        the binding's per-call Python argument checks."""
+        calls = [ds4a.bind(name, *args, stream=stream) for name, args in self._step_calls()]
+
+        def run():
+            for c in calls:
+                c()
+            return self.out
+        return run
+
+    def _step_calls(self):
+        """(binding function, arguments) of each launch of the step, in order."""
         new_k = self.ring_k[self.slot: self.slot + 1]
         new_v = self.ring_v[self.slot: self.slot + 1]
+        win_k, win_v = self.ring_k[: self.n_win], self.ring_v[: self.n_win]
         if self.topk:
-            ds4a.ds4a_indexer_topk_compress(self.q_idx, self.kidx, self.p, self.ratio, self.topk, self.sel,
-                                            self.sel_n, self.ws, new_k, new_v, self.w, self.state, self.comp_k,
-                                            self.comp_v, stream=stream)
-        elif self.ratio:
-            ds4a.ds4a_compress_attn_decode(new_k, new_v, self.w, self.ratio, self.p, self.state, self.comp_k,
-                                           self.comp_v, self.q, self.ring_k[: self.n_win], self.ring_v[: self.n_win],
-                                           self.scale, self.out, stream=stream)
-            return self.out
-        if self.topk:
-            ds4a.ds4a_attn_decode(self.q, self.ring_k[: self.n_win], self.ring_v[: self.n_win], self.comp_k,
-                                  self.comp_v, self.sel, self.topk, self.scale, self.out, stream=stream)
-        else:
-            ds4a.ds4a_attn_decode(self.q, self.ring_k[: self.n_win], self.ring_v[: self.n_win], self.comp_k,
-                                  self.comp_v, None, self.n_vis, self.scale, self.out, stream=stream)
-        return self.out
+            return [("ds4a_indexer_topk_compress", (self.q_idx, self.kidx, self.p, self.ratio, self.topk, self.sel,
+                                                    self.sel_n, self.ws, new_k, new_v, self.w, self.state, self.comp_k,
+                                                    self.comp_v)),
+                    ("ds4a_attn_decode", (self.q, win_k, win_v, self.comp_k, self.comp_v, self.sel, self.topk,
+                                          self.scale, self.out))]
+        if self.ratio:
+            return [("ds4a_compress_attn_decode", (new_k, new_v, self.w, self.ratio, self.p, self.state, self.comp_k,
+                                                   self.comp_v, self.q, win_k, win_v, self.scale, self.out))]
+        return [("ds4a_attn_decode", (self.q, win_k, win_v, self.comp_k, self.comp_v, None, self.n_vis, self.scale,
+                                      self.out))]
 
 
 class PrefillLayer:

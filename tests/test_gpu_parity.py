@@ -331,6 +331,24 @@ def test_compress_attn_decode_matches_the_two_calls(ratio, p, H, D):
     assert ds4a.ds4a_last_device_error() == 0
 
 
+@pytest.mark.parametrize("layer", [0, 2, 3])   # window only, ratio 4 + indexer, ratio 128
+def test_bound_step_matches_step(layer):
+    """DecodeLayer.bind() marshals the step once; its launches give the same bits as step()."""
+    inst = configs.decode(configs.c5_layer_params(layer))
+    a = DecodeLayer(inst)
+    b = a.clone()
+    out_a = h(a.step())
+    run = b.bind()
+    out_b = h(run())
+    torch.cuda.synchronize()
+    assert np.array_equal(out_a, out_b)
+    for name in ("state", "comp_k", "comp_v", "sel"):
+        ta, tb = getattr(a, name, None), getattr(b, name, None)
+        if ta is not None:
+            assert np.array_equal(h(ta), h(tb)), name
+    assert ds4a.ds4a_last_device_error() == 0
+
+
 # ---- compressor: chunk-split invariance and online == blockwise ----------------------------------
 
 @pytest.mark.parametrize("ratio", [4, 128])
