@@ -625,8 +625,10 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a, cmp
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");   // the copies read through the async proxy
     __syncthreads();
     cluster_wait();   // every CTA's receive barrier is armed
-    if (threadIdx.x == 0) {
-        for (int o = 0; o < cs; ++o) {
+    // lane 0 of each warp sends the rows of owners warp, warp + 8, ...: the copies are
+    // issued in parallel rather than one after another by one thread
+    if (lane == 0) {
+        for (int o = warp; o < cs; o += kThreads / 32) {
             const int nho = min(a.H, (o + 1) * hpc) - o * hpc;
             if (nho > 0)
                 bulk_copy_to_cta(cluster_addr(recv + rank * hpc * (D + 4), o), send + o * hpc * (D + 4),
@@ -663,8 +665,8 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a, cmp
         packed.y = pack_half2(acc.z * inv, acc.w * inv);
         *reinterpret_cast<uint2 *>(a.out + (hb + hh) * D + d) = packed;
     }
-    // this CTA's outgoing copies have finished reading its shared memory
-    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+    // this CTA's outgoing copies (each issuing lane's) have finished reading its shared memory
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
 
 struct PrefillArgs {
