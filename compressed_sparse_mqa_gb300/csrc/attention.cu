@@ -528,6 +528,43 @@ static_assert(4 * 32 * (128 / 2 + 4) * sizeof(float) <= sizeof(Smem<128>), "exch
 static_assert(64 * (128 + 4) * sizeof(float) <= sizeof(Smem<128>) && 64 * (64 + 4) * sizeof(float) <= sizeof(Smem<64>),
               "the send rows of 64 heads fit in the tiles");
 
+// Log-sum-exp merge of the (O, m, l) rows every rank sent for heads [hb, hb + nh):
+// recv[rank][local head][D + 4]; out[h] = sum_r w_r O_r / sum_r w_r l_r with
+// w_r = 2^(m_r - max_r m_r).  CS: the cluster size (0: runtime cs).
+template <int D, int CS>
+DS4A_DEVINL void merge_heads(const float *recv, int hpc, int hb, int nh, uint16_t *out, int cs_rt = CS) {
+    const int cs = CS > 0 ? CS : cs_rt;
+    for (int idx = threadIdx.x; idx < nh * (D / 2); idx += kThreads) {   // 2 columns per item
+        const int hh = idx / (D / 2), d = (idx % (D / 2)) * 2;
+        float M = -INFINITY;
+        if constexpr (CS > 0) {
+#pragma unroll
+            for (int r = 0; r < CS; ++r) M = fmaxf(M, recv[(r * hpc + hh) * (D + 4) + D]);
+        } else {
+            for (int r = 0; r < cs; ++r) M = fmaxf(M, recv[(r * hpc + hh) * (D + 4) + D]);
+        }
+        float den = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
+        auto add_rank = [&](int r) {
+            const float *row = recv + (r * hpc + hh) * (D + 4);
+            const float mr = row[D];
+            const float w = mr == -INFINITY ? 0.f : exp2f(mr - M);
+            den = fmaf(w, row[D + 1], den);
+            const float2 o = *reinterpret_cast<const float2 *>(row + d);
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+        };
+        if constexpr (CS > 0) {
+#pragma unroll
+            for (int r = 0; r < CS; ++r) add_rank(r);
+        } else {
+            for (int r = 0; r < cs; ++r) add_rank(r);
+        }
+        const float inv = 1.f / den;
+        *reinterpret_cast<uint32_t *>(out + (hb + hh) * D + d) = pack_half2(acc.x * inv, acc.y * inv);
+    }
+}
+
 // kCompress: one CTA (a.comp_rank) also runs the compressor's update for the step's
 // token (n_new = 1, arguments ca): its score before the dependency wait; the
 // running state and, when the token completes a block, the pooled row after it.
@@ -641,30 +678,11 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a, cmp
     // every byte destined for this CTA has landed
     if (!recv_wait(&s_recv_bar)) record_error(a.src.err, DS4A_ERR_TIMEOUT);
 
-    // merge this CTA's heads from local shared memory
-    for (int idx = threadIdx.x; idx < nh * (D / 4); idx += kThreads) {
-        const int hh = idx / (D / 4), d = (idx % (D / 4)) * 4;
-        float M = -INFINITY;
-        for (int r = 0; r < cs; ++r) M = fmaxf(M, recv[(r * hpc + hh) * (D + 4) + D]);
-        float den = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int r = 0; r < cs; ++r) {
-            const float *row = recv + (r * hpc + hh) * (D + 4);
-            const float mr = row[D];
-            const float w = mr == -INFINITY ? 0.f : exp2f(mr - M);
-            den = fmaf(w, row[D + 1], den);
-            const float4 o = *reinterpret_cast<const float4 *>(row + d);
-            acc.x = fmaf(w, o.x, acc.x);
-            acc.y = fmaf(w, o.y, acc.y);
-            acc.z = fmaf(w, o.z, acc.z);
-            acc.w = fmaf(w, o.w, acc.w);
-        }
-        const float inv = 1.f / den;
-        uint2 packed;
-        packed.x = pack_half2(acc.x * inv, acc.y * inv);
-        packed.y = pack_half2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2 *>(a.out + (hb + hh) * D + d) = packed;
-    }
+    // merge this CTA's heads from local shared memory (the loop over the cluster's ranks
+    // unrolled for the usual cluster sizes)
+    if (cs == 16) merge_heads<D, 16>(recv, hpc, hb, nh, a.out);
+    else if (cs == 8) merge_heads<D, 8>(recv, hpc, hb, nh, a.out);
+    else merge_heads<D, 0>(recv, hpc, hb, nh, a.out, cs);
     // this CTA's outgoing copies (each issuing lane's) have finished reading its shared memory
     if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
