@@ -157,3 +157,29 @@ def test_attn_prefill_validation(ds4a_lib):
              None) == UNSUP
     assert f(None, 0, 64, 128, None, None, 0, 128, None, None, 0, None, 0, 0, 4, s, None, None, 0,
              None) == 0     # T = 0: no-op
+
+
+def test_binding_refuses_host_tensors(ds4a_lib):
+    """The product path has no CPU fallback: the binding refuses host tensors before any
+    C call (plain and one-launch decode calls, and the marshalled-once form)."""
+    import torch
+    H, D, W = 8, 64, 32
+    q = torch.zeros(H, D, dtype=torch.float16)
+    win = torch.zeros(W, D, dtype=torch.float16)
+    comp = torch.zeros(4, D, dtype=torch.float16)
+    tok = torch.zeros(1, D, dtype=torch.float16)
+    w = torch.zeros(D, dtype=torch.float32)
+    state = torch.zeros(2 + 2 * D, dtype=torch.float32)
+    out = torch.zeros(H, D, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ds4a_lib.ds4a_attn_decode(q, win, win, comp, comp, None, 4, 0.125, out)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ds4a_lib.ds4a_compress_attn_decode(tok, tok, w, 128, 511, state, comp, comp, q, win, win, 0.125, out)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ds4a_lib.bind("ds4a_attn_decode", q, win, win, comp, comp, None, 4, 0.125, out)
+    kidx = torch.zeros(4, 32, dtype=torch.float16)
+    qi = torch.zeros(32, dtype=torch.float16)
+    sel = torch.zeros(16, dtype=torch.int32)
+    ws = torch.zeros(4096, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ds4a_lib.ds4a_indexer_topk_compress(qi, kidx, 19, 4, 16, sel, None, ws, tok, tok, w, state, comp, comp)
