@@ -1,5 +1,6 @@
 // ds4a_api.cu -- the C ABI: argument validation, per-device setup, dispatch to
 // the kernel launchers, status strings and the device error word.
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -14,10 +15,12 @@ __device__ unsigned int g_device_error;
 
 constexpr int kMaxDevices = 64;
 
+// Filled once per device under g_mu; `ready` is stored with release order after the
+// fields, and read with acquire order, so a thread that sees it set also sees them.
 struct DeviceInfo {
     unsigned int *err = nullptr;
     int num_sms = 0;
-    bool ready = false;
+    std::atomic<bool> ready{false};
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -34,9 +37,9 @@ int make_ctx(void *stream, ds4a::Ctx &c) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DS4A_ERR_CUDA;
     DeviceInfo &d = g_dev[dev];
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!d.ready) {
+        if (!d.ready.load(std::memory_order_relaxed)) {
             void *p = nullptr;
             if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return DS4A_ERR_CUDA;
             int sms = 0;
@@ -44,7 +47,7 @@ int make_ctx(void *stream, ds4a::Ctx &c) {
                 return DS4A_ERR_CUDA;
             d.err = static_cast<unsigned int *>(p);
             d.num_sms = sms;
-            d.ready = true;
+            d.ready.store(true, std::memory_order_release);
         }
     }
     c.stream = static_cast<cudaStream_t>(stream);
@@ -176,6 +179,7 @@ int ds4a_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
     int rc = check_heads(H, D);
     if (rc != DS4A_OK) return rc;
     if (n_win < 1 || n_win > 4096 || n_sel < 0 || n_comp < 0) return DS4A_ERR_ARG;
+    if (n_sel > 0x7fffffff - n_win) return DS4A_ERR_UNSUPPORTED;   // n_win + n_sel must fit in int
     if (!q || !win_k || !win_v || !out) return DS4A_ERR_ARG;
     if (n_sel > 0 && (!comp_k || !comp_v)) return DS4A_ERR_ARG;
     if (!sel && n_sel > n_comp) return DS4A_ERR_ARG;
@@ -250,19 +254,26 @@ int ds4a_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *ra
 // whose enqueue step must not allocate device memory (an allocation there can
 // synchronise the device or is simply not allowed by the host), and callers that
 // run under a fixed, pre-reserved memory budget.  For them this file keeps the
-// one-query indexer's scratch (ticket header + one u32 key per row) in a
+// one-query indexer's scratch (ticket header + one u32 key per visible row) in a
 // statically sized device array that every GPU loading the library holds until
 // the process exits.
 namespace {
 
-constexpr long long kNoAllocMaxRows = 65536;   // 65536 rows: 256 KiB of keys
+constexpr long long kNoAllocMaxRows = 65536;   // 65536 visible rows: 256 KiB of keys
 constexpr size_t kNoAllocHeaderBytes = 256;
 constexpr size_t kNoAllocScratchBytes = kNoAllocHeaderBytes + kNoAllocMaxRows * sizeof(uint32_t);
 
+// Zero when the module loads.  The indexer kernel's last CTA puts the completion
+// ticket in the header back to zero when it finishes, so no call has to clear it.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-void *g_noalloc_addr[kMaxDevices];
-bool g_noalloc_ready[kMaxDevices];
+// The array's device address, looked up once per device (with that device current);
+// `ready` is stored with release order after the address, read with acquire order.
+struct NoAllocSlot {
+    void *addr = nullptr;
+    std::atomic<bool> ready{false};
+};
+NoAllocSlot g_noalloc[kMaxDevices];
 
 }  // namespace
 
@@ -271,35 +282,33 @@ extern "C" int ds4a_indexer_topk_noalloc(const uint16_t *q_idx, const uint16_t *
                                          int32_t *out_n, void *stream) {
     if (n_rows < 0 || q_pos < 0 || ratio < 1 || k < 1) return DS4A_ERR_ARG;
     if (d_idx < 8 || d_idx > 256 || d_idx % 8 != 0 || k > 2048) return DS4A_ERR_UNSUPPORTED;
-    if (n_rows > kNoAllocMaxRows) return DS4A_ERR_WORKSPACE;   // beyond the built-in scratch
-    if (!q_idx || !out_idx || (n_rows > 0 && !k_idx)) return DS4A_ERR_ARG;
+    // the kernel scores (and keeps a key for) the visible rows only
+    const long long n_vis = (q_pos + 1) / ratio < n_rows ? (q_pos + 1) / ratio : n_rows;
+    if (n_vis > kNoAllocMaxRows) return DS4A_ERR_WORKSPACE;   // beyond the built-in scratch
+    if (!q_idx || !out_idx || (n_vis > 0 && !k_idx)) return DS4A_ERR_ARG;
     if (!aligned(q_idx, 16) || !aligned(k_idx, 16) || !aligned(out_idx, 4) || !aligned(out_n, 4))
         return DS4A_ERR_ARG;
-    if (ds4a::indexer_ws_bytes(1, n_rows, k) > kNoAllocScratchBytes) return DS4A_ERR_WORKSPACE;
+    if (ds4a::indexer_ws_bytes(1, n_vis, k) > kNoAllocScratchBytes) return DS4A_ERR_WORKSPACE;
     ds4a::Ctx c;
     int rc = make_ctx(stream, c);
     if (rc != DS4A_OK) return rc;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DS4A_ERR_CUDA;
-    if (!g_noalloc_ready[dev]) {
+    NoAllocSlot &slot = g_noalloc[dev];
+    if (!slot.ready.load(std::memory_order_acquire)) {
         // once per device, with that device current: the device address of the array
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_noalloc_ready[dev]) {
+        if (!slot.ready.load(std::memory_order_relaxed)) {
             void *p = nullptr;
             if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
                 cudaGetLastError();
                 return DS4A_ERR_CUDA;
             }
-            g_noalloc_addr[dev] = p;
-            g_noalloc_ready[dev] = true;
+            slot.addr = p;
+            slot.ready.store(true, std::memory_order_release);
         }
     }
-    void *scratch = g_noalloc_addr[dev];
-    // the completion ticket in the header must start at zero; the keys need no clearing
-    if (cudaMemsetAsync(scratch, 0, kNoAllocHeaderBytes, c.stream) != cudaSuccess) {
-        cudaGetLastError();
-        return DS4A_ERR_CUDA;
-    }
-    return from_cuda(ds4a::launch_indexer(q_idx, 1, k_idx, n_rows, d_idx, q_pos, ratio, k, out_idx, out_n,
-                                          scratch, c));
+    // rows past n_vis are never read: the call is the same as one over the visible rows
+    return from_cuda(ds4a::launch_indexer(q_idx, 1, k_idx, n_vis, d_idx, q_pos, ratio, k, out_idx, out_n,
+                                          slot.addr, c));
 }

@@ -155,15 +155,15 @@ int ds4a_indexer_topk_compress(const uint16_t *q_idx, const uint16_t *k_idx, lon
  * by every GPU that loads the library until the process exits.
  *
  *   Arguments as ds4a_indexer_topk with n_q = 1 and q_pos0 = q_pos.
- *   n_rows     at most 65536; larger returns DS4A_ERR_WORKSPACE and enqueues
- *              nothing.
+ *   The limit counts the rows the query sees, min(n_rows, floor((q_pos+1)/ratio)):
+ *   at most 65536; more returns DS4A_ERR_WORKSPACE and enqueues nothing.
  *   The first call on each device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
- *   Each call enqueues a cudaMemsetAsync that clears the array's ticket
- *   header, then the indexer kernel.  All calls share the one array and it keeps
- *   the last call's contents: calls whose work overlaps on the GPU (different
- *   streams, or different host threads, without ordering between them) race
- *   and give wrong results.
+ *   Each call enqueues the indexer kernel only: the array starts at zero and the
+ *   kernel leaves its completion ticket at zero when it finishes.  All calls
+ *   share the one array and it keeps the last call's contents: calls whose work
+ *   overlaps on the GPU (different streams, or different host threads, without
+ *   ordering between them) race and give wrong results.
  */
 int ds4a_indexer_topk_noalloc(const uint16_t *q_idx, const uint16_t *k_idx, long long n_rows,
                               int d_idx, long long q_pos, int ratio, int k, int32_t *out_idx,

@@ -140,6 +140,24 @@ def test_attn_decode_validation(ds4a_lib):
     # sel = NULL means rows 0..n_sel-1: n_sel may not exceed n_comp
     assert f(FAKE, 64, 128, FAKE, FAKE, 128, FAKE, FAKE, 100, None, 101, s, FAKE, None, 0, None) == ARG
     assert f(FAKE, 64, 128, FAKE + 8, FAKE, 128, FAKE, FAKE, 100, None, 10, s, FAKE, None, 0, None) == ARG
+    # n_win + n_sel must fit in an int (the kernel's row count)
+    assert f(FAKE, 64, 128, FAKE, FAKE, 128, FAKE, FAKE, 100, FAKE, 2**31 - 100, s, FAKE, None, 0,
+             None) == UNSUP
+
+
+def test_noalloc_indexer_validation(ds4a_lib):
+    """The allocation-free indexer's limit counts the rows the query sees: more rows than
+    its scratch holds are refused only when the position makes them visible."""
+    L = ctypes.CDLL(ds4a_lib.LIB_PATH)
+    f = L.ds4a_indexer_topk_noalloc
+    P, I, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+    f.argtypes = [P, P, LL, I, LL, I, I, P, P, P]
+    f.restype = I
+    assert f(FAKE, FAKE, 70000, 128, 4 * 70000, 4, 512, FAKE, FAKE, None) == WS     # 70000 visible
+    assert f(FAKE, FAKE, 65537, 128, 4 * 65537, 4, 512, FAKE, FAKE, None) == WS
+    assert f(FAKE, FAKE, 70000, 128, 4 * 60000, 4, 0, FAKE, FAKE, None) == ARG      # 60000 visible, bad k
+    assert f(FAKE, FAKE, 70000, 100, 4 * 60000, 4, 512, FAKE, FAKE, None) == UNSUP  # d_idx
+    assert f(FAKE + 4, FAKE, 70000, 128, 4 * 60000, 4, 512, FAKE, FAKE, None) == ARG  # misaligned query
 
 
 def test_attn_prefill_validation(ds4a_lib):

@@ -13,6 +13,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
+from parity import check_sel
+
 pytestmark = pytest.mark.gpu
 
 DS4A_OK, DS4A_ERR_WORKSPACE = 0, 6
@@ -37,8 +40,10 @@ def _with_workspace(lib):
     return f
 
 
+# the last case passes more rows than the scratch holds, of which the query sees only
+# floor((q_pos + 1) / 4) = 50001: the limit counts visible rows
 @pytest.mark.parametrize("n_rows,d_idx,k,q_pos", [(8192, 128, 512, 32768), (20000, 64, 100, 4 * 20000 + 1),
-                                                  (300, 32, 512, 4 * 300 + 3)])
+                                                  (300, 32, 512, 4 * 300 + 3), (70000, 64, 512, 200006)])
 def test_noalloc_indexer_matches_workspace_indexer(ds4a_lib, n_rows, d_idx, k, q_pos):
     assert torch.cuda.is_available()
     lib = ctypes.CDLL(ds4a_lib.LIB_PATH)
@@ -58,9 +63,15 @@ def test_noalloc_indexer_matches_workspace_indexer(ds4a_lib, n_rows, d_idx, k, q
         assert noalloc(q.data_ptr(), kidx.data_ptr(), n_rows, d_idx, q_pos, 4, k, got_idx.data_ptr(),
                        got_n.data_ptr(), stream) == DS4A_OK
         torch.cuda.synchronize()
-        assert int(got_n.item()) == int(ref_n.item()) == min(k, min(n_rows, (q_pos + 1) // 4))
+        n_vis = min(n_rows, (q_pos + 1) // 4)
+        assert int(got_n.item()) == int(ref_n.item()) == min(k, n_vis)
         # kept rows are integers: bit-exact
         assert torch.equal(got_idx, ref_idx), f"call {call}: rows differ"
+        if call == 1:
+            # and against the oracle: the same rows up to near-ties of the k-th score
+            q_h, k_h = q.cpu().numpy(), kidx[:n_vis].cpu().numpy()
+            scores = oracle.index_scores(q_h, k_h)
+            check_sel(got_idx.cpu().numpy(), oracle.topk(scores, k), scores, k, "noalloc vs oracle")
     assert ds4a_lib.ds4a_last_device_error() == 0
 
 
