@@ -485,8 +485,8 @@ DS4A_DEVINL void tc_mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))),
                  "r"(count));
 }
-// bounded wait (about a second of wall time) for phase 0 of a receive barrier
-DS4A_DEVINL bool recv_wait(uint64_t *bar) {
+// bounded wait (limit_ns of wall time) for phase 0 of a receive barrier
+DS4A_DEVINL bool recv_wait(uint64_t *bar, uint64_t limit_ns) {
     const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
@@ -499,9 +499,10 @@ DS4A_DEVINL bool recv_wait(uint64_t *bar) {
         uint64_t now;
         asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(now));
         if (it == 0) t0 = now;
-        else if (now - t0 > 1000000000ull) return false;
+        else if (now - t0 > limit_ns) return false;
     }
 }
+constexpr uint64_t kRecvLimitNs = 1000000000ull;   // about a second
 DS4A_DEVINL void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
 DS4A_DEVINL void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
 
@@ -514,6 +515,7 @@ struct DecodeArgs {
     float scale_log2;
     int comp_rank;     // with the compressor: the CTA that runs its update (it attends the row it may write)
     int comp_first;    // the update completes a block: its row is written before that CTA attends
+    long long test_wait_ns;   // > 0 (test hook only): CTA 0 also waits this long on a barrier nobody completes
 };
 
 constexpr int kRecvRows = 80;   // >= cluster size * ceil(H / cluster size) for H <= 64
@@ -676,7 +678,16 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a, cmp
     if (comp_here && !a.comp_first)   // off the critical path: while the partials travel
         cmp::pool_segment<kThreads>(ca, ca.pos / ca.ratio, ca.pos, ca.pos + 1, ca.pos % ca.ratio != 0, s_cw, s_cred);
     // every byte destined for this CTA has landed
-    if (!recv_wait(&s_recv_bar)) record_error(a.src.err, DS4A_ERR_TIMEOUT);
+    if (!recv_wait(&s_recv_bar, kRecvLimitNs)) record_error(a.src.err, DS4A_ERR_TIMEOUT);
+    if (a.test_wait_ns > 0 && rank == 0) {
+        // Test hook: the bounded wait's give-up path, exercised with nothing in flight.
+        // Every copy destined for this CTA has landed (the wait above completed), and
+        // this barrier, armed for one arrival that no thread makes, never completes.
+        __shared__ __align__(8) uint64_t s_never_bar;
+        if (threadIdx.x == 0) tc_mbar_init(&s_never_bar, 1);
+        __syncthreads();
+        if (!recv_wait(&s_never_bar, static_cast<uint64_t>(a.test_wait_ns))) record_error(a.src.err, DS4A_ERR_TIMEOUT);
+    }
 
     // merge this CTA's heads from local shared memory (the loop over the cluster's ranks
     // unrolled for the usual cluster sizes)
@@ -826,6 +837,7 @@ cudaError_t launch_attn_decode(const uint16_t *q, int H, int D, const uint16_t *
     a.scale_log2 = scale * kLog2e;
     a.comp_rank = -1;
     a.comp_first = 0;
+    a.test_wait_ns = test_wait_limit_ns();
     int cluster = 16;
     cudaError_t e;
     if (D == 128) {
@@ -852,6 +864,7 @@ cudaError_t launch_compress_attn_decode(const uint16_t *k_new, const uint16_t *v
     a.n_rows = n_win + static_cast<int>(n_vis);
     a.scale_log2 = scale * kLog2e;
     a.comp_first = (pos + 1) % ratio == 0;
+    a.test_wait_ns = test_wait_limit_ns();
     const cmp::CompressArgs ca{k_new, v_new, score_w, state, comp_k, comp_v, pos, 1, D, ratio};
     int cluster = 16;
     cudaError_t e = D == 128 ? configure<128>(cluster) : configure<64>(cluster);

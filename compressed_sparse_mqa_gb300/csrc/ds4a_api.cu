@@ -57,6 +57,8 @@ int make_ctx(void *stream, ds4a::Ctx &c) {
     return DS4A_OK;
 }
 
+std::atomic<long long> g_test_wait_ns{0};
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int from_cuda(cudaError_t e) {
@@ -67,7 +69,15 @@ int from_cuda(cudaError_t e) {
 
 }  // namespace
 
+long long ds4a::test_wait_limit_ns() { return g_test_wait_ns.load(std::memory_order_relaxed); }
+
 extern "C" {
+
+int ds4a_test_set_wait_limit(long long limit_ns) {
+    if (limit_ns < 0 || limit_ns > 10000000000LL) return DS4A_ERR_ARG;
+    g_test_wait_ns.store(limit_ns, std::memory_order_relaxed);
+    return DS4A_OK;
+}
 
 const char *ds4a_status_str(int status) {
     switch (status) {

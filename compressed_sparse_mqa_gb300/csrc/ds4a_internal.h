@@ -19,6 +19,9 @@ cudaError_t launch_compress(const uint16_t *k, const uint16_t *v, int n_new, int
                             uint16_t *comp_v, const Ctx &c);
 
 size_t indexer_ws_bytes(int n_q, long long n_rows, int k);
+
+// test hook (ds4a_test_set_wait_limit): 0, or the limit of the extra never-completed wait
+long long test_wait_limit_ns();
 cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
                            int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
                            int32_t *out_n, void *ws, const Ctx &c);

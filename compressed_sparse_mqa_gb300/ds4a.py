@@ -28,7 +28,8 @@ DS4A_ERR_DEVICE_INDEX = 7
 
 EXPORTED = ["ds4a_status_str", "ds4a_last_device_error", "ds4a_compress_append",
             "ds4a_indexer_topk", "ds4a_indexer_workspace_bytes", "ds4a_attn_decode",
-            "ds4a_attn_prefill", "ds4a_indexer_topk_compress", "ds4a_compress_attn_decode"]
+            "ds4a_attn_prefill", "ds4a_indexer_topk_compress", "ds4a_compress_attn_decode",
+            "ds4a_indexer_topk_noalloc", "ds4a_test_set_wait_limit"]
 
 
 class Ds4aError(RuntimeError):
@@ -47,6 +48,8 @@ def lib() -> ctypes.CDLL:
         L.ds4a_status_str.argtypes = [I]
         L.ds4a_status_str.restype = ctypes.c_char_p
         L.ds4a_last_device_error.argtypes = [P]
+        L.ds4a_test_set_wait_limit.argtypes = [LL]
+        L.ds4a_indexer_topk_noalloc.argtypes = [P, P, LL, I, LL, I, I, P, P, P]
         L.ds4a_compress_append.argtypes = [P, P, I, I, P, I, LL, P, P, P, LL, P]
         L.ds4a_indexer_topk.argtypes = [P, I, P, LL, I, LL, I, I, P, P, P, SZ, P]
         L.ds4a_indexer_topk_compress.argtypes = [P, P, LL, I, LL, I, I, P, P, P, SZ, P, P, I, P, P, P, P, LL, P]
@@ -95,6 +98,12 @@ def _stream(stream):
 
 def ds4a_last_device_error(stream=None) -> int:
     return lib().ds4a_last_device_error(_stream(stream))
+
+
+def ds4a_test_set_wait_limit(limit_ns: int):
+    """Test hook: decode attention launches enqueued afterwards add a wait that gives up
+    after limit_ns and records DS4A_ERR_TIMEOUT (0 turns it off)."""
+    _check(lib().ds4a_test_set_wait_limit(int(limit_ns)), "ds4a_test_set_wait_limit")
 
 
 def ds4a_compress_append(k, v, score_w, ratio: int, pos: int, state, comp_k, comp_v, stream=None):

@@ -89,7 +89,11 @@ class DecodeLayer:
         else:
             self.comp_k = self.comp_v = None
         if self.topk:
-            self.kidx = _dev(inst.kidx, dev)
+            # one indexer key per compressed row; rows past the given ones are filled as
+            # advance() completes their blocks
+            self.kidx = torch.zeros(max(1, self.n_vis + cap_extra), inst.d_idx, dtype=torch.float16, device=dev)
+            if inst.kidx.shape[0]:
+                self.kidx[: inst.kidx.shape[0]] = _dev(inst.kidx, dev)
             self.q_idx = _dev(inst.q_idx, dev)
             self.sel = torch.full((self.topk,), -1, dtype=torch.int32, device=dev)
             self.sel_n = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -136,6 +140,45 @@ class DecodeLayer:
         for name, args in self._step_calls():
             getattr(ds4a, name)(*args, stream=stream)
         return self.out
+
+    def advance(self, k, v, q, q_idx=None, kidx_row=None, stream=None):
+        """Decode the next token: position p + 1.
+
+        Appends the token's K and V (device [D] or [1, D] fp16) to the raw window
+        ring, in slot (p + 1) % W, overwriting the token that leaves the window;
+        takes the step's query q [H, D] and, on an indexer layer, its indexer query
+        q_idx [d_idx]; then runs step() at the new position.  On an indexer layer a
+        step that completes a block (p + 2 a multiple of the ratio) makes a new
+        compressed row visible to its own query, so the row's indexer key kidx_row
+        [d_idx] is required then.  The copies are stream-ordered device copies on
+        `stream`, issued before the step's kernels.  Calls marshalled by bind()
+        keep the position they were bound at: bind again after advancing.
+        """
+        p = self.p + 1
+        n_vis = (p + 1) // self.ratio if self.ratio else 0
+        if self.ratio and n_vis > self.comp_k.shape[0]:
+            raise ValueError(f"advance: row {n_vis - 1} is past the compressed-row capacity {self.comp_k.shape[0]}")
+        completes = bool(self.ratio) and (p + 1) % self.ratio == 0
+        if self.topk:
+            if q_idx is None:
+                raise ValueError("advance: an indexer layer needs the step's indexer query")
+            if completes and kidx_row is None:
+                raise ValueError(f"advance: position {p} completes row {n_vis - 1}, whose indexer key is required")
+            if n_vis > self.kidx.shape[0]:
+                raise ValueError("advance: past the indexer-key capacity")
+        cur = torch.cuda.current_stream(self.q.device) if stream is None else stream
+        slot = p % self.W
+        with torch.cuda.stream(cur):
+            self.ring_k[slot].copy_(k.reshape(-1), non_blocking=True)
+            self.ring_v[slot].copy_(v.reshape(-1), non_blocking=True)
+            self.q.copy_(q.reshape(self.q.shape), non_blocking=True)
+            if self.topk:
+                self.q_idx.copy_(q_idx.reshape(-1), non_blocking=True)
+                if completes:
+                    self.kidx[n_vis - 1].copy_(kidx_row.reshape(-1), non_blocking=True)
+        self.p, self.slot, self.n_vis = p, slot, n_vis
+        self.n_win = min(self.W, p + 1)
+        return self.step(stream=stream)
 
     def bind(self, stream=None):
         """The decode step marshalled once (the layer's tensors are persistent): a

@@ -98,6 +98,53 @@ def time_graph(g: torch.cuda.CUDAGraph, reps: int, stream: torch.cuda.Stream) ->
     return start.elapsed_time(end)
 
 
+class L2Flush:
+    """A device buffer of twice the L2 size; flush() overwrites it on a stream, which
+    evicts whatever the L2 held (the write allocates every line)."""
+
+    def __init__(self, device=None):
+        dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.nbytes = 2 * l2
+        self.buf = torch.empty(self.nbytes // 4, dtype=torch.int32, device=dev)
+        self.n = 0
+
+    def flush(self, stream: torch.cuda.Stream):
+        with torch.cuda.stream(stream):
+            self.n += 1
+            self.buf.fill_(self.n)
+
+
+def time_graph_samples(g: torch.cuda.CUDAGraph, samples: int, stream: torch.cuda.Stream,
+                       flush: "L2Flush | None" = None, replays: int = 1) -> list:
+    """Milliseconds of each of `samples` timed regions, each `replays` back-to-back
+    replays of g, timed with CUDA events on `stream`.  With `flush`, the L2 is
+    overwritten on the same stream before each region and outside it; the flush also
+    keeps the GPU busy while the host enqueues the region, so no launch gap is timed."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(samples)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            if flush is not None:
+                flush.flush(stream)
+            a.record(stream)
+            for _ in range(replays):
+                g.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def spread(ms: list) -> dict:
+    """Median and spread of a list of sample times (ms)."""
+    xs = sorted(ms)
+    n = len(xs)
+
+    def q(f):
+        return xs[min(n - 1, max(0, int(round(f * (n - 1)))))]
+    return {"median": statistics.median(xs), "min": xs[0], "p10": q(0.1), "p90": q(0.9), "max": xs[-1], "n": n}
+
+
 def time_each(fn, n: int, stream: torch.cuda.Stream) -> float:
     """Average milliseconds of fn(t) over n calls, each bracketed by events on `stream`."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]

@@ -61,6 +61,19 @@ const char *ds4a_status_str(int status);
 int ds4a_last_device_error(void *stream);
 
 /*
+ * ds4a_test_set_wait_limit -- TEST HOOK, not part of the attention path; the
+ * pages have no counterpart.  With limit_ns > 0, every decode attention launch
+ * enqueued afterwards by this process (ds4a_attn_decode,
+ * ds4a_compress_attn_decode) makes CTA 0 of its cluster, once every partial sent
+ * to it has arrived, also wait on a barrier that nothing completes.  That wait
+ * gives up after limit_ns, records DS4A_ERR_TIMEOUT in the device error word and
+ * the launch finishes with its normal output, so a test can drive the bounded
+ * wait's give-up path without any fault.  0 (the default) turns it off.
+ * Returns DS4A_ERR_ARG for a limit outside 0 .. 10 s.
+ */
+int ds4a_test_set_wait_limit(long long limit_ns);
+
+/*
  * ds4a_compress_append -- feed n_new tokens to the KV compressor of one layer.
  * ("DS4 (DwarfStar 4)", Key Techniques, "KV attention compression": rolling
  * score/KV state, pooled rows appended at ratio boundaries.)

@@ -201,3 +201,10 @@ def test_binding_refuses_host_tensors(ds4a_lib):
     ws = torch.zeros(4096, dtype=torch.uint8)
     with pytest.raises(ValueError, match="CUDA tensor"):
         ds4a_lib.ds4a_indexer_topk_compress(qi, kidx, 19, 4, 16, sel, None, ws, tok, tok, w, state, comp, comp)
+
+
+def test_wait_limit_hook_validation(ds4a_lib):
+    L = ds4a_lib.lib()
+    assert L.ds4a_test_set_wait_limit(-1) == ARG
+    assert L.ds4a_test_set_wait_limit(20_000_000_000) == ARG
+    assert L.ds4a_test_set_wait_limit(0) == 0
