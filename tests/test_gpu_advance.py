@@ -104,3 +104,70 @@ def test_decode_advance_across_ring_wraps(H, D, W, ratio, d_idx, topk, p0, S):
     ring_k = L.ring_k.cpu().numpy()
     for t in range(p_last - W + 1, p_last + 1):
         assert np.array_equal(ring_k[t % W], raw_k[t]), t
+
+
+def test_restore_mid_block_continues_bit_for_bit():
+    """A snapshot taken between two steps in the middle of a compressor block (both the
+    ratio-4 and the ratio-128 block open), restored into freshly built layers, must
+    continue exactly as the uninterrupted run: the same kept rows, outputs, pooled
+    rows and compressor state, bit for bit.  ("DS4 (DwarfStar 4)", Key Techniques,
+    "KV cache with disk as first-class citizen": snapshots carry the raw window rows
+    and the compressor/indexer frontiers.)"""
+    from compressed_sparse_mqa_gb300 import snapshot
+    H, D, W, d_idx, p0, S1, S2 = 64, 128, 128, 128, 3000, 141, 150
+    assert (p0 + S1 + 1) % 4 and (p0 + S1 + 1) % 128          # mid-block at the snapshot
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    specs = [(0, 0), (4, 512), (128, 0)]                       # window only, indexer layer, ratio 128
+    hist = [_history(11 + i, H, D, W, r if r else 4, d_idx, k, p0, S1 + S2) for i, (r, k) in enumerate(specs)]
+
+    def build():
+        out = []
+        for (r, k), (raw_k, raw_v, kidx, q, q_idx, w) in zip(specs, hist):
+            if r == 0:
+                inst = synth.DecodeInstance(H=H, D=D, window=W, ratio=0, d_idx=d_idx, topk=0, p=p0,
+                                            pooled_history=False, raw_pos0=0, raw_k=raw_k[: p0 + 1],
+                                            raw_v=raw_v[: p0 + 1], comp_k=np.zeros((0, D), np.float16),
+                                            comp_v=np.zeros((0, D), np.float16), kidx=np.zeros((0, d_idx), np.float16),
+                                            q=q[0], q_idx=np.zeros(0, np.float16), w=w)
+            else:
+                inst = _instance(p0, H, D, W, r, d_idx, k, raw_k, raw_v, kidx, q[0], q_idx[0] if k else q_idx[0], w)
+            out.append(DecodeLayer(inst, cap_extra=(S1 + S2) // (r if r else 4) + 2))
+        return out
+
+    def run(layers, s_from, s_to, record):
+        for s in range(s_from, s_to):
+            p = p0 + s
+            for L, (r, k), (raw_k, raw_v, kidx, q, q_idx, w), d in zip(layers, specs, hist, devs):
+                n_vis = (p + 1) // r if r else 0
+                completes = bool(r) and (p + 1) % r == 0
+                L.advance(d[0][p], d[1][p], d[3][s], d[4][s] if k else None,
+                          d[2][n_vis - 1] if (k and completes) else None)
+                if record is not None:
+                    record.append(L.out.clone())
+                    if k:
+                        record.append(L.sel.clone())
+
+    devs = [(dev(a), dev(b), dev(c), dev(e), dev(f)) for a, b, c, e, f, _ in hist]
+    A = build()
+    for L in A:
+        L.step()
+    run(A, 1, S1 + 1, None)
+    blob = snapshot.snapshot(A)
+    rec_a = []
+    run(A, S1 + 1, S1 + S2 + 1, rec_a)
+    B = build()
+    snapshot.restore(blob, B)
+    assert [L.p for L in B] == [p0 + S1] * 3
+    rec_b = []
+    run(B, S1 + 1, S1 + S2 + 1, rec_b)
+    torch.cuda.synchronize()
+    assert len(rec_a) == len(rec_b) and rec_a
+    for i, (x, y) in enumerate(zip(rec_a, rec_b)):
+        assert torch.equal(x, y), f"record {i} differs after restore"
+    for La, Lb in zip(A, B):
+        assert torch.equal(La.state, Lb.state)
+        if La.ratio:
+            n = (La.p + 1) // La.ratio
+            assert torch.equal(La.comp_k[:n], Lb.comp_k[:n]) and torch.equal(La.comp_v[:n], Lb.comp_v[:n])
+    from compressed_sparse_mqa_gb300 import ds4a
+    assert ds4a.ds4a_last_device_error() == 0
