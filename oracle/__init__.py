@@ -52,6 +52,11 @@ def lib():
         L.orc_pool_block.restype = None
         L.orc_compress_range.argtypes = [_D, _D, _L, _L, ctypes.c_int, _D, ctypes.c_int, _L, _L, _D, _D]
         L.orc_compress_range.restype = _L
+        L.orc_pool_block_keys.argtypes = [_D, _D, ctypes.c_int, ctypes.c_int, ctypes.c_int, _D, _D]
+        L.orc_pool_block_keys.restype = None
+        L.orc_compress_range_keys.argtypes = [_D, _D, _L, _L, ctypes.c_int, ctypes.c_int, _D, ctypes.c_int, _L, _L,
+                                              _D]
+        L.orc_compress_range_keys.restype = _L
         L.orc_index_scores.argtypes = [_D, _D, _L, ctypes.c_int, _D]
         L.orc_index_scores.restype = None
         L.orc_topk.argtypes = [_D, _L, ctypes.c_int, _I]
@@ -114,6 +119,31 @@ def compress_range(raw_k, raw_v, raw_pos0: int, w, r: int, b0: int, b1: int):
     if rc < 0:
         raise ValueError("compress_range: a block reaches outside the raw rows given")
     return ok, ov
+
+
+def pool_block_keys(k, ki, w):
+    """Pooled indexer key of one block: the block's softmax weights of w . k_t applied
+    to the tokens' indexer keys ki [n, DI]."""
+    k, ki, w = _f64(k), _f64(ki), _f64(w)
+    n, D = k.shape
+    DI = ki.shape[1]
+    out = np.zeros(DI)
+    lib().orc_pool_block_keys(_dp(k), _dp(ki), n, D, DI, _dp(w), _dp(out))
+    return out
+
+
+def compress_range_keys(raw_k, raw_ki, raw_pos0: int, w, r: int, b0: int, b1: int):
+    """Pooled indexer keys of blocks b0..b1-1 (float64 [b1-b0, DI]) from the raw tokens'
+    K rows and indexer keys at positions raw_pos0.."""
+    raw_k, raw_ki, w = _f64(raw_k), _f64(raw_ki), _f64(w)
+    n_raw, D = raw_k.shape
+    DI = raw_ki.shape[1]
+    out = np.zeros((max(b1 - b0, 0), DI))
+    rc = lib().orc_compress_range_keys(_dp(raw_k), _dp(raw_ki), raw_pos0, n_raw, D, DI, _dp(w), r, b0, b1,
+                                       _dp(out))
+    if rc < 0:
+        raise ValueError("compress_range_keys: a block reaches outside the raw rows given")
+    return out
 
 
 def index_scores(q, kidx):

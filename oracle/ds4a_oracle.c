@@ -115,6 +115,47 @@ long orc_compress_range(const double *raw_k, const double *raw_v, long raw_pos0,
     return b1 - b0;
 }
 
+/* ---- [KVC], the pooled-key reading of R3 ----------------------------------
+ * In the alternative reading of where an indexer key comes from, the compressor
+ * pools per-token indexer keys with the block's own weights: the key of block b
+ * is sum_t alpha_t ki_t with alpha = softmax over the block of w . k_t (the
+ * same alpha as orc_pool_block). */
+void orc_pool_block_keys(const double *k, const double *ki, int n, int D, int DI,
+                         const double *w, double *out_ki)
+{
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    double smax = -INFINITY;
+    for (int t = 0; t < n; ++t) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += w[d] * k[(size_t)t * D + d];
+        s[t] = acc;
+        if (acc > smax) smax = acc;
+    }
+    double z = 0.0;
+    for (int t = 0; t < n; ++t) z += exp(s[t] - smax);
+    for (int c = 0; c < DI; ++c) out_ki[c] = 0.0;
+    for (int t = 0; t < n; ++t) {
+        double a = exp(s[t] - smax) / z;
+        for (int c = 0; c < DI; ++c) out_ki[c] += a * ki[(size_t)t * DI + c];
+    }
+    free(s);
+}
+
+/* Pooled keys of blocks b0 .. b1-1 (rows as orc_compress_range); -1 if a block
+ * reaches outside the raw rows given. */
+long orc_compress_range_keys(const double *raw_k, const double *raw_ki, long raw_pos0, long n_raw,
+                             int D, int DI, const double *w, int r, long b0, long b1, double *out_ki)
+{
+    if (r <= 0 || b1 < b0) return -1;
+    for (long b = b0; b < b1; ++b) {
+        long first = b * r - raw_pos0;
+        if (first < 0 || first + r > n_raw) return -1;
+        orc_pool_block_keys(raw_k + (size_t)first * D, raw_ki + (size_t)first * DI, r, D, DI, w,
+                            out_ki + (size_t)(b - b0) * DI);
+    }
+    return b1 - b0;
+}
+
 /* ---- [KVC] + R3/R4/R10/R11: the indexer ----------------------------------- */
 
 /* score_j = q . kidx_j in double, for j = 0 .. n-1 */

@@ -116,6 +116,49 @@ def test_compress_range_offsets_and_bounds():
         oracle.compress_range(k[13:], v[13:], 13, w, r, 3, 10)   # block 3 starts at 12
 
 
+# ---- pooled indexer keys (the compressor pooling per-token indexer keys) -------
+
+def test_pooled_keys_ratio_one_is_identity():
+    k, ki, w = f16((21, 16)), f16((21, 24)), rng.standard_normal(16)
+    assert np.array_equal(oracle.compress_range_keys(k, ki, 0, w, 1, 0, 21), ki.astype(np.float64))
+
+
+@pytest.mark.parametrize("r", [4, 128])
+def test_pooled_keys_zero_weights_give_block_mean(r):
+    k, ki = f16((2 * r, 16)), f16((2 * r, 40))
+    got = oracle.compress_range_keys(k, ki, 0, np.zeros(16), r, 0, 2)
+    assert np.array_equal(got, ki.astype(np.float64).reshape(2, r, 40).mean(axis=1))
+
+
+def test_pooled_keys_two_token_closed_form():
+    k = np.array([[0.0, 2.0], [1.0, -4.0]])
+    ki = np.array([[5.0, -1.0, 0.25], [1.0, 3.0, -0.5]])
+    got = oracle.pool_block_keys(k, ki, np.array([1.0, 0.0]))
+    a1 = 1.0 / (1.0 + math.exp(-1.0))
+    np.testing.assert_allclose(got, (1 - a1) * ki[0] + a1 * ki[1], rtol=1e-15, atol=1e-15)
+
+
+def test_pooled_keys_use_the_library_softmax_of_the_k_scores():
+    # the weights come from w . k_t, not from the indexer keys: a library softmax of the
+    # K scores applied to the indexer keys
+    r, D, DI = 4, 16, 8
+    k, ki, w = f16((6 * r, D)), f16((6 * r, DI)), rng.standard_normal(D)
+    got = oracle.compress_range_keys(k, ki, 0, w, r, 0, 6)
+    K = torch.tensor(k.astype(np.float64)).view(6, r, D)
+    KI = torch.tensor(ki.astype(np.float64)).view(6, r, DI)
+    a = torch.softmax(K @ torch.tensor(w), dim=1)
+    np.testing.assert_allclose(got, (a[..., None] * KI).sum(1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_pooled_keys_offsets_and_bounds():
+    r, D, DI = 4, 8, 16
+    k, ki, w = f16((40, D)), f16((40, DI)), rng.standard_normal(D)
+    full = oracle.compress_range_keys(k, ki, 0, w, r, 0, 10)
+    assert np.array_equal(oracle.compress_range_keys(k[12:], ki[12:], 12, w, r, 3, 10), full[3:])
+    with pytest.raises(ValueError):
+        oracle.compress_range_keys(k[13:], ki[13:], 13, w, r, 3, 10)
+
+
 # ---- indexer ------------------------------------------------------------------
 
 def test_index_scores_on_orthonormal_keys():
