@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the C3/C4/C5 sub-results")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["c3", "c4", "c5"], default=None,
+    ap.add_argument("--only", choices=["c3", "c4", "c5", "prefill_stack"], default=None,
                     help="run one sub-configuration alone and print its result (for profiling)")
     return ap.parse_args()
 
@@ -183,7 +183,8 @@ def run_ours(args, rank, world, local):
     if args.only:
         fn = {"c3": lambda: sub_decode(configs.C3, l2, stream, hbm_peak, flush),
               "c4": lambda: sub_prefill(configs.C4, stream, peaks, flush),
-              "c5": lambda: sub_stack(l2, stream, hbm_peak, flush)}[args.only]
+              "c5": lambda: sub_stack(l2, stream, hbm_peak, flush),
+              "prefill_stack": lambda: sub_prefill_stack(stream, peaks, flush)}[args.only]
         return {"only": args.only, "result": fn()}
 
     # ---- headline: C2 decode step --------------------------------------------------------
@@ -253,8 +254,10 @@ def run_ours(args, rank, world, local):
     sub = {}
     if not args.no_sub:
         sub["c3_decode_ratio128_ctx131072"] = sub_decode(configs.C3, l2, stream, hbm_peak, flush)
+        sub["c2_pooled_indexer_keys"] = sub_decode(configs.C2_POOLED, l2, stream, hbm_peak, flush)
         sub["c4_prefill_2048_ratio4"] = sub_prefill(configs.C4, stream, peaks, flush)
         sub["c5_stack_43_layers_ctx65536"] = sub_stack(l2, stream, hbm_peak, flush)
+        sub["prefill_stack_43_layers_2048_after_30720"] = sub_prefill_stack(stream, peaks, flush)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -402,6 +405,32 @@ def sub_prefill(params, stream, peaks, flush):
             "peak": f"{peak} TFLOP/s dense bf16 burst, measured (fp16 runs at the same rate)",
             "flops_per_chunk": C4_FLOPS,
             "timed": "graph of 2 chunks (2 copies), L2 flushed before each of 10 regions, median"}
+
+
+def sub_prefill_stack(stream, peaks, flush):
+    """One 2048-token chunk through all 43 layers (window only, ratio 4 + indexer,
+    ratio 128), every layer's state resident; the flops are the algorithmic flops of
+    every layer's indexer GEMM and attention."""
+    import torch
+
+    from compressed_sparse_mqa_gb300 import configs, timing
+    from compressed_sparse_mqa_gb300.layer import PrefillStack
+    insts = configs.prefill_stack()
+    flops = sum(configs.prefill_flops(i) for i in insts)
+    stack = PrefillStack(insts)
+    with torch.cuda.stream(stream):
+        stack.step()
+    torch.cuda.synchronize()
+    g, reps = timed_graph(lambda t: stack.step(), 1, stream)
+    sp = timing.spread(sampled(g, reps, 1, 8, stream, flush))
+    s = sp["median"] / 1e3
+    tflops = flops / s / 1e12
+    sus = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
+    return {"tokens_per_s": round(insts[0].T / s, 1), "ms_per_chunk_43_layers": round(s * 1e3, 3),
+            "tflops": round(tflops, 2), "tensor_frac_sustained": round(tflops / sus, 4),
+            "peak": f"{sus} TFLOP/s dense bf16 sustained, measured (fp16 runs at the same rate)",
+            "flops_per_chunk": flops, "prefix_tokens": insts[0].P, "chunk_tokens": insts[0].T,
+            "timed": "graph of one chunk through 43 layers, L2 flushed before each of 8 regions, median"}
 
 
 def sub_stack(l2, stream, hbm_peak, flush):

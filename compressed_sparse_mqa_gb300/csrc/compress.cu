@@ -75,9 +75,9 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(CompressArgs a) {
 
 cudaError_t launch_compress(const uint16_t *k, const uint16_t *v, int n_new, int D, const float *w,
                             int ratio, long long pos, float *state, uint16_t *comp_k,
-                            uint16_t *comp_v, const Ctx &c) {
+                            uint16_t *comp_v, const Ctx &c, const uint16_t *ki, uint16_t *comp_ki, int DI) {
     if (n_new <= 0) return cudaSuccess;
-    if (ratio > kMaxRatio || D > kMaxD) return cudaErrorInvalidValue;
+    if (ratio > kMaxRatio || D > kMaxD || DI > kMaxD) return cudaErrorInvalidValue;
     const long long end = pos + n_new;
     const long long b_first = pos / ratio, b_last = (end - 1) / ratio;
     const bool first_open = (pos % ratio) != 0;
@@ -94,7 +94,7 @@ cudaError_t launch_compress(const uint16_t *k, const uint16_t *v, int n_new, int
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    CompressArgs a{k, v, w, state, comp_k, comp_v, pos, n_new, D, ratio};
+    CompressArgs a{k, v, w, state, comp_k, comp_v, pos, n_new, D, ratio, ki, comp_ki, ki ? DI : 0};
     return launch(compress_kernel, dim3(static_cast<unsigned>(1 + n_fc)), dim3(kThreads), 0, c, 1, a);
 }
 

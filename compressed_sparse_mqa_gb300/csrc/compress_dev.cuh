@@ -5,8 +5,11 @@
 // "DS4 (DwarfStar 4)", Key Techniques, "KV attention compression": pooled row of
 // block b = sum_t a_t [k_t ; v_t], a = softmax_t(w . k_t); the running state of
 // the open block is (m, l, acc_k[D], acc_v[D]): running max of the scores, sum of
-// exp(s - m), and the exp(s - m)-weighted sums of K and V.  NT: threads of the
-// calling block (every thread calls these routines: they synchronise the block).
+// exp(s - m), and the exp(s - m)-weighted sums of K and V.  With per-token indexer
+// keys (ki != nullptr) the same weights also pool them into the block's indexer
+// key, and the state carries their weighted sum too: (m, l, acc_k[D], acc_v[D],
+// acc_ki[DI]).  NT: threads of the calling block (every thread calls these
+// routines: they synchronise the block).
 #pragma once
 
 #include "ds4a_common.cuh"
@@ -28,6 +31,9 @@ struct CompressArgs {
     int n_new;
     int D;
     int ratio;
+    const uint16_t *ki = nullptr;   // [n_new, DI] per-token indexer keys, or nullptr
+    uint16_t *comp_ki = nullptr;    // [cap, DI] pooled indexer keys
+    int DI = 0;
 };
 
 // Scores s_i = w . k_i of tokens [t0, t1) into s_w: one warp per token, lanes
@@ -102,6 +108,16 @@ __device__ void pool_segment(const CompressArgs &a, long long b, long long t0, l
         } else {
             a.state[2 + d] = ak;
             a.state[2 + D + d] = av;
+        }
+    }
+    if (a.ki != nullptr) {   // the indexer keys, pooled with the same weights
+        const int DI = a.DI;
+        const uint16_t *ib = a.ki + (t0 - a.pos) * DI;
+        for (int d = tid; d < DI; d += NT) {
+            float ai = resume ? c_old * a.state[2 + 2 * D + d] : 0.f;
+            for (int i = 0; i < n; ++i) ai = fmaf(s_w[i], h2f(ib[static_cast<size_t>(i) * DI + d]), ai);
+            if (closes) a.comp_ki[b * DI + d] = f2h(ai * (1.f / l));
+            else a.state[2 + 2 * D + d] = ai;
         }
     }
     if (!closes && tid == 0) { a.state[0] = m_new; a.state[1] = l; }

@@ -125,6 +125,25 @@ int ds4a_compress_append(const uint16_t *k, const uint16_t *v, int n_new, int he
                                            comp_v, c));
 }
 
+int ds4a_compress_append_keys(const uint16_t *k, const uint16_t *v, const uint16_t *k_idx_tok, int n_new,
+                              int head_dim, int d_idx, const float *score_w, int ratio, long long pos, float *state,
+                              uint16_t *comp_k, uint16_t *comp_v, uint16_t *comp_kidx, long long cap, void *stream) {
+    if (n_new < 0 || pos < 0 || cap < 0 || ratio < 1) return DS4A_ERR_ARG;
+    if (head_dim < 8 || head_dim > 256 || head_dim % 8 != 0 || ratio > 1024) return DS4A_ERR_UNSUPPORTED;
+    if (d_idx < 8 || d_idx > 256 || d_idx % 8 != 0) return DS4A_ERR_UNSUPPORTED;
+    if (n_new == 0) return DS4A_OK;
+    if (!k || !v || !k_idx_tok || !score_w || !state || !comp_k || !comp_v || !comp_kidx) return DS4A_ERR_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_idx_tok, 16) || !aligned(score_w, 4) ||
+        !aligned(state, 4) || !aligned(comp_k, 2) || !aligned(comp_v, 2) || !aligned(comp_kidx, 2))
+        return DS4A_ERR_ARG;
+    if ((pos + n_new) / ratio > cap) return DS4A_ERR_CAPACITY;
+    ds4a::Ctx c;
+    int rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    return from_cuda(ds4a::launch_compress(k, v, n_new, head_dim, score_w, ratio, pos, state, comp_k, comp_v, c,
+                                           k_idx_tok, comp_kidx, d_idx));
+}
+
 size_t ds4a_indexer_workspace_bytes(int n_q, long long n_rows, int k) {
     if (n_q < 0 || n_rows < 0) return 0;
     return ds4a::indexer_ws_bytes(n_q, n_rows, k);

@@ -14,9 +14,11 @@ struct Ctx {
     bool pdl;            // launch with programmatic stream serialization
 };
 
+// ki/comp_ki/DI: per-token indexer keys pooled with the same weights (ki = nullptr: none)
 cudaError_t launch_compress(const uint16_t *k, const uint16_t *v, int n_new, int D, const float *w,
                             int ratio, long long pos, float *state, uint16_t *comp_k,
-                            uint16_t *comp_v, const Ctx &c);
+                            uint16_t *comp_v, const Ctx &c, const uint16_t *ki = nullptr,
+                            uint16_t *comp_ki = nullptr, int DI = 0);
 
 size_t indexer_ws_bytes(int n_q, long long n_rows, int k);
 

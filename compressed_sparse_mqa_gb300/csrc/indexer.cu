@@ -325,11 +325,12 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     const long long n_vis = visible_rows(a, 0);
     const long long j0 = static_cast<long long>(blockIdx.x) * rows_per_cta;
     const long long j1 = min(n_vis, j0 + rows_per_cta);
-    // The query and the key rows are inputs no kernel of this library writes, so the
-    // first kStagedRows rows of the slice are scored into shared memory before
-    // waiting on the previous kernel; only the workspace and the output (which the
-    // previous kernel may still be using) are written after the wait.
-    const long long js = min(j1, j0 + kStagedRows);
+    // The query and the key rows complete before the query's token (j < floor(q_pos/ratio))
+    // are inputs the kernel just ahead does not write, so up to kStagedRows of those rows
+    // of the slice are scored into shared memory before waiting on the previous kernel.
+    // A row the query's own token completes (which a compressor call just ahead may
+    // write), the workspace and the output are read or written after the wait.
+    const long long js = max(j0, min(min(j1, j0 + kStagedRows), a.q_pos0 / a.ratio));
     float qf[2][8];
     load_query(a.q_idx, a.d_idx, qf);
     for (long long base = j0; base < js; base += kRowsPerCta) {

@@ -40,6 +40,7 @@ struct TcScoreArgs {
     float *tile_kmax2; // [n_ntiles] largest squared key norm of each 256-row tile
     unsigned int *err;
     long long n_rows;
+    long long early_rows;   // key rows below this may be read before the dependency wait
     int n_q;
     int ld;
     int n_ntiles;
@@ -88,10 +89,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
             else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
         }
     };
-    // key rows are cache state: the first tile is fetched before waiting on the previous kernel
-    if (n_my > 0) load_b(0, 0);
+    // key rows complete before the chunk are cache state: the first tile is fetched before
+    // waiting on the previous kernel when all of its rows are (later rows may be written by
+    // the compressor call just ahead of this one)
+    const bool early = n_my > 0 && static_cast<long long>(ns + 1) * kTN <= a.early_rows;
+    if (early) load_b(0, 0);
     pdl_wait();
     pdl_trigger();
+    if (n_my > 0 && !early) load_b(0, 0);
     for (int i = tid; i < kTM * kChunks; i += kGemmThreads) {
         const int r = i / kChunks, c = i % kChunks;
         unsigned char *dst = sa + (c >> 3) * (kTM * 128) + tc::sw128_chunk(r, c & 7);
@@ -440,6 +445,7 @@ cudaError_t launch_indexer_prefill_tc(const uint16_t *q_idx, int n_q, const uint
     g.tile_kmax2 = tile_kmax2;
     g.err = c.err;
     g.n_rows = n_rows;
+    g.early_rows = q_pos0 / ratio;
     g.n_q = n_q;
     g.ld = ld;
     g.n_ntiles = ld / kTN;

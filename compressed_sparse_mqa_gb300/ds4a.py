@@ -29,7 +29,7 @@ DS4A_ERR_DEVICE_INDEX = 7
 EXPORTED = ["ds4a_status_str", "ds4a_last_device_error", "ds4a_compress_append",
             "ds4a_indexer_topk", "ds4a_indexer_workspace_bytes", "ds4a_attn_decode",
             "ds4a_attn_prefill", "ds4a_indexer_topk_compress", "ds4a_compress_attn_decode",
-            "ds4a_indexer_topk_noalloc", "ds4a_test_set_wait_limit"]
+            "ds4a_indexer_topk_noalloc", "ds4a_test_set_wait_limit", "ds4a_compress_append_keys"]
 
 
 class Ds4aError(RuntimeError):
@@ -52,6 +52,7 @@ def lib() -> ctypes.CDLL:
         L.ds4a_indexer_topk_noalloc.argtypes = [P, P, LL, I, LL, I, I, P, P, P]
         L.ds4a_compress_append.argtypes = [P, P, I, I, P, I, LL, P, P, P, LL, P]
         L.ds4a_indexer_topk.argtypes = [P, I, P, LL, I, LL, I, I, P, P, P, SZ, P]
+        L.ds4a_compress_append_keys.argtypes = [P, P, P, I, I, I, P, I, LL, P, P, P, P, LL, P]
         L.ds4a_indexer_topk_compress.argtypes = [P, P, LL, I, LL, I, I, P, P, P, SZ, P, P, I, P, P, P, P, LL, P]
         L.ds4a_compress_attn_decode.argtypes = [P, P, P, I, LL, P, P, P, LL, P, I, I, P, P, I, F, P, P]
         L.ds4a_indexer_workspace_bytes.argtypes = [I, LL, I]
@@ -122,6 +123,45 @@ def ds4a_compress_append(k, v, score_w, ratio: int, pos: int, state, comp_k, com
     _check(rc, "ds4a_compress_append")
 
 
+def _marshal_compress_append_keys(k, v, ki, score_w, ratio: int, pos: int, state, comp_k, comp_v, comp_kidx,
+                                  stream=None):
+    n_new, D = k.shape
+    DI = ki.shape[1]
+    if v.shape != k.shape or ki.shape[0] != n_new or comp_k.shape != comp_v.shape or comp_k.shape[1] != D:
+        raise ValueError("compress_append_keys: shape mismatch")
+    if comp_kidx.shape[0] != comp_k.shape[0] or comp_kidx.shape[1] != DI:
+        raise ValueError("compress_append_keys: pooled-key rows must match the compressed rows")
+    if state.numel() < 2 + 2 * D + DI or score_w.numel() != D:
+        raise ValueError("compress_append_keys: state / score_w size")
+    return (_ptr(k, torch.float16, "k"), _ptr(v, torch.float16, "v"), _ptr(ki, torch.float16, "ki"), n_new, D, DI,
+            _ptr(score_w, torch.float32, "score_w"), ratio, pos, _ptr(state, torch.float32, "state"),
+            _ptr(comp_k, torch.float16, "comp_k"), _ptr(comp_v, torch.float16, "comp_v"),
+            _ptr(comp_kidx, torch.float16, "comp_kidx"), comp_k.shape[0], _stream(stream))
+
+
+def ds4a_compress_append_keys(k, v, ki, score_w, ratio: int, pos: int, state, comp_k, comp_v, comp_kidx,
+                              stream=None):
+    """ds4a_compress_append that also pools the tokens' indexer keys ki [n_new, DI] into
+    comp_kidx [cap, DI] with the same weights; state [2 + 2D + DI] fp32."""
+    args = _marshal_compress_append_keys(k, v, ki, score_w, ratio, pos, state, comp_k, comp_v, comp_kidx, stream)
+    _check(lib().ds4a_compress_append_keys(*args), "ds4a_compress_append_keys")
+
+
+def _marshal_indexer_topk(q_idx, k_idx, q_pos0: int, ratio: int, k: int, out_idx, out_n, ws, n_rows=None,
+                          stream=None):
+    q2 = q_idx if q_idx.dim() == 2 else q_idx.view(1, -1)
+    n_q, d = q2.shape
+    rows = k_idx.shape[0] if n_rows is None else n_rows
+    if k_idx.shape[0] < rows or (k_idx.numel() and k_idx.shape[1] != d):
+        raise ValueError("indexer_topk: k_idx shape")
+    if out_idx.numel() < n_q * k:
+        raise ValueError("indexer_topk: out_idx too small")
+    return (_ptr(q2, torch.float16, "q_idx"), n_q, _ptr(k_idx, torch.float16, "k_idx") if k_idx.numel() else None,
+            rows, d, q_pos0, ratio, k, _ptr(out_idx, torch.int32, "out_idx"),
+            _ptr(out_n, torch.int32, "out_n", optional=True), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+            _stream(stream))
+
+
 def ds4a_indexer_workspace_bytes(n_q: int, n_rows: int, k: int) -> int:
     return int(lib().ds4a_indexer_workspace_bytes(n_q, n_rows, k))
 
@@ -130,19 +170,8 @@ def ds4a_indexer_topk(q_idx, k_idx, q_pos0: int, ratio: int, k: int, out_idx, ou
                       stream=None):
     """q_idx [n_q, d] fp16, k_idx [n_rows, d] fp16 -> out_idx [n_q, k] int32 (ascending, -1 pad),
     out_n [n_q] int32 (or None).  ws: uint8 tensor of ds4a_indexer_workspace_bytes bytes."""
-    q2 = q_idx if q_idx.dim() == 2 else q_idx.view(1, -1)
-    n_q, d = q2.shape
-    rows = k_idx.shape[0] if n_rows is None else n_rows
-    if k_idx.shape[0] < rows or (k_idx.numel() and k_idx.shape[1] != d):
-        raise ValueError("indexer_topk: k_idx shape")
-    if out_idx.numel() < n_q * k:
-        raise ValueError("indexer_topk: out_idx too small")
-    rc = lib().ds4a_indexer_topk(_ptr(q2, torch.float16, "q_idx"), n_q,
-                                 _ptr(k_idx, torch.float16, "k_idx") if k_idx.numel() else None, rows, d,
-                                 q_pos0, ratio, k, _ptr(out_idx, torch.int32, "out_idx"),
-                                 _ptr(out_n, torch.int32, "out_n", optional=True),
-                                 _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
-    _check(rc, "ds4a_indexer_topk")
+    args = _marshal_indexer_topk(q_idx, k_idx, q_pos0, ratio, k, out_idx, out_n, ws, n_rows, stream)
+    _check(lib().ds4a_indexer_topk(*args), "ds4a_indexer_topk")
 
 
 def _marshal_indexer_topk_compress(q_idx, k_idx, q_pos: int, ratio: int, k: int, out_idx, out_n, ws, k_new, v_new,
@@ -241,6 +270,8 @@ def ds4a_attn_prefill(q, raw_k, raw_v, n_prior: int, window: int, comp_k, comp_v
 
 
 _MARSHAL = {"ds4a_attn_decode": _marshal_attn_decode,
+            "ds4a_indexer_topk": _marshal_indexer_topk,
+            "ds4a_compress_append_keys": _marshal_compress_append_keys,
             "ds4a_compress_attn_decode": _marshal_compress_attn_decode,
             "ds4a_indexer_topk_compress": _marshal_indexer_topk_compress}
 

@@ -68,7 +68,10 @@ class DecodeLayer:
         self.n_win = len(pos)
         self.q = _dev(inst.q, dev)
         self.w = _dev(inst.w, dev)
-        self.state = torch.zeros(2 + 2 * D, dtype=torch.float32, device=dev)
+        # pooled keys: the compressor also pools per-token indexer keys into the rows' keys
+        self.pooled_keys = getattr(inst, "kidx_tok", None) is not None and inst.topk > 0
+        d_state = 2 + 2 * D + (inst.d_idx if self.pooled_keys else 0)
+        self.state = torch.zeros(d_state, dtype=torch.float32, device=dev)
         self.out = torch.empty(self.H, D, dtype=torch.float16, device=dev)
         self.n_vis = (p + 1) // self.ratio if self.ratio else 0
         if self.ratio:
@@ -79,13 +82,6 @@ class DecodeLayer:
             if n_given:
                 self.comp_k[:n_given] = _dev(inst.comp_k, dev)
                 self.comp_v[:n_given] = _dev(inst.comp_v, dev)
-            # feed the compressor every raw token before p that it has not seen
-            first = 0 if inst.pooled_history else (p // self.ratio) * self.ratio
-            if p > first:
-                hk = _dev(inst.raw_k[first - inst.raw_pos0: p - inst.raw_pos0], dev)
-                hv = _dev(inst.raw_v[first - inst.raw_pos0: p - inst.raw_pos0], dev)
-                ds4a.ds4a_compress_append(hk, hv, self.w, self.ratio, first, self.state,
-                                          self.comp_k, self.comp_v)
         else:
             self.comp_k = self.comp_v = None
         if self.topk:
@@ -101,6 +97,21 @@ class DecodeLayer:
             self.ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
         else:
             self.kidx = self.q_idx = self.sel = self.sel_n = self.ws = None
+        self.ki_tok = None
+        if self.pooled_keys:
+            self.ki_tok = _dev(inst.kidx_tok[p - inst.raw_pos0: p - inst.raw_pos0 + 1], dev)   # token p's key
+        if self.ratio:
+            # feed the compressor every raw token before p that it has not seen
+            first = 0 if inst.pooled_history else (p // self.ratio) * self.ratio
+            if p > first:
+                a, b = first - inst.raw_pos0, p - inst.raw_pos0
+                hk, hv = _dev(inst.raw_k[a:b], dev), _dev(inst.raw_v[a:b], dev)
+                if self.pooled_keys:
+                    ds4a.ds4a_compress_append_keys(hk, hv, _dev(inst.kidx_tok[a:b], dev), self.w, self.ratio, first,
+                                                   self.state, self.comp_k, self.comp_v, self.kidx)
+                else:
+                    ds4a.ds4a_compress_append(hk, hv, self.w, self.ratio, first, self.state, self.comp_k,
+                                              self.comp_v)
         self.slot = p % W
 
     def clone(self) -> "DecodeLayer":
@@ -125,6 +136,8 @@ class DecodeLayer:
         if self.topk:
             b += self.n_vis * self.kidx.shape[1] * 2 + self.kidx.shape[1] * 2  # indexer keys, query
             b += self.topk * 4 * 2 + 4                          # kept indices written, read back
+        if self.pooled_keys:
+            b += self.kidx.shape[1] * (2 + 4)                   # the token's indexer key; its state
         return b
 
     def step(self, stream=None):
@@ -141,7 +154,7 @@ class DecodeLayer:
             getattr(ds4a, name)(*args, stream=stream)
         return self.out
 
-    def advance(self, k, v, q, q_idx=None, kidx_row=None, stream=None):
+    def advance(self, k, v, q, q_idx=None, kidx_row=None, stream=None, ki_tok=None):
         """Decode the next token: position p + 1.
 
         Appends the token's K and V (device [D] or [1, D] fp16) to the raw window
@@ -162,7 +175,9 @@ class DecodeLayer:
         if self.topk:
             if q_idx is None:
                 raise ValueError("advance: an indexer layer needs the step's indexer query")
-            if completes and kidx_row is None:
+            if self.pooled_keys and ki_tok is None:
+                raise ValueError("advance: a layer that pools its indexer keys needs the token's key")
+            if completes and kidx_row is None and not self.pooled_keys:
                 raise ValueError(f"advance: position {p} completes row {n_vis - 1}, whose indexer key is required")
             if n_vis > self.kidx.shape[0]:
                 raise ValueError("advance: past the indexer-key capacity")
@@ -174,7 +189,9 @@ class DecodeLayer:
             self.q.copy_(q.reshape(self.q.shape), non_blocking=True)
             if self.topk:
                 self.q_idx.copy_(q_idx.reshape(-1), non_blocking=True)
-                if completes:
+                if self.pooled_keys:
+                    self.ki_tok.copy_(ki_tok.reshape(self.ki_tok.shape), non_blocking=True)
+                elif completes:
                     self.kidx[n_vis - 1].copy_(kidx_row.reshape(-1), non_blocking=True)
         self.p, self.slot, self.n_vis = p, slot, n_vis
         self.n_win = min(self.W, p + 1)
@@ -197,6 +214,15 @@ class DecodeLayer:
         new_k = self.ring_k[self.slot: self.slot + 1]
         new_v = self.ring_v[self.slot: self.slot + 1]
         win_k, win_v = self.ring_k[: self.n_win], self.ring_v[: self.n_win]
+        if self.pooled_keys:
+            # the compressor writes the key of a row this token completes before the indexer
+            # ranks it: three launches in stream order
+            return [("ds4a_compress_append_keys", (new_k, new_v, self.ki_tok, self.w, self.ratio, self.p, self.state,
+                                                   self.comp_k, self.comp_v, self.kidx)),
+                    ("ds4a_indexer_topk", (self.q_idx, self.kidx, self.p, self.ratio, self.topk, self.sel,
+                                           self.sel_n, self.ws)),
+                    ("ds4a_attn_decode", (self.q, win_k, win_v, self.comp_k, self.comp_v, self.sel, self.topk,
+                                          self.scale, self.out))]
         if self.topk:
             return [("ds4a_indexer_topk_compress", (self.q_idx, self.kidx, self.p, self.ratio, self.topk, self.sel,
                                                     self.sel_n, self.ws, new_k, new_v, self.w, self.state, self.comp_k,
@@ -263,3 +289,19 @@ class PrefillLayer:
         ds4a.ds4a_attn_prefill(self.q, self.raw_k, self.raw_v, self.n_prior, self.W, self.comp_k, self.comp_v,
                                self.sel, self.P, self.ratio, self.scale, self.out, stream=stream)
         return self.out
+
+
+class PrefillStack:
+    """One prefill chunk through a stack of layers, each with its own schedule
+    (layer_schedule: window only, ratio 4 + indexer top-512, ratio 128) and its own
+    device state.  "DS4 (DwarfStar 4)", Architecture, "Whole-model graph execution":
+    prefill runs the model's layers over chunks of tokens (2048 by default)."""
+
+    def __init__(self, instances, device="cuda"):
+        self.layers = [PrefillLayer(inst, device) for inst in instances]
+
+    def step(self, stream=None):
+        """Every layer's compress_append -> indexer_topk -> attn_prefill, layer after layer."""
+        for L in self.layers:
+            L.step(stream=stream)
+        return [L.out for L in self.layers]

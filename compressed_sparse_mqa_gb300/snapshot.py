@@ -22,9 +22,11 @@ and outputs, not state.
 
 Blob layout (little-endian): a 16-byte header "DS4ASNAP", u32 version, u32
 layer count; then per layer a 64-byte record header (seven i32: ratio, topk, H,
-D, W, d_idx, reserved; then i64 p, i64 n_rows; zero padding) followed by the
-arrays, each padded to a 16-byte multiple: ring K, ring V (fp16), state (fp32),
-compressed K, compressed V (fp16), indexer keys (fp16, indexer layers only).
+D, W, d_idx, pooled (1 when the layer's compressor pools indexer keys, whose
+weighted sum then extends the state by d_idx floats); then i64 p, i64 n_rows;
+zero padding) followed by the arrays, each padded to a 16-byte multiple: ring K,
+ring V (fp16), state (fp32), compressed K, compressed V (fp16), indexer keys
+(fp16, indexer layers only).
 """
 from __future__ import annotations
 
@@ -67,6 +69,10 @@ def _arrays(L):
     return n_rows, [a.detach().contiguous().cpu().numpy() for a in arrs]
 
 
+def _pooled(L) -> bool:
+    return bool(getattr(L, "pooled_keys", False))
+
+
 def snapshot(layers) -> bytes:
     """One blob holding the decode state of every layer (DecodeLayer objects, or any
     objects with the same fields).  Reads the device state after the current stream's
@@ -77,7 +83,7 @@ def snapshot(layers) -> bytes:
     for L in layers:
         n_rows, arrs = _arrays(L)
         d_idx = L.kidx.shape[1] if L.topk else 0
-        rec = _REC.pack(L.ratio, L.topk, L.H, L.D, L.W, d_idx, 0, L.p, n_rows)
+        rec = _REC.pack(L.ratio, L.topk, L.H, L.D, L.W, d_idx, int(_pooled(L)), L.p, n_rows)
         parts.append(rec + b"\0" * (_REC_BYTES - len(rec)))
         for a in arrs:
             b = a.tobytes()
@@ -114,17 +120,17 @@ def restore(blob: bytes, layers) -> None:
     plan = []
     for i, L in enumerate(layers):
         rec, off = _take(blob, off, _REC_BYTES)
-        ratio, topk, H, D, W, d_idx, _, p, n_rows = _REC.unpack_from(rec, 0)
-        mine = (L.ratio, L.topk, L.H, L.D, L.W, L.kidx.shape[1] if L.topk else 0)
-        if (ratio, topk, H, D, W, d_idx) != mine:
-            raise SnapshotError(f"snapshot: layer {i} is (ratio, topk, H, D, W, d_idx) = "
-                                f"{(ratio, topk, H, D, W, d_idx)}, the target is {mine}")
+        ratio, topk, H, D, W, d_idx, pooled, p, n_rows = _REC.unpack_from(rec, 0)
+        mine = (L.ratio, L.topk, L.H, L.D, L.W, L.kidx.shape[1] if L.topk else 0, int(_pooled(L)))
+        if (ratio, topk, H, D, W, d_idx, pooled) != mine:
+            raise SnapshotError(f"snapshot: layer {i} is (ratio, topk, H, D, W, d_idx, pooled) = "
+                                f"{(ratio, topk, H, D, W, d_idx, pooled)}, the target is {mine}")
         if p < 0 or n_rows != ((p + 1) // ratio if ratio else 0):
             raise SnapshotError(f"snapshot: layer {i} row count {n_rows} does not match position {p}")
         if ratio and (n_rows > L.comp_k.shape[0] or (topk and n_rows > L.kidx.shape[0])):
             raise SnapshotError(f"snapshot: layer {i} has {n_rows} rows, more than the target's capacity")
         specs = [(L.ring_k, (W, D), np.float16), (L.ring_v, (W, D), np.float16),
-                 (L.state, (2 + 2 * D,), np.float32)]
+                 (L.state, (2 + 2 * D + (d_idx if pooled else 0),), np.float32)]
         if ratio:
             specs += [(L.comp_k, (n_rows, D), np.float16), (L.comp_v, (n_rows, D), np.float16)]
         if topk:

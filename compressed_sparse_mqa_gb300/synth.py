@@ -29,6 +29,8 @@ GOLDEN = 0x9E3779B97F4A7C15
 
 # one stream per tensor kind
 T_Q, T_KRAW, T_VRAW, T_COMPK, T_COMPV, T_KIDX, T_QIDX, T_W = 1, 2, 3, 4, 5, 6, 7, 8
+# per-token indexer keys (the reading in which the compressor pools them into the rows' keys)
+T_KIDX_TOK = 9
 
 
 def _mix_scalar(z: int) -> int:
@@ -103,7 +105,11 @@ class DecodeInstance:
                  (given data), or empty when `pooled_history` is set, in which
                  case raw_k/raw_v hold every position 0 .. p and the rows come
                  from running the compressor over them.
-    kidx [n_vis, d_i] fp16: one indexer key per compressed row visible to p.
+    kidx [n_vis, d_i] fp16: one indexer key per compressed row visible to p; with
+                 pooled keys, the keys of the given rows only.
+    kidx_tok [n_raw, d_i] fp16 or None: with pooled keys, the indexer key of every
+                 raw token (positions raw_pos0 .. p), which the compressor pools into
+                 the keys of the rows they complete.
     q [H, D] fp16, q_idx [d_i] fp16, w [D] fp32 (compressor score weights).
     """
     H: int
@@ -123,6 +129,7 @@ class DecodeInstance:
     q: np.ndarray
     q_idx: np.ndarray
     w: np.ndarray
+    kidx_tok: "np.ndarray | None" = None
     meta: dict = field(default_factory=dict)
 
     @property
@@ -132,11 +139,13 @@ class DecodeInstance:
 
 def decode_instance(*, seed: int, layer: int, H: int, D: int, window: int, ratio: int,
                     d_idx: int, topk: int, p: int, pooled_history: bool = False,
-                    sigma_w: float = 1.0) -> DecodeInstance:
+                    sigma_w: float = 1.0, pooled_keys: bool = False) -> DecodeInstance:
     """Draw the inputs of one decode step (all values N(0,1) except w ~ N(0, sigma_w^2)).
 
     ratio == 0 means a raw-window-only layer (no compressed rows, no indexer);
-    topk == 0 means no indexer (every visible compressed row is attended).
+    topk == 0 means no indexer (every visible compressed row is attended);
+    pooled_keys: the rows' indexer keys are pooled from per-token keys (drawn for
+    every raw token), and only the given rows' keys are drawn directly.
     """
     if pooled_history:
         raw_pos0 = 0
@@ -150,14 +159,16 @@ def decode_instance(*, seed: int, layer: int, H: int, D: int, window: int, ratio
     raw_v = normal_f16(seed, layer, T_VRAW, (n_raw, D))
     comp_k = normal_f16(seed, layer, T_COMPK, (n_given, D))
     comp_v = normal_f16(seed, layer, T_COMPV, (n_given, D))
-    kidx = normal_f16(seed, layer, T_KIDX, (n_vis if topk > 0 else 0, d_idx))
+    n_keys = (n_given if pooled_keys else n_vis) if topk > 0 else 0
+    kidx = normal_f16(seed, layer, T_KIDX, (n_keys, d_idx))
+    kidx_tok = normal_f16(seed, layer, T_KIDX_TOK, (n_raw, d_idx)) if (pooled_keys and topk > 0) else None
     q = normal_f16(seed, layer, T_Q, (H, D))
     q_idx = normal_f16(seed, layer, T_QIDX, (d_idx if topk > 0 else 0,))
     w = normal_f32(seed, layer, T_W, (D,), sigma_w)
     return DecodeInstance(H=H, D=D, window=window, ratio=ratio, d_idx=d_idx, topk=topk,
                           p=p, pooled_history=pooled_history, raw_pos0=raw_pos0,
                           raw_k=raw_k, raw_v=raw_v, comp_k=comp_k, comp_v=comp_v,
-                          kidx=kidx, q=q, q_idx=q_idx, w=w)
+                          kidx=kidx, q=q, q_idx=q_idx, w=w, kidx_tok=kidx_tok)
 
 
 @dataclass
@@ -196,11 +207,21 @@ class PrefillInstance:
 
 
 def prefill_instance(*, seed: int, layer: int, H: int, D: int, window: int, ratio: int,
-                     d_idx: int, topk: int, P: int, T: int, sigma_w: float = 1.0) -> PrefillInstance:
+                     d_idx: int, topk: int, P: int, T: int, sigma_w: float = 1.0,
+                     queries=None) -> PrefillInstance:
+    """Draw the inputs of one prefill chunk.  `queries`, if given, is a (q, q_idx) pair
+    drawn once elsewhere (several layers fed the same chunk of queries); q_idx is
+    dropped on a layer without an indexer."""
     # enough prefix tokens for the raw window and for the compressor's open block
     n_prior = min(P, max(window - 1, P % ratio if ratio > 0 else 0))
     n_given = P // ratio if ratio > 0 else 0
     n_vis_end = (P + T) // ratio if ratio > 0 else 0
+    if queries is None:
+        q = normal_f16(seed, layer, T_Q, (T, H, D))
+        q_idx = normal_f16(seed, layer, T_QIDX, (T, d_idx) if topk > 0 else (T, 0))
+    else:
+        q, q_idx = queries
+        q_idx = q_idx if topk > 0 else np.zeros((T, 0), np.float16)
     return PrefillInstance(
         H=H, D=D, window=window, ratio=ratio, d_idx=d_idx, topk=topk, P=P, T=T, n_prior=n_prior,
         raw_k=normal_f16(seed, layer, T_KRAW, (n_prior + T, D)),
@@ -208,7 +229,11 @@ def prefill_instance(*, seed: int, layer: int, H: int, D: int, window: int, rati
         comp_k=normal_f16(seed, layer, T_COMPK, (n_given, D)),
         comp_v=normal_f16(seed, layer, T_COMPV, (n_given, D)),
         kidx=normal_f16(seed, layer, T_KIDX, (n_vis_end if topk > 0 else 0, d_idx)),
-        q=normal_f16(seed, layer, T_Q, (T, H, D)),
-        q_idx=normal_f16(seed, layer, T_QIDX, (T, d_idx) if topk > 0 else (T, 0)),
+        q=q, q_idx=q_idx,
         w=normal_f32(seed, layer, T_W, (D,), sigma_w),
     )
+
+
+def chunk_queries(seed: int, T: int, H: int, D: int, d_idx: int):
+    """One draw of a chunk's attention and indexer queries (stream of layer 0)."""
+    return normal_f16(seed, 0, T_Q, (T, H, D)), normal_f16(seed, 0, T_QIDX, (T, d_idx))

@@ -33,6 +33,17 @@
  *     row index out of range, a bounded wait that gave up) do not fail the
  *     call; the kernel skips the access and records the first such error in
  *     a per-device error word read by ds4a_last_device_error.
+ *   - Launch order: kernels are launched with programmatic dependent launch.
+ *     A kernel may start once the kernel ahead of it on the stream has started
+ *     its own dependent phase, reads a few named inputs early (each call lists
+ *     them: cache state such as key rows and window rows, and its queries), and
+ *     waits for the kernel ahead to finish before it reads anything else or
+ *     writes anything.  So the kernel directly ahead on the stream must not
+ *     write those early inputs.  The calls of this library never write another
+ *     call's early inputs; a kernel that does not use programmatic launch
+ *     finishes before the next call starts.  With the environment variable
+ *     DS4A_PDL=0 (read once per process) every kernel waits for the kernel
+ *     ahead before it starts.
  */
 #ifndef DS4A_H
 #define DS4A_H
@@ -96,11 +107,36 @@ int ds4a_test_set_wait_limit(long long limit_ns);
  *              floor(pos/ratio) .. floor((pos+n_new)/ratio)-1 are written.
  *   cap        rows allocated; DS4A_ERR_CAPACITY if the last row written
  *              would be >= cap.
- * n_new = 0 is a no-op.
+ * n_new = 0 is a no-op.  Early reads: k and score_w.
  */
 int ds4a_compress_append(const uint16_t *k, const uint16_t *v, int n_new, int head_dim,
                          const float *score_w, int ratio, long long pos, float *state,
                          uint16_t *comp_k, uint16_t *comp_v, long long cap, void *stream);
+
+/*
+ * ds4a_compress_append_keys -- ds4a_compress_append that also pools per-token
+ * indexer keys: each compressed row's indexer key is the same softmax-weighted
+ * sum over the block, sum_t a_t kidx_t, with a = softmax over the block of
+ * score_w . k_t.  ("DS4 (DwarfStar 4)", Key Techniques, "KV attention
+ * compression": the compressor keeps a rolling score/KV state and appends pooled
+ * rows at ratio boundaries, and the ratio-4 layers rank those rows with a
+ * learned indexer.  The pages do not say where an indexer key comes from; this
+ * call is the reading in which the compressor pools it from per-token keys, the
+ * alternative to ds4a_indexer_topk's caller-supplied key per row.)
+ *
+ *   Arguments as ds4a_compress_append, and:
+ *   k_idx_tok  [n_new, d_idx] fp16: the indexer keys of tokens pos .. pos+n_new-1.
+ *   d_idx      multiple of 8, 8 .. 256.
+ *   state      [2 + 2*head_dim + d_idx] float: the state of ds4a_compress_append
+ *              followed by the open block's weighted indexer-key sum.
+ *   comp_kidx  [cap, d_idx] fp16: pooled indexer keys, row j beside comp_k's row j.
+ * The pooled K and V rows are the same bits ds4a_compress_append writes.  An
+ * ds4a_indexer_topk call may follow it directly on the stream: the indexer reads
+ * the key rows this call can write only after the call has finished.
+ */
+int ds4a_compress_append_keys(const uint16_t *k, const uint16_t *v, const uint16_t *k_idx_tok, int n_new,
+                              int head_dim, int d_idx, const float *score_w, int ratio, long long pos, float *state,
+                              uint16_t *comp_k, uint16_t *comp_v, uint16_t *comp_kidx, long long cap, void *stream);
 
 /*
  * ds4a_indexer_topk -- rank compressed rows for n_q queries and keep the top k.
@@ -123,6 +159,11 @@ int ds4a_compress_append(const uint16_t *k, const uint16_t *v, int n_new, int he
  *              zero-filled by the caller once before its first use (the call
  *              leaves its counters at zero again).  Calls that share one
  *              workspace must be stream-ordered.
+ * Early reads (see "Launch order" above): the queries and the key rows
+ * j < floor(q_pos0 / ratio), the rows complete before the first query's token.
+ * Key rows from floor(q_pos0 / ratio) on, which a compressor call for the same
+ * tokens may write (ds4a_compress_append_keys), are read only after the kernel
+ * ahead has finished.
  */
 int ds4a_indexer_topk(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
                       int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
@@ -148,6 +189,7 @@ size_t ds4a_indexer_workspace_bytes(int n_q, long long n_rows, int k);
  *   Compressor arguments as ds4a_compress_append with n_new = 1 and pos = q_pos
  *   (k_new, v_new: [1, head_dim] fp16, the token at position q_pos).
  *   Errors: the union of the two calls' checks; nothing is enqueued on error.
+ *   Early reads: the union of the two calls' early reads.
  */
 int ds4a_indexer_topk_compress(const uint16_t *q_idx, const uint16_t *k_idx, long long n_rows, int d_idx,
                                long long q_pos, int ratio, int k, int32_t *out_idx, int32_t *out_n, void *ws,
@@ -202,6 +244,7 @@ int ds4a_indexer_topk_noalloc(const uint16_t *q_idx, const uint16_t *k_idx, long
  *   scale      softmax scale, 1/sqrt(D) in the model.
  *   out        [H, D] fp16.
  *   ws, ws_bytes  unused by this kernel design (pass NULL, 0); reserved.
+ * Early reads: q and up to 64 window rows.
  */
 int ds4a_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
                      const uint16_t *win_v, int n_win, const uint16_t *comp_k,
@@ -225,6 +268,7 @@ int ds4a_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
  *   (k_new, v_new: [1, D] fp16, the token at position pos).
  *   Attention arguments as ds4a_attn_decode; the window must hold the token at pos.
  *   Errors: the union of the two calls' checks; nothing is enqueued on error.
+ *   Early reads: k_new, score_w, q and up to 64 window rows.
  */
 int ds4a_compress_attn_decode(const uint16_t *k_new, const uint16_t *v_new, const float *score_w, int ratio,
                               long long pos, float *state, uint16_t *comp_k, uint16_t *comp_v, long long cap,
@@ -249,6 +293,7 @@ int ds4a_compress_attn_decode(const uint16_t *k_new, const uint16_t *v_new, cons
  *   sel        [T, k_stride] int32 (as written by ds4a_indexer_topk), or NULL.
  *   out        [T, H, D] fp16.
  *   ws, ws_bytes  unused by this kernel design (pass NULL, 0); reserved.
+ * Early reads: none.
  */
 int ds4a_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *raw_k,
                       const uint16_t *raw_v, int n_prior, int window, const uint16_t *comp_k,

@@ -220,7 +220,9 @@ def decode_step(inst) -> dict:
 
     Order: the current token enters the compressor (a block it completes becomes
     visible: append-then-attend), the indexer ranks the visible rows, then one
-    softmax runs over the raw window and the kept (or all) compressed rows.
+    softmax runs over the raw window and the kept (or all) compressed rows.  With
+    per-token indexer keys (inst.kidx_tok), rows past the given keys are ranked
+    by the keys pooled from their tokens' keys.
     Returns out [H, D] float64, sel (ascending kept rows, or None), the pooled
     rows (float64) and the number of visible rows.
     """
@@ -239,7 +241,14 @@ def decode_step(inst) -> dict:
                 nk, nv = compress_range(inst.raw_k, inst.raw_v, inst.raw_pos0, inst.w, r, n_given, n_vis)
                 ck, cv = np.concatenate([ck, nk]), np.concatenate([cv, nv])
         if inst.topk > 0:
-            idx, n = indexer(inst.q_idx[None, :], inst.kidx, p, r, inst.topk)
+            kidx = inst.kidx
+            ki_tok = getattr(inst, "kidx_tok", None)
+            if ki_tok is not None and n_vis > kidx.shape[0]:
+                # pooled keys: the rows past the given ones take the keys the compressor
+                # pools from their tokens' indexer keys, with the same weights as K and V
+                pk = compress_range_keys(inst.raw_k, ki_tok, inst.raw_pos0, inst.w, r, kidx.shape[0], n_vis)
+                kidx = np.concatenate([_f64(kidx).reshape(-1, pk.shape[1]), pk])
+            idx, n = indexer(inst.q_idx[None, :], kidx, p, r, inst.topk)
             sel = idx[0, : n[0]]
     n_sel = (len(sel) if sel is not None else n_vis)
     out = decode_attend(inst.q, p, inst.window, inst.raw_k, inst.raw_v, inst.raw_pos0,
