@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the C3/C4/C5 sub-results")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["c3", "c4", "c5", "prefill_stack"], default=None,
+    ap.add_argument("--only", choices=["c3", "c4", "c5", "prefill_stack", "batched16", "batched64"], default=None,
                     help="run one sub-configuration alone and print its result (for profiling)")
     return ap.parse_args()
 
@@ -184,7 +184,9 @@ def run_ours(args, rank, world, local):
         fn = {"c3": lambda: sub_decode(configs.C3, l2, stream, hbm_peak, flush),
               "c4": lambda: sub_prefill(configs.C4, stream, peaks, flush),
               "c5": lambda: sub_stack(l2, stream, hbm_peak, flush),
-              "prefill_stack": lambda: sub_prefill_stack(stream, peaks, flush)}[args.only]
+              "prefill_stack": lambda: sub_prefill_stack(stream, peaks, flush),
+              "batched16": lambda: sub_batched(16, l2, stream, hbm_peak, flush),
+              "batched64": lambda: sub_batched(64, l2, stream, hbm_peak, flush)}[args.only]
         return {"only": args.only, "result": fn()}
 
     # ---- headline: C2 decode step --------------------------------------------------------
@@ -255,6 +257,8 @@ def run_ours(args, rank, world, local):
     if not args.no_sub:
         sub["c3_decode_ratio128_ctx131072"] = sub_decode(configs.C3, l2, stream, hbm_peak, flush)
         sub["c2_pooled_indexer_keys"] = sub_decode(configs.C2_POOLED, l2, stream, hbm_peak, flush)
+        sub["batched_decode_16_sessions_c2"] = sub_batched(16, l2, stream, hbm_peak, flush)
+        sub["batched_decode_64_sessions_c2"] = sub_batched(64, l2, stream, hbm_peak, flush)
         sub["c4_prefill_2048_ratio4"] = sub_prefill(configs.C4, stream, peaks, flush)
         sub["c5_stack_43_layers_ctx65536"] = sub_stack(l2, stream, hbm_peak, flush)
         sub["prefill_stack_43_layers_2048_after_30720"] = sub_prefill_stack(stream, peaks, flush)
@@ -405,6 +409,35 @@ def sub_prefill(params, stream, peaks, flush):
             "peak": f"{peak} TFLOP/s dense bf16 burst, measured (fp16 runs at the same rate)",
             "flops_per_chunk": C4_FLOPS,
             "timed": "graph of 2 chunks (2 copies), L2 flushed before each of 10 regions, median"}
+
+
+def sub_batched(B, l2, stream, hbm_peak, flush):
+    """B independent C2-shaped sessions (ratio-4 layer + indexer, context 32768, each
+    session its own seeded cache) decoded together: one batched indexer launch and one
+    batched attention launch per step."""
+    import torch
+
+    from compressed_sparse_mqa_gb300 import configs, timing
+    from compressed_sparse_mqa_gb300.layer import BatchedDecodeLayer
+    import dataclasses
+    insts = [configs.decode(dict(configs.C2, seed=s)) for s in range(B)]
+    insts = [dataclasses.replace(i, w=insts[0].w) for i in insts]   # one layer: shared score weights
+    base = BatchedDecodeLayer(insts)
+    b = base.bytes_touched()
+    R = rotation_copies(b, l2, minimum=2)
+    layers = [base] + [base.clone() for _ in range(R - 1)]
+    with torch.cuda.stream(stream):
+        for L in layers:
+            L.step()
+    torch.cuda.synchronize()
+    K = R
+    g, reps = timed_graph(lambda t: layers[t % R].step(), K, stream)
+    sp = timing.spread(sampled(g, reps, K, 30, stream, flush))
+    s = sp["median"] / 1e3
+    return {"sessions": B, "tokens_per_s": round(B / s, 1), "us_per_step": round(s * 1e6, 3),
+            "us_per_token_layer": round(s * 1e6 / B, 3), "bytes_per_step": b,
+            "hbm_gbs": round(b / s / 1e9, 1), "hbm_frac": round(b / s / 1e9 / hbm_peak, 4),
+            "timed": f"graph of {K} batched steps over {R} copies, L2 flushed before each of 30 regions, median"}
 
 
 def sub_prefill_stack(stream, peaks, flush):

@@ -516,6 +516,20 @@ struct DecodeArgs {
     int comp_rank;     // with the compressor: the CTA that runs its update (it attends the row it may write)
     int comp_first;    // the update completes a block: its row is written before that CTA attends
     long long test_wait_ns;   // > 0 (test hook only): CTA 0 also waits this long on a barrier nobody completes
+    // Batched decode: cluster blockIdx.y serves session s, whose inputs sit at fixed
+    // strides from session 0's and whose position is pos[s] (device memory, read early).
+    // The fields above are then session 0's pointers; the row counts, the window length
+    // and the compressor's CTA follow from each session's position.
+    const long long *pos;     // nullptr: one session, the fields above as given
+    long long q_stride;       // elements between the sessions' q and out
+    long long win_stride;     // elements between the sessions' window rings
+    long long comp_stride;    // elements between the sessions' compressed rows
+    long long sel_stride;     // entries between the sessions' kept-row lists
+    long long state_stride;   // floats between the sessions' compressor states
+    long long cap;            // compressed rows allocated per session
+    int W;                    // ring length: window rows min(W, p + 1), slot p % W holds token p
+    int ratio;                // 0: window only
+    int n_sel_list;           // with sel: entries per list (-1 entries are skipped)
 };
 
 constexpr int kRecvRows = 80;   // >= cluster size * ceil(H / cluster size) for H <= 64
@@ -583,6 +597,42 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a, cmp
     cg::cluster_group cluster = cg::this_cluster();
     const int cs = static_cast<int>(cluster.num_blocks());
     const int rank = static_cast<int>(cluster.block_rank());
+    if (a.pos != nullptr) {   // batched: this cluster's session
+        const long long sid = blockIdx.y;
+        const long long p = a.pos[sid];
+        a.q += sid * a.q_stride;
+        a.out += sid * a.q_stride;
+        a.src.wk += sid * a.win_stride;
+        a.src.wv += sid * a.win_stride;
+        a.src.ck += sid * a.comp_stride;
+        a.src.cv += sid * a.comp_stride;
+        if (a.src.sel) a.src.sel += sid * a.sel_stride;
+        a.src.n_w = static_cast<int>(p + 1 < a.W ? p + 1 : a.W);
+        long long n_sel = a.n_sel_list;
+        if (!a.src.sel) {   // every visible row
+            const long long nv = a.ratio > 0 ? (p + 1) / a.ratio : 0;
+            n_sel = nv < a.cap ? nv : a.cap;
+            a.src.n_comp = n_sel;
+        }
+        a.n_rows = a.src.n_w + static_cast<int>(n_sel);
+        if constexpr (kCompress) {
+            const long long slot = (p % a.W) * D;
+            ca.pos = p;
+            ca.k = a.src.wk + slot;
+            ca.v = a.src.wv + slot;
+            ca.state += sid * a.state_stride;
+            ca.comp_k += sid * a.comp_stride;
+            ca.comp_v += sid * a.comp_stride;
+            const int chunk = (a.n_rows + cs - 1) / cs;
+            a.comp_rank = (a.n_rows - 1) / chunk;
+            a.comp_first = (p + 1) % a.ratio == 0;
+            if ((p + 1) / a.ratio > a.cap) {
+                // the row this token completes is past the session's capacity: no update
+                a.comp_rank = -1;
+                if (rank == 0 && threadIdx.x == 0) record_error(a.src.err, DS4A_ERR_CAPACITY);
+            }
+        }
+    }
     // heads [hb, hb + nh) are merged here: every CTA of the cluster sends (O, m, l) of
     // each of them, a row of D + 4 floats (16-byte multiple), into this CTA's receive buffer
     const int hpc = (a.H + cs - 1) / cs;
@@ -828,7 +878,7 @@ cudaError_t launch_attn_decode(const uint16_t *q, int H, int D, const uint16_t *
                                const uint16_t *win_v, int n_win, const uint16_t *comp_k,
                                const uint16_t *comp_v, long long n_comp, const int32_t *sel,
                                int n_sel, float scale, uint16_t *out, const Ctx &c) {
-    DecodeArgs a;
+    DecodeArgs a{};
     a.q = q;
     a.out = out;
     a.src = RowSrc{win_k, win_v, comp_k, comp_v, sel, c.err, n_comp, n_win};
@@ -856,7 +906,7 @@ cudaError_t launch_compress_attn_decode(const uint16_t *k_new, const uint16_t *v
                                         uint16_t *comp_v, float scale, uint16_t *out, const Ctx &c) {
     if (ratio > cmp::kMaxRatio || D > cmp::kMaxD) return cudaErrorInvalidValue;
     const long long n_vis = (pos + 1) / ratio;   // every visible row, the one this step may complete included
-    DecodeArgs a;
+    DecodeArgs a{};
     a.q = q;
     a.out = out;
     a.src = RowSrc{win_k, win_v, comp_k, comp_v, nullptr, c.err, n_vis, n_win};
@@ -876,6 +926,48 @@ cudaError_t launch_compress_attn_decode(const uint16_t *k_new, const uint16_t *v
         return launch(attn_decode_kernel<128, true>, dim3(cluster), dim3(kThreads), decode_smem<128>(), c, cluster, a,
                       ca);
     return launch(attn_decode_kernel<64, true>, dim3(cluster), dim3(kThreads), decode_smem<64>(), c, cluster, a, ca);
+}
+
+cudaError_t launch_attn_decode_batched(int B, const uint16_t *q, int H, int D, const uint16_t *ring_k,
+                                       const uint16_t *ring_v, int W, const long long *pos, const uint16_t *comp_k,
+                                       const uint16_t *comp_v, long long cap, const int32_t *sel, int n_sel,
+                                       int ratio, float scale, uint16_t *out, const float *score_w, float *state,
+                                       const Ctx &c) {
+    if (state != nullptr && (ratio > cmp::kMaxRatio || D > cmp::kMaxD)) return cudaErrorInvalidValue;
+    DecodeArgs a{};
+    a.q = q;
+    a.out = out;
+    a.src = RowSrc{ring_k, ring_v, comp_k, comp_v, sel, c.err, cap, W};
+    a.H = H;
+    a.scale_log2 = scale * kLog2e;
+    a.comp_rank = -1;
+    a.test_wait_ns = test_wait_limit_ns();
+    a.pos = pos;
+    a.q_stride = static_cast<long long>(H) * D;
+    a.win_stride = static_cast<long long>(W) * D;
+    a.comp_stride = cap * D;
+    a.sel_stride = n_sel;
+    a.state_stride = 2 + 2LL * D;
+    a.cap = cap;
+    a.W = W;
+    a.ratio = ratio;
+    a.n_sel_list = sel ? n_sel : 0;
+    int cluster = 16;
+    cudaError_t e = D == 128 ? configure<128>(cluster) : configure<64>(cluster);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(cluster, B);
+    if (state != nullptr) {   // the compressor's update for each session's token, in the same launch
+        const cmp::CompressArgs ca{nullptr, nullptr, score_w, state, const_cast<uint16_t *>(comp_k),
+                                   const_cast<uint16_t *>(comp_v), 0, 1, D, ratio};
+        if (D == 128)
+            return launch(attn_decode_kernel<128, true>, grid, dim3(kThreads), decode_smem<128>(), c, cluster, a, ca);
+        return launch(attn_decode_kernel<64, true>, grid, dim3(kThreads), decode_smem<64>(), c, cluster, a, ca);
+    }
+    if (D == 128)
+        return launch(attn_decode_kernel<128, false>, grid, dim3(kThreads), decode_smem<128>(), c, cluster, a,
+                      cmp::CompressArgs{});
+    return launch(attn_decode_kernel<64, false>, grid, dim3(kThreads), decode_smem<64>(), c, cluster, a,
+                  cmp::CompressArgs{});
 }
 
 cudaError_t launch_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *raw_k,

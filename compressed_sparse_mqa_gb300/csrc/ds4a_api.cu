@@ -276,6 +276,98 @@ int ds4a_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *ra
                                                n_comp, sel, k_stride, q_pos0, ratio, scale, out, c));
 }
 
+// ---- batched decode: B independent sessions per call ------------------------------------
+
+size_t ds4a_decode_batched_workspace_bytes(int B, long long cap) {
+    if (B < 0 || cap < 0) return 0;
+    return static_cast<size_t>(B) * ds4a::indexer_batched_ws_stride(cap);
+}
+
+static int check_batch(int B, int W, long long cap, const long long *pos) {
+    if (B < 0 || cap < 0 || W < 1 || W > 4096) return DS4A_ERR_ARG;
+    if (B > 65535 || cap > 0x7fffffffLL) return DS4A_ERR_UNSUPPORTED;
+    if (B > 0 && (!pos || !aligned(pos, 8))) return DS4A_ERR_ARG;
+    return DS4A_OK;
+}
+
+int ds4a_indexer_topk_compress_batched(int B, const uint16_t *q_idx, const uint16_t *k_idx, long long cap,
+                                       int d_idx, const long long *pos, int ratio, int k, int32_t *out_idx,
+                                       int32_t *out_n, void *ws, size_t ws_bytes, const uint16_t *ring_k,
+                                       const uint16_t *ring_v, int W, int head_dim, const float *score_w,
+                                       float *state, uint16_t *comp_k, uint16_t *comp_v, void *stream) {
+    int rc = check_batch(B, W, cap, pos);
+    if (rc != DS4A_OK) return rc;
+    if (ratio < 1 || k < 1) return DS4A_ERR_ARG;
+    if (d_idx < 8 || d_idx > 256 || d_idx % 8 != 0 || k > 2048) return DS4A_ERR_UNSUPPORTED;
+    if (head_dim < 8 || head_dim > 256 || head_dim % 8 != 0 || ratio > 1024) return DS4A_ERR_UNSUPPORTED;
+    if (B == 0) return DS4A_OK;
+    if (!q_idx || !out_idx || (cap > 0 && !k_idx) || !ring_k || !ring_v || !score_w || !state || !comp_k ||
+        !comp_v)
+        return DS4A_ERR_ARG;
+    if (!aligned(q_idx, 16) || !aligned(k_idx, 16) || !aligned(out_idx, 4) || !aligned(out_n, 4) ||
+        !aligned(ring_k, 16) || !aligned(ring_v, 16) || !aligned(score_w, 4) || !aligned(state, 4) ||
+        !aligned(comp_k, 2) || !aligned(comp_v, 2))
+        return DS4A_ERR_ARG;
+    if (!ws || !aligned(ws, 256) || ws_bytes < ds4a_decode_batched_workspace_bytes(B, cap)) return DS4A_ERR_WORKSPACE;
+    ds4a::Ctx c;
+    rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    return from_cuda(ds4a::launch_indexer_compress_batched(B, q_idx, k_idx, cap, d_idx, pos, ratio, k, out_idx, out_n,
+                                                           ws, ring_k, ring_v, W, head_dim, score_w, state, comp_k,
+                                                           comp_v, c));
+}
+
+static int attn_batched_common(int B, const uint16_t *q, int H, int D, const uint16_t *ring_k, const uint16_t *ring_v,
+                               int W, const long long *pos, const uint16_t *comp_k, const uint16_t *comp_v,
+                               long long cap, int ratio, uint16_t *out) {
+    int rc = check_batch(B, W, cap, pos);
+    if (rc != DS4A_OK) return rc;
+    rc = check_heads(H, D);
+    if (rc != DS4A_OK) return rc;
+    if (ratio < 0) return DS4A_ERR_ARG;
+    if (ratio > 1024) return DS4A_ERR_UNSUPPORTED;
+    if (B > 0 && (!q || !ring_k || !ring_v || !out || (ratio > 0 && cap > 0 && (!comp_k || !comp_v))))
+        return DS4A_ERR_ARG;
+    if (!aligned(q, 4) || !aligned(ring_k, 16) || !aligned(ring_v, 16) || !aligned(comp_k, 16) ||
+        !aligned(comp_v, 16) || !aligned(out, 16))
+        return DS4A_ERR_ARG;
+    if (W + cap > 0x7fffffffLL) return DS4A_ERR_UNSUPPORTED;
+    return DS4A_OK;
+}
+
+int ds4a_attn_decode_batched(int B, const uint16_t *q, int H, int D, const uint16_t *ring_k, const uint16_t *ring_v,
+                             int W, const long long *pos, const uint16_t *comp_k, const uint16_t *comp_v,
+                             long long cap, const int32_t *sel, int n_sel, int ratio, float scale, uint16_t *out,
+                             void *stream) {
+    int rc = attn_batched_common(B, q, H, D, ring_k, ring_v, W, pos, comp_k, comp_v, cap, ratio, out);
+    if (rc != DS4A_OK) return rc;
+    if (n_sel < 0 || !aligned(sel, 4)) return DS4A_ERR_ARG;
+    if (sel && (n_sel > 0x7fffffff - W)) return DS4A_ERR_UNSUPPORTED;
+    if (B == 0) return DS4A_OK;
+    ds4a::Ctx c;
+    rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    return from_cuda(ds4a::launch_attn_decode_batched(B, q, H, D, ring_k, ring_v, W, pos, comp_k, comp_v, cap, sel,
+                                                      n_sel, ratio, scale, out, nullptr, nullptr, c));
+}
+
+int ds4a_compress_attn_decode_batched(int B, const float *score_w, int ratio, float *state, uint16_t *comp_k,
+                                      uint16_t *comp_v, long long cap, const uint16_t *q, int H, int D,
+                                      const uint16_t *ring_k, const uint16_t *ring_v, int W, const long long *pos,
+                                      float scale, uint16_t *out, void *stream) {
+    int rc = attn_batched_common(B, q, H, D, ring_k, ring_v, W, pos, comp_k, comp_v, cap, ratio, out);
+    if (rc != DS4A_OK) return rc;
+    if (ratio < 1) return DS4A_ERR_ARG;
+    if (B > 0 && (!score_w || !state || !comp_k || !comp_v)) return DS4A_ERR_ARG;
+    if (!aligned(score_w, 4) || !aligned(state, 4)) return DS4A_ERR_ARG;
+    if (B == 0) return DS4A_OK;
+    ds4a::Ctx c;
+    rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    return from_cuda(ds4a::launch_attn_decode_batched(B, q, H, D, ring_k, ring_v, W, pos, comp_k, comp_v, cap,
+                                                      nullptr, 0, ratio, scale, out, score_w, state, c));
+}
+
 }  // extern "C"
 
 // ---- indexer entry point that allocates nothing -------------------------------------------

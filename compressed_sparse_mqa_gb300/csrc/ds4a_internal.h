@@ -35,6 +35,21 @@ cudaError_t launch_indexer_compress(const uint16_t *q_idx, const uint16_t *k_idx
                                    const uint16_t *k_new, const uint16_t *v_new, int D, const float *score_w,
                                    float *state, uint16_t *comp_k, uint16_t *comp_v, const Ctx &c);
 
+// batched decode (B sessions, positions pos[B] in device memory): the indexer query
+// and the compressor update of each session's token; workspace bytes per session
+size_t indexer_batched_ws_stride(long long cap);
+cudaError_t launch_indexer_compress_batched(int B, const uint16_t *q_idx, const uint16_t *k_idx, long long cap,
+                                           int d_idx, const long long *pos, int ratio, int k, int32_t *out_idx,
+                                           int32_t *out_n, void *ws, const uint16_t *ring_k, const uint16_t *ring_v,
+                                           int W, int D, const float *score_w, float *state, uint16_t *comp_k,
+                                           uint16_t *comp_v, const Ctx &c);
+// batched decode attention; state != nullptr: with each session's compressor update
+cudaError_t launch_attn_decode_batched(int B, const uint16_t *q, int H, int D, const uint16_t *ring_k,
+                                       const uint16_t *ring_v, int W, const long long *pos, const uint16_t *comp_k,
+                                       const uint16_t *comp_v, long long cap, const int32_t *sel, int n_sel,
+                                       int ratio, float scale, uint16_t *out, const float *score_w, float *state,
+                                       const Ctx &c);
+
 // tensor-core prefill indexer (many queries): availability, workspace, launch
 bool indexer_prefill_tc_ok(int n_q, long long n_rows, int d_idx);
 size_t indexer_prefill_tc_ws_bytes(int n_q, long long n_rows);

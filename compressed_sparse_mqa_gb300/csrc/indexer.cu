@@ -302,16 +302,77 @@ DS4A_DEVINL void compress_one_token(const cmp::CompressArgs &c, float *s_w, floa
     cmp::pool_segment<kThreads>(c, b, c.pos, c.pos + 1, resume, s_w, s_red);
 }
 
-// one query: CTA b < n_score scores rows [b*rows_per_cta, (b+1)*rows_per_cta) in
-// 64-row slices; the last of them to finish selects.  With kCompress the grid has
-// one more CTA, which feeds the query's token to the layer's compressor: that
-// update reads nothing the selection writes and vice versa.
+// Rows [lo, hi) of a slice scored into keys[j - kbase], kDeep 64-row batches per
+// round: the loads of a round are all issued before any of them is scored, so a
+// CTA that covers many rows keeps kDeep x 16 KB of key rows in flight.
+constexpr int kDeep = 4;
+DS4A_DEVINL void score_rows(const IndexerArgs &a, const float (&qf)[2][8], long long lo, long long hi,
+                           uint32_t *keys, long long kbase) {
+    for (long long base = lo; base < hi; base += kDeep * kRowsPerCta) {
+        RowLoads L[kDeep];
+#pragma unroll
+        for (int u = 0; u < kDeep; ++u) load_rows(a.k_idx, a.d_idx, base + u * kRowsPerCta, hi, L[u]);
+#pragma unroll
+        for (int u = 0; u < kDeep; ++u) {
+            const long long bu = base + u * kRowsPerCta;
+            if (bu < hi) score_loaded(qf, L[u], bu, hi, keys + (bu - kbase));   // block-uniform
+        }
+    }
+}
+
+// The sessions of a batched decode step: session s's inputs sit at fixed strides
+// from session 0's and its position is pos[s] (device memory, read early).
+struct DecodeBatch {
+    const long long *pos;     // nullptr: one session, at IndexerArgs::q_pos0
+    long long q_stride;       // elements between the sessions' indexer queries
+    long long k_stride;       // elements between the sessions' indexer keys
+    long long out_stride;     // elements between the sessions' kept-row lists
+    long long ws_stride;      // bytes between the sessions' workspaces
+    const uint16_t *ring_k;   // compressor: the new token is slot pos % W of the session's ring
+    const uint16_t *ring_v;
+    long long ring_stride;    // elements between the sessions' rings
+    long long state_stride;   // floats between the sessions' compressor states
+    long long comp_stride;    // elements between the sessions' compressed rows
+    long long cap;            // compressed rows allocated per session
+    unsigned int *err;
+    int W;
+};
+
+// one query per session: CTA x < n_score scores rows [x*rows_per_cta, (x+1)*rows_per_cta)
+// in 64-row slices; the last of them to finish selects.  With kCompress the grid has
+// one more CTA per session, which feeds the query's token to the layer's compressor:
+// that update reads nothing the selection writes and vice versa.  blockIdx.y is the
+// session of a batched step.
 template <bool kCompress>
 __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs a, int rows_per_cta,
-                                                                     cmp::CompressArgs c) {
+                                                                     cmp::CompressArgs c, DecodeBatch bt) {
     __shared__ SelectSmem sm;
     __shared__ bool s_last;
     __shared__ uint32_t s_keys[kStagedRows];
+    if (bt.pos != nullptr) {
+        const long long sid = blockIdx.y;
+        const long long p = bt.pos[sid];
+        a.q_pos0 = p;
+        a.q_idx += sid * bt.q_stride;
+        a.k_idx += sid * bt.k_stride;
+        a.out_idx += sid * bt.out_stride;
+        if (a.out_n) a.out_n += sid;
+        a.ws += sid * bt.ws_stride;
+        if constexpr (kCompress) {
+            if (blockIdx.x == gridDim.x - 1 && (p + 1) / c.ratio > bt.cap) {
+                // the row this token completes is past the session's capacity: no update
+                if (threadIdx.x == 0) record_error(bt.err, DS4A_ERR_CAPACITY);
+                return;
+            }
+            const long long slot = (p % bt.W) * c.D;
+            c.pos = p;
+            c.k = bt.ring_k + sid * bt.ring_stride + slot;
+            c.v = bt.ring_v + sid * bt.ring_stride + slot;
+            c.state += sid * bt.state_stride;
+            c.comp_k += sid * bt.comp_stride;
+            c.comp_v += sid * bt.comp_stride;
+        }
+    }
     if constexpr (kCompress) {
         if (blockIdx.x == gridDim.x - 1) {
             static_assert(sizeof(sm.scan) >= kWarps * sizeof(float), "one float per warp");
@@ -333,22 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     const long long js = max(j0, min(min(j1, j0 + kStagedRows), a.q_pos0 / a.ratio));
     float qf[2][8];
     load_query(a.q_idx, a.d_idx, qf);
-    for (long long base = j0; base < js; base += kRowsPerCta) {
-        RowLoads L;
-        load_rows(a.k_idx, a.d_idx, base, js, L);
-        score_loaded(qf, L, base, js, s_keys + (base - j0));
-    }
+    score_rows(a, qf, j0, js, s_keys, j0);
     pdl_wait();
     pdl_trigger();
     unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws);
     uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + kWsHeader);
     __syncthreads();
     for (long long j = j0 + threadIdx.x; j < js; j += kThreads) keys[j] = s_keys[j - j0];
-    for (long long base = js; base < j1; base += kRowsPerCta) {
-        RowLoads L;
-        load_rows(a.k_idx, a.d_idx, base, j1, L);
-        score_loaded(qf, L, base, j1, keys + base);
-    }
+    score_rows(a, qf, js, j1, keys, 0);
     // one acquire-release atomic per CTA: releases this CTA's keys (ordered before it
     // by the barrier) and, for the last CTA, acquires everyone else's
     __syncthreads();
@@ -432,7 +485,7 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
         int rows_per_cta = 0;
         const unsigned grid = decode_grid(q_pos0, n_rows, ratio, c.num_sms, rows_per_cta);
         return launch(indexer_decode_kernel<false>, dim3(grid), dim3(kThreads), 0, c, 1, a, rows_per_cta,
-                      cmp::CompressArgs{});
+                      cmp::CompressArgs{}, DecodeBatch{});
     }
     if (indexer_prefill_tc_ok(n_q, n_rows, d_idx))
         return launch_indexer_prefill_tc(q_idx, n_q, k_idx, n_rows, d_idx, q_pos0, ratio, k, out_idx, out_n, ws, c);
@@ -453,7 +506,33 @@ cudaError_t launch_indexer_compress(const uint16_t *q_idx, const uint16_t *k_idx
     int rows_per_cta = 0;
     // the scoring CTAs leave one SM for the compressor's CTA
     const unsigned grid = decode_grid(q_pos, n_rows, ratio, c.num_sms > 1 ? c.num_sms - 1 : 1, rows_per_cta);
-    return launch(indexer_decode_kernel<true>, dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca);
+    return launch(indexer_decode_kernel<true>, dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
+                  DecodeBatch{});
+}
+
+size_t indexer_batched_ws_stride(long long cap) {
+    return (kWsHeader + static_cast<size_t>(cap) * sizeof(uint32_t) + 255) / 256 * 256;
+}
+
+cudaError_t launch_indexer_compress_batched(int B, const uint16_t *q_idx, const uint16_t *k_idx, long long cap,
+                                           int d_idx, const long long *pos, int ratio, int k, int32_t *out_idx,
+                                           int32_t *out_n, void *ws, const uint16_t *ring_k, const uint16_t *ring_v,
+                                           int W, int D, const float *score_w, float *state, uint16_t *comp_k,
+                                           uint16_t *comp_v, const Ctx &c) {
+    if (d_idx > kMaxDIdx || cap > 0x7fffffffLL || ratio > cmp::kMaxRatio || D > cmp::kMaxD)
+        return cudaErrorInvalidValue;
+    cudaError_t e = configure_indexer(c);
+    if (e != cudaSuccess) return e;
+    IndexerArgs a{q_idx, k_idx, out_idx, out_n, static_cast<unsigned char *>(ws), cap, 0, 1, d_idx, ratio, k};
+    const cmp::CompressArgs ca{nullptr, nullptr, score_w, state, comp_k, comp_v, 0, 1, D, ratio};
+    DecodeBatch bt{pos, d_idx, cap * d_idx, k, static_cast<long long>(indexer_batched_ws_stride(cap)),
+                   ring_k, ring_v, static_cast<long long>(W) * D, 2 + 2LL * D, cap * D, cap, c.err, W};
+    // every session's scoring CTAs and its compressor CTA in one wave when B allows:
+    // (SMs - B) / B scoring CTAs per session, sized for the largest row count (cap)
+    const int per_session = c.num_sms > 2 * B ? (c.num_sms - B) / B : 1;
+    int rows_per_cta = 0;
+    const unsigned grid = decode_grid(cap * ratio, cap, ratio, per_session, rows_per_cta);
+    return launch(indexer_decode_kernel<true>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca, bt);
 }
 
 // kernel attributes, once per device and host thread

@@ -29,7 +29,9 @@ DS4A_ERR_DEVICE_INDEX = 7
 EXPORTED = ["ds4a_status_str", "ds4a_last_device_error", "ds4a_compress_append",
             "ds4a_indexer_topk", "ds4a_indexer_workspace_bytes", "ds4a_attn_decode",
             "ds4a_attn_prefill", "ds4a_indexer_topk_compress", "ds4a_compress_attn_decode",
-            "ds4a_indexer_topk_noalloc", "ds4a_test_set_wait_limit", "ds4a_compress_append_keys"]
+            "ds4a_indexer_topk_noalloc", "ds4a_test_set_wait_limit", "ds4a_compress_append_keys",
+            "ds4a_decode_batched_workspace_bytes", "ds4a_indexer_topk_compress_batched", "ds4a_attn_decode_batched",
+            "ds4a_compress_attn_decode_batched"]
 
 
 class Ds4aError(RuntimeError):
@@ -53,6 +55,11 @@ def lib() -> ctypes.CDLL:
         L.ds4a_compress_append.argtypes = [P, P, I, I, P, I, LL, P, P, P, LL, P]
         L.ds4a_indexer_topk.argtypes = [P, I, P, LL, I, LL, I, I, P, P, P, SZ, P]
         L.ds4a_compress_append_keys.argtypes = [P, P, P, I, I, I, P, I, LL, P, P, P, P, LL, P]
+        L.ds4a_decode_batched_workspace_bytes.argtypes = [I, LL]
+        L.ds4a_decode_batched_workspace_bytes.restype = SZ
+        L.ds4a_indexer_topk_compress_batched.argtypes = [I, P, P, LL, I, P, I, I, P, P, P, SZ, P, P, I, I, P, P, P, P, P]
+        L.ds4a_attn_decode_batched.argtypes = [I, P, I, I, P, P, I, P, P, P, LL, P, I, I, F, P, P]
+        L.ds4a_compress_attn_decode_batched.argtypes = [I, P, I, P, P, P, LL, P, I, I, P, P, I, P, F, P, P]
         L.ds4a_indexer_topk_compress.argtypes = [P, P, LL, I, LL, I, I, P, P, P, SZ, P, P, I, P, P, P, P, LL, P]
         L.ds4a_compress_attn_decode.argtypes = [P, P, P, I, LL, P, P, P, LL, P, I, I, P, P, I, F, P, P]
         L.ds4a_indexer_workspace_bytes.argtypes = [I, LL, I]
@@ -60,7 +67,7 @@ def lib() -> ctypes.CDLL:
         L.ds4a_attn_decode.argtypes = [P, I, I, P, P, I, P, P, LL, P, I, F, P, P, SZ, P]
         L.ds4a_attn_prefill.argtypes = [P, I, I, I, P, P, I, I, P, P, LL, P, I, LL, I, F, P, P, SZ, P]
         for name in EXPORTED:
-            if name not in ("ds4a_status_str", "ds4a_indexer_workspace_bytes"):
+            if name not in ("ds4a_status_str", "ds4a_indexer_workspace_bytes", "ds4a_decode_batched_workspace_bytes"):
                 getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -269,7 +276,93 @@ def ds4a_attn_prefill(q, raw_k, raw_v, n_prior: int, window: int, comp_k, comp_v
     _check(rc, "ds4a_attn_prefill")
 
 
+def ds4a_decode_batched_workspace_bytes(B: int, cap: int) -> int:
+    return int(lib().ds4a_decode_batched_workspace_bytes(B, cap))
+
+
+def _marshal_indexer_topk_compress_batched(q_idx, k_idx, pos, ratio: int, k: int, out_idx, out_n, ws, ring_k,
+                                           ring_v, score_w, state, comp_k, comp_v, stream=None):
+    B, cap, d = k_idx.shape
+    _, W, D = ring_k.shape
+    if q_idx.shape != (B, d) or pos.shape != (B,) or out_idx.shape[0] != B or out_idx.shape[1] < k:
+        raise ValueError("indexer_topk_compress_batched: query / position / output shapes")
+    if ring_v.shape != ring_k.shape or ring_k.shape[0] != B or comp_k.shape != (B, cap, D) or comp_v.shape != comp_k.shape:
+        raise ValueError("indexer_topk_compress_batched: ring / compressed-row shapes")
+    if state.shape != (B, 2 + 2 * D) or score_w.numel() != D or out_idx.shape[1] != k:
+        raise ValueError("indexer_topk_compress_batched: state / score_w / out_idx shapes")
+    return (B, _ptr(q_idx, torch.float16, "q_idx"), _ptr(k_idx, torch.float16, "k_idx"), cap, d,
+            _ptr(pos, torch.int64, "pos"), ratio, k, _ptr(out_idx, torch.int32, "out_idx"),
+            _ptr(out_n, torch.int32, "out_n", optional=True), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+            _ptr(ring_k, torch.float16, "ring_k"), _ptr(ring_v, torch.float16, "ring_v"), W, D,
+            _ptr(score_w, torch.float32, "score_w"), _ptr(state, torch.float32, "state"),
+            _ptr(comp_k, torch.float16, "comp_k"), _ptr(comp_v, torch.float16, "comp_v"), _stream(stream))
+
+
+def ds4a_indexer_topk_compress_batched(q_idx, k_idx, pos, ratio: int, k: int, out_idx, out_n, ws, ring_k, ring_v,
+                                       score_w, state, comp_k, comp_v, stream=None):
+    """B sessions: q_idx [B, d], k_idx [B, cap, d], pos int64 [B] (device), out_idx [B, k],
+    rings [B, W, D], state [B, 2 + 2D], comp rows [B, cap, D]."""
+    args = _marshal_indexer_topk_compress_batched(q_idx, k_idx, pos, ratio, k, out_idx, out_n, ws, ring_k, ring_v,
+                                                  score_w, state, comp_k, comp_v, stream)
+    _check(lib().ds4a_indexer_topk_compress_batched(*args), "ds4a_indexer_topk_compress_batched")
+
+
+def _marshal_attn_decode_batched(q, ring_k, ring_v, pos, comp_k, comp_v, sel, ratio: int, scale: float, out,
+                                 stream=None):
+    B, H, D = q.shape
+    W = ring_k.shape[1]
+    cap = 0 if comp_k is None else comp_k.shape[1]
+    if ring_k.shape != (B, W, D) or ring_v.shape != ring_k.shape or pos.shape != (B,) or out.shape != q.shape:
+        raise ValueError("attn_decode_batched: shapes")
+    if comp_k is not None and (comp_k.shape != (B, cap, D) or comp_v.shape != comp_k.shape):
+        raise ValueError("attn_decode_batched: compressed-row shapes")
+    n_sel = 0 if sel is None else sel.shape[1]
+    if sel is not None and sel.shape[0] != B:
+        raise ValueError("attn_decode_batched: sel shape")
+    return (B, _ptr(q, torch.float16, "q"), H, D, _ptr(ring_k, torch.float16, "ring_k"),
+            _ptr(ring_v, torch.float16, "ring_v"), W, _ptr(pos, torch.int64, "pos"),
+            _ptr(comp_k, torch.float16, "comp_k", optional=True), _ptr(comp_v, torch.float16, "comp_v", optional=True),
+            cap, _ptr(sel, torch.int32, "sel", optional=True), n_sel, ratio, scale, _ptr(out, torch.float16, "out"),
+            _stream(stream))
+
+
+def ds4a_attn_decode_batched(q, ring_k, ring_v, pos, comp_k, comp_v, sel, ratio: int, scale: float, out,
+                             stream=None):
+    """B sessions: q [B, H, D], rings [B, W, D], pos int64 [B] (device), comp rows [B, cap, D] (or
+    None), sel [B, n] int32 or None (every visible row), out [B, H, D]."""
+    args = _marshal_attn_decode_batched(q, ring_k, ring_v, pos, comp_k, comp_v, sel, ratio, scale, out, stream)
+    _check(lib().ds4a_attn_decode_batched(*args), "ds4a_attn_decode_batched")
+
+
+def _marshal_compress_attn_decode_batched(score_w, ratio: int, state, comp_k, comp_v, q, ring_k, ring_v, pos,
+                                          scale: float, out, stream=None):
+    B, H, D = q.shape
+    W = ring_k.shape[1]
+    cap = comp_k.shape[1]
+    if ring_k.shape != (B, W, D) or ring_v.shape != ring_k.shape or pos.shape != (B,) or out.shape != q.shape:
+        raise ValueError("compress_attn_decode_batched: shapes")
+    if comp_k.shape != (B, cap, D) or comp_v.shape != comp_k.shape or state.shape != (B, 2 + 2 * D):
+        raise ValueError("compress_attn_decode_batched: compressed-row / state shapes")
+    return (B, _ptr(score_w, torch.float32, "score_w"), ratio, _ptr(state, torch.float32, "state"),
+            _ptr(comp_k, torch.float16, "comp_k"), _ptr(comp_v, torch.float16, "comp_v"), cap,
+            _ptr(q, torch.float16, "q"), H, D, _ptr(ring_k, torch.float16, "ring_k"),
+            _ptr(ring_v, torch.float16, "ring_v"), W, _ptr(pos, torch.int64, "pos"), scale,
+            _ptr(out, torch.float16, "out"), _stream(stream))
+
+
+def ds4a_compress_attn_decode_batched(score_w, ratio: int, state, comp_k, comp_v, q, ring_k, ring_v, pos,
+                                      scale: float, out, stream=None):
+    """B sessions of a layer that attends every row: each session's compressor update
+    and attention in one launch."""
+    args = _marshal_compress_attn_decode_batched(score_w, ratio, state, comp_k, comp_v, q, ring_k, ring_v, pos,
+                                                 scale, out, stream)
+    _check(lib().ds4a_compress_attn_decode_batched(*args), "ds4a_compress_attn_decode_batched")
+
+
 _MARSHAL = {"ds4a_attn_decode": _marshal_attn_decode,
+            "ds4a_indexer_topk_compress_batched": _marshal_indexer_topk_compress_batched,
+            "ds4a_attn_decode_batched": _marshal_attn_decode_batched,
+            "ds4a_compress_attn_decode_batched": _marshal_compress_attn_decode_batched,
             "ds4a_indexer_topk": _marshal_indexer_topk,
             "ds4a_compress_append_keys": _marshal_compress_append_keys,
             "ds4a_compress_attn_decode": _marshal_compress_attn_decode,

@@ -305,3 +305,142 @@ class PrefillStack:
         for L in self.layers:
             L.step(stream=stream)
         return [L.out for L in self.layers]
+
+
+class BatchedDecodeLayer:
+    """B independent decode sessions of one layer, stepped together: one launch of
+    each batched kernel serves every session ("DwarfStar (ds4) Deep Dive",
+    Step-by-Step Tutorial, "Start the Server": --batched-session 16).
+
+    Built from one DecodeInstance per session (the same layer shape and schedule,
+    any positions).  Device state is batched along a leading session axis: rings
+    [B, W, D], compressed rows [B, cap, D], indexer keys [B, cap, d_idx], compressor
+    states [B, 2 + 2D], positions pos [B] (int64, device memory).
+    """
+
+    def __init__(self, instances, device="cuda", cap_extra: int = 0):
+        for inst in instances[1:]:
+            if not np.array_equal(inst.w, instances[0].w):
+                raise ValueError("BatchedDecodeLayer: the sessions of one layer share its compressor score weights")
+        singles = [DecodeLayer(inst, device=device, cap_extra=0) for inst in instances]
+        L0 = singles[0]
+        for L in singles:
+            if (L.H, L.D, L.W, L.ratio, L.topk) != (L0.H, L0.D, L0.W, L0.ratio, L0.topk) or L.pooled_keys:
+                raise ValueError("BatchedDecodeLayer: sessions must share the layer's shape and schedule")
+        self.B = len(singles)
+        self.H, self.D, self.W, self.ratio, self.topk = L0.H, L0.D, L0.W, L0.ratio, L0.topk
+        self.scale = L0.scale
+        dev = torch.device(device)
+        self.p_host = [L.p for L in singles]
+        self.pos = torch.tensor(self.p_host, dtype=torch.int64, device=dev)
+        self.ring_k = torch.stack([L.ring_k for L in singles])
+        self.ring_v = torch.stack([L.ring_v for L in singles])
+        self.q = torch.stack([L.q for L in singles])
+        self.w = L0.w
+        self.state = torch.stack([L.state for L in singles])
+        self.out = torch.empty_like(self.q)
+        self.cap = 0
+        self.comp_k = self.comp_v = self.kidx = self.q_idx = self.sel = self.sel_n = self.ws = None
+        if self.ratio:
+            self.cap = max(1, max(L.n_vis for L in singles) + cap_extra)
+            self.comp_k = torch.zeros(self.B, self.cap, self.D, dtype=torch.float16, device=dev)
+            self.comp_v = torch.zeros_like(self.comp_k)
+            for s, L in enumerate(singles):
+                n = min(L.comp_k.shape[0], self.cap)
+                self.comp_k[s, :n] = L.comp_k[:n]
+                self.comp_v[s, :n] = L.comp_v[:n]
+        if self.topk:
+            d_idx = L0.kidx.shape[1]
+            self.kidx = torch.zeros(self.B, self.cap, d_idx, dtype=torch.float16, device=dev)
+            for s, L in enumerate(singles):
+                n = min(L.kidx.shape[0], self.cap)
+                self.kidx[s, :n] = L.kidx[:n]
+            self.q_idx = torch.stack([L.q_idx for L in singles])
+            self.sel = torch.full((self.B, self.topk), -1, dtype=torch.int32, device=dev)
+            self.sel_n = torch.zeros(self.B, dtype=torch.int32, device=dev)
+            self.ws = torch.zeros(ds4a.ds4a_decode_batched_workspace_bytes(self.B, self.cap), dtype=torch.uint8,
+                                  device=dev)
+
+    def clone(self) -> "BatchedDecodeLayer":
+        c = copy.copy(self)
+        for name, val in vars(self).items():
+            if isinstance(val, torch.Tensor):
+                setattr(c, name, val.clone())
+        c.p_host = list(self.p_host)
+        if c.ws is not None:
+            c.ws.zero_()
+        return c
+
+    def bytes_touched(self) -> int:
+        """Device bytes one batched step reads or writes (the sum over the sessions)."""
+        D, b = self.D, 0
+        for p in self.p_host:
+            n_win = min(self.W, p + 1)
+            n_vis = min((p + 1) // self.ratio, self.cap) if self.ratio else 0
+            b += 2 * self.H * D * 2 + 2 * n_win * D * 2 + 8
+            if self.ratio:
+                b += 2 * D * 2 + D * 4 + (2 + 2 * D) * 4
+                b += 2 * (min(self.topk, n_vis) if self.topk else n_vis) * D * 2
+            if self.topk:
+                b += n_vis * self.kidx.shape[2] * 2 + self.kidx.shape[2] * 2 + self.topk * 4 * 2 + 4
+        return b
+
+    def _step_calls(self):
+        if self.topk:
+            return [("ds4a_indexer_topk_compress_batched", (self.q_idx, self.kidx, self.pos, self.ratio, self.topk,
+                                                            self.sel, self.sel_n, self.ws, self.ring_k, self.ring_v,
+                                                            self.w, self.state, self.comp_k, self.comp_v)),
+                    ("ds4a_attn_decode_batched", (self.q, self.ring_k, self.ring_v, self.pos, self.comp_k,
+                                                  self.comp_v, self.sel, self.ratio, self.scale, self.out))]
+        if self.ratio:
+            return [("ds4a_compress_attn_decode_batched", (self.w, self.ratio, self.state, self.comp_k, self.comp_v,
+                                                           self.q, self.ring_k, self.ring_v, self.pos, self.scale,
+                                                           self.out))]
+        return [("ds4a_attn_decode_batched", (self.q, self.ring_k, self.ring_v, self.pos, None, None, None, 0,
+                                              self.scale, self.out))]
+
+    def step(self, stream=None):
+        """One decode step of every session at its position pos[s] (inputs resident)."""
+        for name, args in self._step_calls():
+            getattr(ds4a, name)(*args, stream=stream)
+        return self.out
+
+    def bind(self, stream=None):
+        """The step marshalled once (see DecodeLayer.bind)."""
+        calls = [ds4a.bind(name, *args, stream=stream) for name, args in self._step_calls()]
+
+        def run():
+            for c in calls:
+                c()
+            return self.out
+        return run
+
+    def advance(self, k, v, q, q_idx=None, kidx_rows=None, stream=None):
+        """Every session decodes its next token: k, v [B, D] go to ring slot
+        (pos + 1) % W of each session, q [B, H, D] and q_idx [B, d_idx] are the steps'
+        queries; kidx_rows [B, d_idx] holds the indexer key of the row each session's
+        token completes (rows of sessions that complete none are ignored).  The
+        positions advance on the host and on the device."""
+        p_new = [p + 1 for p in self.p_host]
+        if self.ratio and max((p + 1) // self.ratio for p in p_new) > self.cap:
+            raise ValueError("advance: a session's rows would pass the capacity")
+        cur = torch.cuda.current_stream(self.q.device) if stream is None else stream
+        dev = self.q.device
+        sess = torch.arange(self.B, device=dev)
+        slots = torch.tensor([p % self.W for p in p_new], dtype=torch.int64, device=dev)
+        with torch.cuda.stream(cur):
+            self.ring_k[sess, slots] = k
+            self.ring_v[sess, slots] = v
+            self.q.copy_(q, non_blocking=True)
+            if self.topk:
+                self.q_idx.copy_(q_idx, non_blocking=True)
+                done = [s for s, p in enumerate(p_new) if (p + 1) % self.ratio == 0]
+                if done:
+                    if kidx_rows is None:
+                        raise ValueError("advance: sessions completing a row need its indexer key")
+                    rows = torch.tensor([(p_new[s] + 1) // self.ratio - 1 for s in done], dtype=torch.int64, device=dev)
+                    idx = torch.tensor(done, dtype=torch.int64, device=dev)
+                    self.kidx[idx, rows] = kidx_rows[idx]
+            self.pos.add_(1)
+        self.p_host = p_new
+        return self.step(stream=stream)

@@ -301,6 +301,73 @@ int ds4a_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *ra
                       long long q_pos0, int ratio, float scale, uint16_t *out, void *ws,
                       size_t ws_bytes, void *stream);
 
+/*
+ * Batched decode: B independent sessions of one layer per call.
+ * ("DwarfStar (ds4) Deep Dive", Step-by-Step Tutorial, "Start the Server": the
+ * CUDA server's --batched-session 16 serves 16 decode sessions at once; the
+ * "ds4 antirez DeepSeek V4 Flash local engine 2026 guide" page, Use Cases That
+ * Fit, "A multi-user box on CUDA cards".)
+ * Each session is one decode step as the single-session calls define it, at its
+ * own position; a call amortises the per-launch latency over the sessions and
+ * streams all of their key and KV rows at once.
+ *
+ * Layout: session s's arrays sit at fixed strides from session 0's:
+ *   pos        [B] int64, DEVICE memory: session s decodes the token at pos[s]
+ *              (which the caller has written into slot pos[s] % W of its ring).
+ *   q          [B, H, D] fp16;   out [B, H, D] fp16.
+ *   q_idx      [B, d_idx] fp16;  k_idx [B, cap, d_idx] fp16 (one key per row).
+ *   ring_k, ring_v [B, W, D] fp16: each session's raw window ring, token t in
+ *              slot t % W; the window is its min(W, pos+1) slots 0 .. W-1.
+ *   comp_k, comp_v [B, cap, D] fp16; state [B, 2 + 2D] float.
+ *   out_idx    [B, k] int32 kept rows (as ds4a_indexer_topk); out_n [B] or NULL.
+ * Rows of a session that would reach past cap are not written: the compressor
+ * update is skipped and DS4A_ERR_CAPACITY is recorded in the device error word
+ * (the positions are in device memory, so the host cannot check them).
+ * Early reads: pos, plus each single-session call's early reads.
+ */
+
+/* Workspace bytes of ds4a_indexer_topk_compress_batched: one 256-byte aligned
+ * region per session (ticket + one key per row).  Zero-filled once by the caller;
+ * the calls leave it at zero. */
+size_t ds4a_decode_batched_workspace_bytes(int B, long long cap);
+
+/*
+ * ds4a_indexer_topk_compress_batched -- for every session, the indexer query of
+ * its token at pos[s] over its visible rows min(cap, floor((pos[s]+1)/ratio)),
+ * and the compressor update for that token (read from ring slot pos[s] % W), in
+ * one launch: per session the same results as ds4a_indexer_topk_compress.
+ *   W          ring length, 1 .. 4096; head_dim, d_idx, ratio, k as the
+ *              single-session call; score_w [head_dim] float, shared by the
+ *              sessions (one layer's weights).
+ *   ws         ds4a_decode_batched_workspace_bytes(B, cap) bytes, 256-byte aligned.
+ */
+int ds4a_indexer_topk_compress_batched(int B, const uint16_t *q_idx, const uint16_t *k_idx, long long cap,
+                                       int d_idx, const long long *pos, int ratio, int k, int32_t *out_idx,
+                                       int32_t *out_n, void *ws, size_t ws_bytes, const uint16_t *ring_k,
+                                       const uint16_t *ring_v, int W, int head_dim, const float *score_w,
+                                       float *state, uint16_t *comp_k, uint16_t *comp_v, void *stream);
+
+/*
+ * ds4a_attn_decode_batched -- for every session, one decode query's attention
+ * over its window and compressed rows, as ds4a_attn_decode: the rows listed in
+ * its sel row (sel [B, n_sel] int32, -1 entries skipped), or with sel = NULL
+ * every visible row min(cap, floor((pos[s]+1)/ratio)) (ratio = 0: window only).
+ */
+int ds4a_attn_decode_batched(int B, const uint16_t *q, int H, int D, const uint16_t *ring_k, const uint16_t *ring_v,
+                             int W, const long long *pos, const uint16_t *comp_k, const uint16_t *comp_v,
+                             long long cap, const int32_t *sel, int n_sel, int ratio, float scale, uint16_t *out,
+                             void *stream);
+
+/*
+ * ds4a_compress_attn_decode_batched -- for every session of a layer that attends
+ * every compressed row, the compressor update for its token and the attention,
+ * in one launch: per session the same results as ds4a_compress_attn_decode.
+ */
+int ds4a_compress_attn_decode_batched(int B, const float *score_w, int ratio, float *state, uint16_t *comp_k,
+                                      uint16_t *comp_v, long long cap, const uint16_t *q, int H, int D,
+                                      const uint16_t *ring_k, const uint16_t *ring_v, int W, const long long *pos,
+                                      float scale, uint16_t *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
