@@ -825,9 +825,10 @@ __global__ void __launch_bounds__(kThreads) attn_prefill_kernel(PrefillArgs a) {
 }
 
 template <int D>
-cudaError_t configure(int &cluster) {
+cudaError_t configure(int &cluster, int *active16 = nullptr, int *active8 = nullptr) {
     static thread_local int configured_device = -1;
     static thread_local int cluster_size = 16;
+    static thread_local int n_active16 = 0, n_active8 = 0;   // clusters of 16 / 8 resident at once
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
@@ -865,10 +866,20 @@ cudaError_t configure(int &cluster) {
         if (cudaOccupancyMaxActiveClusters(&n_clusters, attn_decode_kernel<D, false>, &cfg) == cudaSuccess &&
             n_clusters > 0)
             cluster_size = 16;
+        n_active16 = n_clusters > 0 ? n_clusters : 0;
+        cudaGetLastError();
+        attr.val.clusterDim.x = 8;
+        cfg.gridDim = dim3(8);
+        n_clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&n_clusters, attn_decode_kernel<D, false>, &cfg) != cudaSuccess)
+            n_clusters = 0;
+        n_active8 = n_clusters;
         cudaGetLastError();
         configured_device = dev;
     }
     cluster = cluster_size;
+    if (active16) *active16 = n_active16;
+    if (active8) *active8 = n_active8;
     return cudaSuccess;
 }
 
@@ -952,9 +963,12 @@ cudaError_t launch_attn_decode_batched(int B, const uint16_t *q, int H, int D, c
     a.W = W;
     a.ratio = ratio;
     a.n_sel_list = sel ? n_sel : 0;
-    int cluster = 16;
-    cudaError_t e = D == 128 ? configure<128>(cluster) : configure<64>(cluster);
+    int cluster = 16, active16 = 0, active8 = 0;
+    cudaError_t e = D == 128 ? configure<128>(cluster, &active16, &active8) : configure<64>(cluster, &active16, &active8);
     if (e != cudaSuccess) return e;
+    // clusters of 16 while every session's cluster can be resident at once, else of 8
+    // (each CTA then attends twice the rows, but more sessions run side by side)
+    if (cluster == 16 && B > active16 && active8 > active16) cluster = 8;
     const dim3 grid(cluster, B);
     if (state != nullptr) {   // the compressor's update for each session's token, in the same launch
         const cmp::CompressArgs ca{nullptr, nullptr, score_w, state, const_cast<uint16_t *>(comp_k),

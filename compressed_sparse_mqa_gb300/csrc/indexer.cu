@@ -304,8 +304,10 @@ DS4A_DEVINL void compress_one_token(const cmp::CompressArgs &c, float *s_w, floa
 
 // Rows [lo, hi) of a slice scored into keys[j - kbase], kDeep 64-row batches per
 // round: the loads of a round are all issued before any of them is scored, so a
-// CTA that covers many rows keeps kDeep x 16 KB of key rows in flight.
-constexpr int kDeep = 4;
+// CTA that covers many rows (a batched step) keeps kDeep x 16 KB of key rows in
+// flight.  A single decode query spreads its rows at 64 per CTA and takes kDeep = 1:
+// the deeper round measured 0.8 us slower there.
+template <int kDeep>
 DS4A_DEVINL void score_rows(const IndexerArgs &a, const float (&qf)[2][8], long long lo, long long hi,
                            uint32_t *keys, long long kbase) {
     for (long long base = lo; base < hi; base += kDeep * kRowsPerCta) {
@@ -343,7 +345,7 @@ struct DecodeBatch {
 // one more CTA per session, which feeds the query's token to the layer's compressor:
 // that update reads nothing the selection writes and vice versa.  blockIdx.y is the
 // session of a batched step.
-template <bool kCompress>
+template <bool kCompress, int kDeep>
 __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs a, int rows_per_cta,
                                                                      cmp::CompressArgs c, DecodeBatch bt) {
     __shared__ SelectSmem sm;
@@ -394,14 +396,14 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     const long long js = max(j0, min(min(j1, j0 + kStagedRows), a.q_pos0 / a.ratio));
     float qf[2][8];
     load_query(a.q_idx, a.d_idx, qf);
-    score_rows(a, qf, j0, js, s_keys, j0);
+    score_rows<kDeep>(a, qf, j0, js, s_keys, j0);
     pdl_wait();
     pdl_trigger();
     unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws);
     uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + kWsHeader);
     __syncthreads();
     for (long long j = j0 + threadIdx.x; j < js; j += kThreads) keys[j] = s_keys[j - j0];
-    score_rows(a, qf, js, j1, keys, 0);
+    score_rows<kDeep>(a, qf, js, j1, keys, 0);
     // one acquire-release atomic per CTA: releases this CTA's keys (ordered before it
     // by the barrier) and, for the last CTA, acquires everyone else's
     __syncthreads();
@@ -484,7 +486,7 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
     if (n_q == 1) {
         int rows_per_cta = 0;
         const unsigned grid = decode_grid(q_pos0, n_rows, ratio, c.num_sms, rows_per_cta);
-        return launch(indexer_decode_kernel<false>, dim3(grid), dim3(kThreads), 0, c, 1, a, rows_per_cta,
+        return launch(indexer_decode_kernel<false, 1>, dim3(grid), dim3(kThreads), 0, c, 1, a, rows_per_cta,
                       cmp::CompressArgs{}, DecodeBatch{});
     }
     if (indexer_prefill_tc_ok(n_q, n_rows, d_idx))
@@ -506,7 +508,7 @@ cudaError_t launch_indexer_compress(const uint16_t *q_idx, const uint16_t *k_idx
     int rows_per_cta = 0;
     // the scoring CTAs leave one SM for the compressor's CTA
     const unsigned grid = decode_grid(q_pos, n_rows, ratio, c.num_sms > 1 ? c.num_sms - 1 : 1, rows_per_cta);
-    return launch(indexer_decode_kernel<true>, dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
+    return launch(indexer_decode_kernel<true, 1>, dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
                   DecodeBatch{});
 }
 
@@ -532,7 +534,8 @@ cudaError_t launch_indexer_compress_batched(int B, const uint16_t *q_idx, const 
     const int per_session = c.num_sms > 2 * B ? (c.num_sms - B) / B : 1;
     int rows_per_cta = 0;
     const unsigned grid = decode_grid(cap * ratio, cap, ratio, per_session, rows_per_cta);
-    return launch(indexer_decode_kernel<true>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca, bt);
+    return launch(indexer_decode_kernel<true, 4>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
+                  bt);
 }
 
 // kernel attributes, once per device and host thread
@@ -545,10 +548,13 @@ static cudaError_t configure_indexer(const Ctx &c) {
         cudaError_t e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kQuerySmem));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(indexer_decode_kernel<false, 1>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 1>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
