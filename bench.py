@@ -408,7 +408,44 @@ def sub_prefill(params, stream, peaks, flush):
             "tflops": round(tflops, 2), "tensor_frac": round(tflops / peak, 4),
             "peak": f"{peak} TFLOP/s dense bf16 burst, measured (fp16 runs at the same rate)",
             "flops_per_chunk": C4_FLOPS,
-            "timed": "graph of 2 chunks (2 copies), L2 flushed before each of 10 regions, median"}
+            "timed": "graph of 2 chunks (2 copies), L2 flushed before each of 10 regions, median",
+            "attention_gather": prefill_gather_roofline(copies, stream, flush)}
+
+
+def prefill_gather_roofline(copies, stream, flush):
+    """The prefill attention kernel against the rate at which rows can be gathered: every
+    query reads its window rows and its kept compressed rows (K and V, 256 B each).  The
+    peak is measured here with ds4a_probe_gather (16-byte asynchronous copies of rows
+    by index into shared memory, nothing else) on the chunk's own kept-row lists over
+    its compressed K rows, after an L2 flush, median of 10."""
+    import torch
+
+    from compressed_sparse_mqa_gb300 import ds4a, timing
+    L = copies[0]
+    T, D = L.T, L.D
+    n_win = sum(min(L.W, L.P + i + 1) for i in range(T))
+    n_sel = int((L.sel >= 0).sum().item())
+    row = D * 2
+    gathered = 2 * (n_win + n_sel) * row            # K and V rows read by the kernel
+
+    def attn(t):
+        C = copies[t % 2]
+        ds4a.ds4a_attn_prefill(C.q, C.raw_k, C.raw_v, C.n_prior, C.W, C.comp_k, C.comp_v, C.sel, C.P, C.ratio,
+                               C.scale, C.out)
+
+    g, reps = timed_graph(attn, 2, stream)
+    t_attn = timing.spread(sampled(g, reps, 2, 10, stream, flush))["median"] / 1e3
+    idx = L.sel.clamp(min=0).reshape(-1).contiguous()
+    sink = torch.zeros(1, dtype=torch.int32, device=idx.device)
+    gp, rp = timed_graph(lambda t: ds4a.ds4a_probe_gather(L.comp_k, idx, sink), 2, stream)
+    t_probe = timing.spread(sampled(gp, rp, 2, 10, stream, flush))["median"] / 1e3
+    peak = idx.numel() * row / t_probe
+    achieved = gathered / t_attn
+    return {"bytes_gathered": gathered, "attention_us": round(t_attn * 1e6, 2),
+            "achieved_tbs": round(achieved / 1e12, 3), "gather_peak_tbs": round(peak / 1e12, 3),
+            "frac": round(achieved / peak, 4), "probe_us": round(t_probe * 1e6, 2),
+            "peak_how": "ds4a_probe_gather: the chunk's 1,048,576 kept-row indices over its compressed K rows, "
+                        "16-byte cp.async into shared memory, L2 flushed first, median of 10"}
 
 
 def sub_batched(B, l2, stream, hbm_peak, flush):
@@ -434,9 +471,17 @@ def sub_batched(B, l2, stream, hbm_peak, flush):
     g, reps = timed_graph(lambda t: layers[t % R].step(), K, stream)
     sp = timing.spread(sampled(g, reps, K, 30, stream, flush))
     s = sp["median"] / 1e3
+    # each of the step's two launches alone, over the copies, after an L2 flush
+    from compressed_sparse_mqa_gb300 import ds4a
+    kernel_us = {}
+    for name in ("ds4a_indexer_topk_compress_batched", "ds4a_attn_decode_batched"):
+        calls = [dict(L._step_calls())[name] for L in layers]
+        gk, rk = timed_graph(lambda t: getattr(ds4a, name)(*calls[t % R]), K, stream)
+        kernel_us[name] = round(timing.spread(sampled(gk, rk, K, 20, stream, flush))["median"] * 1e3, 3)
     return {"sessions": B, "tokens_per_s": round(B / s, 1), "us_per_step": round(s * 1e6, 3),
             "us_per_token_layer": round(s * 1e6 / B, 3), "bytes_per_step": b,
             "hbm_gbs": round(b / s / 1e9, 1), "hbm_frac": round(b / s / 1e9 / hbm_peak, 4),
+            "kernel_us": kernel_us,
             "timed": f"graph of {K} batched steps over {R} copies, L2 flushed before each of 30 regions, median"}
 
 

@@ -276,6 +276,17 @@ int ds4a_attn_prefill(const uint16_t *q, int T, int H, int D, const uint16_t *ra
                                                n_comp, sel, k_stride, q_pos0, ratio, scale, out, c));
 }
 
+int ds4a_probe_gather(const uint16_t *table, long long n_table, int D, const int32_t *idx, long long n_idx,
+                      unsigned int *sink, void *stream) {
+    if (n_table < 0 || n_idx < 0 || D < 8 || D > 256 || D % 8 != 0) return DS4A_ERR_ARG;
+    if (n_idx == 0) return DS4A_OK;
+    if (!table || !idx || !sink || !aligned(table, 16) || !aligned(idx, 4) || !aligned(sink, 4)) return DS4A_ERR_ARG;
+    ds4a::Ctx c;
+    int rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    return from_cuda(ds4a::launch_gather_probe(table, n_table, D, idx, n_idx, sink, c));
+}
+
 // ---- batched decode: B independent sessions per call ------------------------------------
 
 size_t ds4a_decode_batched_workspace_bytes(int B, long long cap) {

@@ -85,6 +85,10 @@ cudaError_t launch_attn_prefill(const uint16_t *q, int T, int H, int D, const ui
                                 const int32_t *sel, int k_stride, long long q_pos0, int ratio,
                                 float scale, uint16_t *out, const Ctx &c);
 
+// measurement kernel: gather n_idx rows table[idx[i]] (D fp16 each) into shared memory
+cudaError_t launch_gather_probe(const uint16_t *table, long long n_table, int D, const int32_t *idx, long long n_idx,
+                                unsigned int *sink, const Ctx &c);
+
 // Launch helper: optional programmatic-dependent-launch attribute, optional cluster.
 template <typename... KArgs, typename... Args>
 cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, const Ctx &c,

@@ -126,6 +126,37 @@ DS4A_DEVINL void score_loaded(const float (&qf)[2][8], const RowLoads &L, long l
     }
 }
 
+// Approximate scores (fp32 FMA, error far below sel::band_select's eps) of the rows held in
+// L, as order-preserving keys, and the largest squared key norm among them (kn2).
+DS4A_DEVINL void score_loaded_approx(const float (&qf)[2][8], const RowLoads &L, long long base, long long j1,
+                                     uint32_t *keys, float &kn2) {
+    const int tid = threadIdx.x, gl = tid % kGroup;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        float s = 0.f, n2 = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const uint16_t *h = reinterpret_cast<const uint16_t *>(&L.v[p][cc]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float kv = h2f(h[e]);
+                s = fmaf(qf[cc][e], kv, s);
+                n2 = fmaf(kv, kv, n2);
+            }
+        }
+#pragma unroll
+        for (int o = kGroup / 2; o > 0; o >>= 1) {
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+            n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+        }
+        const long long j = base + p * kRowsPerPass + tid / kGroup;
+        if (j < j1) {
+            kn2 = fmaxf(kn2, n2);
+            if (gl == 0) keys[j - base] = float_key(s);
+        }
+    }
+}
+
 // ---- select ------------------------------------------------------------------------------
 
 // Block-wide exclusive scan of one value per thread (kThreads threads).
@@ -285,6 +316,18 @@ struct IndexerArgs {
     int k;
 };
 
+// Approximate keys of n > k rows (the workspace) -> the exact top-k through sel::band_select.
+template <int ITEMS, typename Band>
+__device__ void band_select_regs(const IndexerArgs &a, uint32_t *keys, int n, float eps, Band &band) {
+    uint32_t key[ITEMS];
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int i = it * kThreads + threadIdx.x;
+        key[it] = i < n ? __ldcg(keys + i) : 0u;
+    }
+    sel::band_select<kThreads, ITEMS>(key, n, a.k, eps, a.q_idx, a.k_idx, a.d_idx, band, keys, a.out_idx);
+}
+
 DS4A_DEVINL long long visible_rows(const IndexerArgs &a, int i) {
     const long long v = (a.q_pos0 + i + 1) / a.ratio;
     return v < a.n_rows ? v : a.n_rows;
@@ -306,10 +349,12 @@ DS4A_DEVINL void compress_one_token(const cmp::CompressArgs &c, float *s_w, floa
 // round: the loads of a round are all issued before any of them is scored, so a
 // CTA that covers many rows (a batched step) keeps kDeep x 16 KB of key rows in
 // flight.  A single decode query spreads its rows at 64 per CTA and takes kDeep = 1:
-// the deeper round measured 0.8 us slower there.
-template <int kDeep>
+// the deeper round measured 0.8 us slower there.  kApprox: fp32 FMA scores (about a
+// quarter of the TwoSum arithmetic) for sel::band_select, which rescores the rows
+// near the k-th exactly; kn2 collects the largest squared key norm for its bound.
+template <int kDeep, bool kApprox>
 DS4A_DEVINL void score_rows(const IndexerArgs &a, const float (&qf)[2][8], long long lo, long long hi,
-                           uint32_t *keys, long long kbase) {
+                           uint32_t *keys, long long kbase, float &kn2) {
     for (long long base = lo; base < hi; base += kDeep * kRowsPerCta) {
         RowLoads L[kDeep];
 #pragma unroll
@@ -317,7 +362,10 @@ DS4A_DEVINL void score_rows(const IndexerArgs &a, const float (&qf)[2][8], long 
 #pragma unroll
         for (int u = 0; u < kDeep; ++u) {
             const long long bu = base + u * kRowsPerCta;
-            if (bu < hi) score_loaded(qf, L[u], bu, hi, keys + (bu - kbase));   // block-uniform
+            if (bu < hi) {   // block-uniform
+                if constexpr (kApprox) score_loaded_approx(qf, L[u], bu, hi, keys + (bu - kbase), kn2);
+                else score_loaded(qf, L[u], bu, hi, keys + (bu - kbase));
+            }
         }
     }
 }
@@ -345,12 +393,19 @@ struct DecodeBatch {
 // one more CTA per session, which feeds the query's token to the layer's compressor:
 // that update reads nothing the selection writes and vice versa.  blockIdx.y is the
 // session of a batched step.
-template <bool kCompress, int kDeep>
+constexpr int kBandMaxRows = kThreads * kMaxItems;   // approximate path: rows per session
+
+template <bool kCompress, int kDeep, bool kApprox>
 __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs a, int rows_per_cta,
                                                                      cmp::CompressArgs c, DecodeBatch bt) {
-    __shared__ SelectSmem sm;
+    __shared__ union {
+        SelectSmem sm;
+        sel::BandSmem<kThreads, kBandMaxRows> band;
+    } u;
+    SelectSmem &sm = u.sm;
     __shared__ bool s_last;
     __shared__ uint32_t s_keys[kStagedRows];
+    __shared__ float s_red[kWarps];
     if (bt.pos != nullptr) {
         const long long sid = blockIdx.y;
         const long long p = bt.pos[sid];
@@ -395,15 +450,29 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     // write), the workspace and the output are read or written after the wait.
     const long long js = max(j0, min(min(j1, j0 + kStagedRows), a.q_pos0 / a.ratio));
     float qf[2][8];
+    float kn2 = 0.f;   // approximate path: largest squared key norm of this CTA's rows
     load_query(a.q_idx, a.d_idx, qf);
-    score_rows<kDeep>(a, qf, j0, js, s_keys, j0);
+    score_rows<kDeep, kApprox>(a, qf, j0, js, s_keys, j0, kn2);
     pdl_wait();
     pdl_trigger();
     unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws);
+    unsigned int *kmax2_word = ticket + 1;   // approximate path: the session's largest squared key norm
     uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + kWsHeader);
     __syncthreads();
     for (long long j = j0 + threadIdx.x; j < js; j += kThreads) keys[j] = s_keys[j - j0];
-    score_rows<kDeep>(a, qf, js, j1, keys, 0);
+    score_rows<kDeep, kApprox>(a, qf, js, j1, keys, 0, kn2);
+    if constexpr (kApprox) {
+        // non-negative floats order like their bit patterns: one atomicMax per CTA
+        kn2 = warp_max(kn2);
+        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = kn2;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float m = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) m = fmaxf(m, s_red[w]);
+            atomicMax(kmax2_word, __float_as_uint(m));
+        }
+    }
     // one acquire-release atomic per CTA: releases this CTA's keys (ordered before it
     // by the barrier) and, for the last CTA, acquires everyone else's
     __syncthreads();
@@ -414,7 +483,34 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     }
     __syncthreads();
     if (!s_last) return;
-    select_topk<true>(keys, static_cast<int>(n_vis), a.k, a.out_idx, a.out_n, sm);
+    if constexpr (kApprox) {
+        const int n = static_cast<int>(n_vis);
+        if (a.out_n && threadIdx.x == 0) *a.out_n = n < a.k ? n : a.k;
+        if (n <= a.k) {
+            for (int i = threadIdx.x; i < a.k; i += kThreads) a.out_idx[i] = i < n ? i : -1;
+        } else {
+            // eps bounds |approximate - exact| score for every row: 2^-12 |q| max |k|
+            if ((threadIdx.x >> 5) == 0) {
+                const int lane = threadIdx.x & 31;
+                float qn2 = 0.f;
+                for (int cidx = lane; cidx < a.d_idx; cidx += 32) {
+                    const float x = h2f(a.q_idx[cidx]);
+                    qn2 = fmaf(x, x, qn2);
+                }
+                qn2 = warp_sum(qn2);
+                if (lane == 0)
+                    u.band.eps = ldexpf(sqrtf(qn2 * __uint_as_float(__ldcg(kmax2_word))) * 1.01f, -12) + 1e-30f;
+            }
+            __syncthreads();
+            const float eps = u.band.eps;
+            if (n <= kThreads * 8) band_select_regs<8>(a, keys, n, eps, u.band);
+            else if (n <= kThreads * 16) band_select_regs<16>(a, keys, n, eps, u.band);
+            else band_select_regs<kMaxItems>(a, keys, n, eps, u.band);
+        }
+        if (threadIdx.x == 0) *kmax2_word = 0u;
+    } else {
+        select_topk<true>(keys, static_cast<int>(n_vis), a.k, a.out_idx, a.out_n, sm);
+    }
     if (threadIdx.x == 0) *ticket = 0u;
 }
 
@@ -486,7 +582,7 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
     if (n_q == 1) {
         int rows_per_cta = 0;
         const unsigned grid = decode_grid(q_pos0, n_rows, ratio, c.num_sms, rows_per_cta);
-        return launch(indexer_decode_kernel<false, 1>, dim3(grid), dim3(kThreads), 0, c, 1, a, rows_per_cta,
+        return launch(indexer_decode_kernel<false, 1, false>, dim3(grid), dim3(kThreads), 0, c, 1, a, rows_per_cta,
                       cmp::CompressArgs{}, DecodeBatch{});
     }
     if (indexer_prefill_tc_ok(n_q, n_rows, d_idx))
@@ -508,7 +604,7 @@ cudaError_t launch_indexer_compress(const uint16_t *q_idx, const uint16_t *k_idx
     int rows_per_cta = 0;
     // the scoring CTAs leave one SM for the compressor's CTA
     const unsigned grid = decode_grid(q_pos, n_rows, ratio, c.num_sms > 1 ? c.num_sms - 1 : 1, rows_per_cta);
-    return launch(indexer_decode_kernel<true, 1>, dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
+    return launch(indexer_decode_kernel<true, 1, false>, dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
                   DecodeBatch{});
 }
 
@@ -534,8 +630,12 @@ cudaError_t launch_indexer_compress_batched(int B, const uint16_t *q_idx, const 
     const int per_session = c.num_sms > 2 * B ? (c.num_sms - B) / B : 1;
     int rows_per_cta = 0;
     const unsigned grid = decode_grid(cap * ratio, cap, ratio, per_session, rows_per_cta);
-    return launch(indexer_decode_kernel<true, 4>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
-                  bt);
+    // approximate scores with an exact band when every session's rows fit the band select
+    if (cap <= kBandMaxRows)
+        return launch(indexer_decode_kernel<true, 4, true>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a,
+                      rows_per_cta, ca, bt);
+    return launch(indexer_decode_kernel<true, 4, false>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a,
+                  rows_per_cta, ca, bt);
 }
 
 // kernel attributes, once per device and host thread
@@ -548,14 +648,17 @@ static cudaError_t configure_indexer(const Ctx &c) {
         cudaError_t e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kQuerySmem));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel<false, 1>, cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(indexer_decode_kernel<false, 1, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 1>, cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 1, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
+            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, true>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, false>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);

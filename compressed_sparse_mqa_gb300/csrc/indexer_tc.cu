@@ -204,8 +204,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
 // ---- per-query select on approximate scores with an exact band ------------------------------
 
 constexpr int kSelMaxRows = 8192;
-constexpr int kBandCap = 1024;
-constexpr int kBins = 2048;               // 11-bit digits
 
 struct SelArgs {
     const uint16_t *q_idx;
@@ -222,56 +220,10 @@ struct SelArgs {
     int ld;
 };
 
-template <int NT>
-struct SelSmem {
-    uint32_t hist[kBins];
-    uint32_t cnt[NT];
-    uint32_t scan[NT / 32];
-    int band_idx[kBandCap];
-    uint32_t band_key[kBandCap];
-    uint32_t sel_bits[kSelMaxRows / 32];
-    uint32_t res[3], band_n, n_in;
-    float eps;
-};
-
-DS4A_DEVINL float key_to_float(uint32_t key) {
-    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
-
-// TwoSum-exact score of one row, computed by a group of 16 threads (all 32 lanes of
-// every warp call this; `valid` masks the rows).
-DS4A_DEVINL uint32_t exact_key16(const uint16_t *q, const uint16_t *krow, int d_idx, bool valid) {
-    const int gl = threadIdx.x & 15;
-    float s = 0.f, c = 0.f;
-    for (int ch = gl; ch < d_idx / 8; ch += 16) {
-        if (valid) {
-            const uint4 qa = *reinterpret_cast<const uint4 *>(q + ch * 8);
-            const uint4 ka = __ldg(reinterpret_cast<const uint4 *>(krow + ch * 8));
-            const uint16_t *hq = reinterpret_cast<const uint16_t *>(&qa);
-            const uint16_t *hk = reinterpret_cast<const uint16_t *>(&ka);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                float err;
-                two_sum(s, h2f(hq[e]) * h2f(hk[e]), s, err);
-                c += err;
-            }
-        }
-    }
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) {
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
-        float err;
-        two_sum(s, s2, s, err);
-        c = (c + c2) + err;
-    }
-    return float_key(s + c);
-}
-
 template <int NT, int ITEMS, int MIN_BLOCKS>
 __global__ void __launch_bounds__(NT, MIN_BLOCKS) indexer_select_kernel(SelArgs a) {
     constexpr int kSelThreads = NT;
-    __shared__ SelSmem<NT> sm;
+    __shared__ sel::BandSmem<NT, kSelMaxRows> sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();
     pdl_trigger();
@@ -308,98 +260,8 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) indexer_select_kernel(SelArgs 
         if (lane == 0) sm.eps = ldexpf(sqrtf(qn2 * kmax2) * 1.01f, -12) + 1e-30f;
     }
     __syncthreads();
-    const float eps = sm.eps;
-
-    // bracket the k-th largest approximate score: bits 31..21, then 20..10
-    uint32_t kk = static_cast<uint32_t>(a.k);
-    sel::radix_pass<kSelThreads, ITEMS>(key, n, 0u, 0u, 21, 11, kk, sm.hist, sm.scan, sm.res);
-    uint32_t prefix = sm.res[0] << 21, mask = 0xFFE00000u;
-    kk -= sm.res[1];
-    sel::radix_pass<kSelThreads, ITEMS>(key, n, prefix, mask, 10, 11, kk, sm.hist, sm.scan, sm.res);
-    prefix |= sm.res[0] << 10;
-    const uint32_t lo_key = prefix, hi_key = prefix | 0x3FFu;
-    const float t_lo = key_to_float(lo_key), t_hi = key_to_float(hi_key);
-    const float big = fmaxf(fabsf(t_lo), fabsf(t_hi));
-    const float ulp = ldexpf(1.f, ilogbf(big > 0.f ? big : 1.f) - 23);
-    const float margin = 2.f * eps + 4.f * ulp;
-    const float in_thr = t_hi + margin, out_thr = t_lo - margin;
-
-    // classify: certainly in, certainly out, or band (rescored exactly)
-    if (tid == 0) {
-        sm.band_n = 0;
-        sm.n_in = 0;
-    }
-    for (int w = tid; w < ITEMS * kSelThreads / 32; w += kSelThreads) sm.sel_bits[w] = 0;
-    __syncthreads();
-    uint32_t flags = 0, my_in = 0;
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const int j = it * kSelThreads + tid;
-        if (j < n) {
-            const float s = key_to_float(key[it]);
-            if (s > in_thr) {
-                flags |= 1u << it;
-                ++my_in;
-            } else if (s >= out_thr) {
-                const uint32_t b = atomicAdd(&sm.band_n, 1u);
-                if (b < kBandCap) sm.band_idx[b] = j;
-            }
-        }
-    }
-    my_in = __reduce_add_sync(0xffffffffu, my_in);
-    if (lane == 0 && my_in) atomicAdd(&sm.n_in, my_in);
-    __syncthreads();
-    const uint32_t band_n = sm.band_n, n_in = sm.n_in;
-    const bool fits = band_n <= kBandCap && n_in <= static_cast<uint32_t>(a.k) &&
-                      n_in + band_n >= static_cast<uint32_t>(a.k);
-    if (fits) {
-        // exact keys of the band rows: 16 threads per row
-        for (uint32_t b0 = 0; b0 < band_n; b0 += kSelThreads / 16) {
-            const uint32_t b = b0 + tid / 16;
-            const bool valid = b < band_n;
-            const int j = valid ? sm.band_idx[b] : 0;
-            const uint32_t kx = exact_key16(q, a.k_idx + static_cast<size_t>(j) * a.d_idx, a.d_idx, valid);
-            if (valid && (tid & 15) == 0) sm.band_key[b] = kx;
-        }
-        __syncthreads();
-        // keep the (k - n_in) best band rows: higher exact key, then lower index
-        const uint32_t need = static_cast<uint32_t>(a.k) - n_in;
-        for (uint32_t b = tid; b < band_n; b += kSelThreads) {
-            const uint32_t kb = sm.band_key[b];
-            const int jb = sm.band_idx[b];
-            uint32_t rank = 0;
-            for (uint32_t o = 0; o < band_n; ++o) {
-                const uint32_t ko = sm.band_key[o];
-                rank += (ko > kb) || (ko == kb && sm.band_idx[o] < jb);
-            }
-            if (rank < need) atomicOr(&sm.sel_bits[jb >> 5], 1u << (jb & 31));
-        }
-        // the certainly kept rows join the band's kept rows in the row bitmask
-        // (a warp's ballot of one item is the word of its 32 consecutive rows)
-#pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-            const unsigned b = __ballot_sync(0xffffffffu, (flags >> it) & 1u);
-            if (lane == 0 && b) atomicOr(&sm.sel_bits[it * (kSelThreads / 32) + warp], b);
-        }
-        __syncthreads();
-        sel::emit_bits<kSelThreads, ITEMS>(sm.sel_bits, sm.scan, out);
-        return;
-    }
-
-    // fallback: exact keys for every visible row, then an exact radix select
-    for (int b0 = 0; b0 < ITEMS * kSelThreads; b0 += kSelThreads / 16) {
-        const int j = b0 + tid / 16;
-        const uint32_t kx = exact_key16(q, a.k_idx + static_cast<size_t>(j < n ? j : 0) * a.d_idx, a.d_idx, j < n);
-        if (j < n && (tid & 15) == 0) reinterpret_cast<uint32_t *>(row)[j] = kx;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const int j = it * kSelThreads + tid;
-        key[it] = j < n ? reinterpret_cast<const uint32_t *>(row)[j] : 0u;
-    }
-    const bool all_eq = sel::find_threshold<kSelThreads, ITEMS>(key, n, a.k, sm.hist, sm.scan, sm.res, prefix, mask, kk);
-    sel::emit_topk_bits<kSelThreads, ITEMS>(key, n, prefix, mask, kk, all_eq, sm.cnt, sm.sel_bits, sm.scan, out);
+    sel::band_select<kSelThreads, ITEMS>(key, n, a.k, sm.eps, q, a.k_idx, a.d_idx, sm,
+                                         reinterpret_cast<uint32_t *>(row), out);
 }
 
 constexpr int kSelNT = 256, kSelMinBlocks = 4;   // threads per query, CTAs per SM (<= 64 registers)

@@ -216,5 +216,165 @@ DS4A_DEVINL void emit_bits(const uint32_t *bits, uint32_t *scratch, int32_t *out
     }
 }
 
+// ---- top-k from approximate scores with an exact band ---------------------------------------
+// The approximate score s~ of a row differs from its exact score s by at most eps.
+// Two 11-bit radix passes over the approximate keys bracket the k-th largest s~ in
+// [T_lo, T_hi]; rows with s~ > T_hi + 2 eps + 4 ulp are kept for certain, rows with
+// s~ < T_lo - 2 eps - 4 ulp dropped for certain, and only the rows in between (a
+// handful) are rescored exactly (TwoSum over the exact fp16 products, rounded once
+// to binary32) and ranked (higher score, then lower index).  The result is the
+// exact top-k of the binary32-rounded exact scores.  If the band is ever larger
+// than its buffer (many equal keys, say), every row is rescored exactly and an
+// exact radix select runs instead.
+
+constexpr int kBandCap = 1024;
+
+template <int NT, int MAXROWS>
+struct BandSmem {
+    uint32_t hist[kMaxBins];
+    uint32_t cnt[NT];
+    uint32_t scan[NT / 32];
+    int band_idx[kBandCap];
+    uint32_t band_key[kBandCap];
+    uint32_t sel_bits[MAXROWS / 32];
+    uint32_t res[3], band_n, n_in;
+    float eps;
+};
+
+DS4A_DEVINL float key_to_float(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// TwoSum-exact score key of one row, computed by a group of 16 threads (all 32 lanes
+// of every warp call this; `valid` masks the rows).
+DS4A_DEVINL uint32_t exact_key16(const uint16_t *q, const uint16_t *krow, int d_idx, bool valid) {
+    const int gl = threadIdx.x & 15;
+    float s = 0.f, c = 0.f;
+    for (int ch = gl; ch < d_idx / 8; ch += 16) {
+        if (valid) {
+            const uint4 qa = *reinterpret_cast<const uint4 *>(q + ch * 8);
+            const uint4 ka = __ldg(reinterpret_cast<const uint4 *>(krow + ch * 8));
+            const uint16_t *hq = reinterpret_cast<const uint16_t *>(&qa);
+            const uint16_t *hk = reinterpret_cast<const uint16_t *>(&ka);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float err;
+                two_sum(s, h2f(hq[e]) * h2f(hk[e]), s, err);
+                c += err;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        float err;
+        two_sum(s, s2, s, err);
+        c = (c + c2) + err;
+    }
+    return float_key(s + c);
+}
+
+// key[] holds the approximate keys (item `it` of thread t is row it * NT + t), n > k.
+// q: the query (d_idx fp16), k_idx: [>= n, d_idx] fp16 key rows; spill: n u32 of
+// scratch for the exact keys of the fallback.  Writes the kept rows, ascending, to out.
+template <int NT, int ITEMS, int MAXROWS>
+__device__ void band_select(uint32_t (&key)[ITEMS], int n, int k, float eps, const uint16_t *q,
+                            const uint16_t *k_idx, int d_idx, BandSmem<NT, MAXROWS> &sm, uint32_t *spill,
+                            int32_t *out) {
+    static_assert(ITEMS * NT <= MAXROWS, "row bitmask covers every row");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // bracket the k-th largest approximate score: bits 31..21, then 20..10
+    uint32_t kk = static_cast<uint32_t>(k);
+    radix_pass<NT, ITEMS>(key, n, 0u, 0u, 21, 11, kk, sm.hist, sm.scan, sm.res);
+    uint32_t prefix = sm.res[0] << 21, mask = 0xFFE00000u;
+    kk -= sm.res[1];
+    radix_pass<NT, ITEMS>(key, n, prefix, mask, 10, 11, kk, sm.hist, sm.scan, sm.res);
+    prefix |= sm.res[0] << 10;
+    const uint32_t lo_key = prefix, hi_key = prefix | 0x3FFu;
+    const float t_lo = key_to_float(lo_key), t_hi = key_to_float(hi_key);
+    const float big = fmaxf(fabsf(t_lo), fabsf(t_hi));
+    const float ulp = ldexpf(1.f, ilogbf(big > 0.f ? big : 1.f) - 23);
+    const float margin = 2.f * eps + 4.f * ulp;
+    const float in_thr = t_hi + margin, out_thr = t_lo - margin;
+
+    // classify: certainly in, certainly out, or band (rescored exactly)
+    if (tid == 0) {
+        sm.band_n = 0;
+        sm.n_in = 0;
+    }
+    for (int w = tid; w < ITEMS * NT / 32; w += NT) sm.sel_bits[w] = 0;
+    __syncthreads();
+    uint32_t flags = 0, my_in = 0;
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int j = it * NT + tid;
+        if (j < n) {
+            const float s = key_to_float(key[it]);
+            if (s > in_thr) {
+                flags |= 1u << it;
+                ++my_in;
+            } else if (s >= out_thr) {
+                const uint32_t b = atomicAdd(&sm.band_n, 1u);
+                if (b < kBandCap) sm.band_idx[b] = j;
+            }
+        }
+    }
+    my_in = __reduce_add_sync(0xffffffffu, my_in);
+    if (lane == 0 && my_in) atomicAdd(&sm.n_in, my_in);
+    __syncthreads();
+    const uint32_t band_n = sm.band_n, n_in = sm.n_in;
+    const bool fits = band_n <= kBandCap && n_in <= static_cast<uint32_t>(k) &&
+                      n_in + band_n >= static_cast<uint32_t>(k);
+    if (fits) {
+        // exact keys of the band rows: 16 threads per row
+        for (uint32_t b0 = 0; b0 < band_n; b0 += NT / 16) {
+            const uint32_t b = b0 + tid / 16;
+            const bool valid = b < band_n;
+            const int j = valid ? sm.band_idx[b] : 0;
+            const uint32_t kx = exact_key16(q, k_idx + static_cast<size_t>(j) * d_idx, d_idx, valid);
+            if (valid && (tid & 15) == 0) sm.band_key[b] = kx;
+        }
+        __syncthreads();
+        // keep the (k - n_in) best band rows: higher exact key, then lower index
+        const uint32_t need = static_cast<uint32_t>(k) - n_in;
+        for (uint32_t b = tid; b < band_n; b += NT) {
+            const uint32_t kb = sm.band_key[b];
+            const int jb = sm.band_idx[b];
+            uint32_t rank = 0;
+            for (uint32_t o = 0; o < band_n; ++o) {
+                const uint32_t ko = sm.band_key[o];
+                rank += (ko > kb) || (ko == kb && sm.band_idx[o] < jb);
+            }
+            if (rank < need) atomicOr(&sm.sel_bits[jb >> 5], 1u << (jb & 31));
+        }
+        // the certainly kept rows join the band's kept rows in the row bitmask
+        // (a warp's ballot of one item is the word of its 32 consecutive rows)
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) {
+            const unsigned b = __ballot_sync(0xffffffffu, (flags >> it) & 1u);
+            if (lane == 0 && b) atomicOr(&sm.sel_bits[it * (NT / 32) + warp], b);
+        }
+        __syncthreads();
+        emit_bits<NT, ITEMS>(sm.sel_bits, sm.scan, out);
+        return;
+    }
+
+    // fallback: exact keys for every visible row, then an exact radix select
+    for (int b0 = 0; b0 < ITEMS * NT; b0 += NT / 16) {
+        const int j = b0 + tid / 16;
+        const uint32_t kx = exact_key16(q, k_idx + static_cast<size_t>(j < n ? j : 0) * d_idx, d_idx, j < n);
+        if (j < n && (tid & 15) == 0) spill[j] = kx;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int j = it * NT + tid;
+        key[it] = j < n ? spill[j] : 0u;
+    }
+    const bool all_eq = find_threshold<NT, ITEMS>(key, n, k, sm.hist, sm.scan, sm.res, prefix, mask, kk);
+    emit_topk_bits<NT, ITEMS>(key, n, prefix, mask, kk, all_eq, sm.cnt, sm.sel_bits, sm.scan, out);
+}
+
 }  // namespace sel
 }  // namespace ds4a

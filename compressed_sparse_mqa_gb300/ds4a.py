@@ -31,7 +31,7 @@ EXPORTED = ["ds4a_status_str", "ds4a_last_device_error", "ds4a_compress_append",
             "ds4a_attn_prefill", "ds4a_indexer_topk_compress", "ds4a_compress_attn_decode",
             "ds4a_indexer_topk_noalloc", "ds4a_test_set_wait_limit", "ds4a_compress_append_keys",
             "ds4a_decode_batched_workspace_bytes", "ds4a_indexer_topk_compress_batched", "ds4a_attn_decode_batched",
-            "ds4a_compress_attn_decode_batched"]
+            "ds4a_compress_attn_decode_batched", "ds4a_probe_gather"]
 
 
 class Ds4aError(RuntimeError):
@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
         L.ds4a_compress_append.argtypes = [P, P, I, I, P, I, LL, P, P, P, LL, P]
         L.ds4a_indexer_topk.argtypes = [P, I, P, LL, I, LL, I, I, P, P, P, SZ, P]
         L.ds4a_compress_append_keys.argtypes = [P, P, P, I, I, I, P, I, LL, P, P, P, P, LL, P]
+        L.ds4a_probe_gather.argtypes = [P, LL, I, P, LL, P, P]
         L.ds4a_decode_batched_workspace_bytes.argtypes = [I, LL]
         L.ds4a_decode_batched_workspace_bytes.restype = SZ
         L.ds4a_indexer_topk_compress_batched.argtypes = [I, P, P, LL, I, P, I, I, P, P, P, SZ, P, P, I, I, P, P, P, P, P]
@@ -274,6 +275,15 @@ def ds4a_attn_prefill(q, raw_k, raw_v, n_prior: int, window: int, comp_k, comp_v
                                  _ptr(sel, torch.int32, "sel", optional=True), k_stride, q_pos0, ratio, scale,
                                  _ptr(out, torch.float16, "out"), None, 0, _stream(stream))
     _check(rc, "ds4a_attn_prefill")
+
+
+def ds4a_probe_gather(table, idx, sink, stream=None):
+    """Measurement call: gather rows table[idx] ([n, D] fp16, idx int32) into shared memory;
+    sink: a one-element int32 device tensor that receives one word of the result."""
+    rc = lib().ds4a_probe_gather(_ptr(table, torch.float16, "table"), table.shape[0], table.shape[1],
+                                 _ptr(idx, torch.int32, "idx"), idx.numel(), _ptr(sink, torch.int32, "sink"),
+                                 _stream(stream))
+    _check(rc, "ds4a_probe_gather")
 
 
 def ds4a_decode_batched_workspace_bytes(B: int, cap: int) -> int:

@@ -368,6 +368,19 @@ int ds4a_compress_attn_decode_batched(int B, const float *score_w, int ratio, fl
                                       const uint16_t *ring_k, const uint16_t *ring_v, int W, const long long *pos,
                                       float scale, uint16_t *out, void *stream);
 
+/*
+ * ds4a_probe_gather -- MEASUREMENT CALL, not a step of the attention path; the
+ * pages have no counterpart.  Gathers the n_idx rows table[idx[i]] (D fp16 each,
+ * D a multiple of 8, 8 .. 256) into shared memory with 16-byte asynchronous copies,
+ * two 128-row tiles in flight per CTA, and adds one word of the result to *sink
+ * (a device u32).  Prefill attention is bound by gathering its rows, so the
+ * benchmark states the attention kernel's gather rate against this call's rate
+ * on the same rows.  Indices outside [0, n_table) are skipped and recorded as
+ * DS4A_ERR_DEVICE_INDEX.
+ */
+int ds4a_probe_gather(const uint16_t *table, long long n_table, int D, const int32_t *idx, long long n_idx,
+                      unsigned int *sink, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
