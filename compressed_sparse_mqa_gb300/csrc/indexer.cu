@@ -370,6 +370,68 @@ DS4A_DEVINL void score_rows(const IndexerArgs &a, const float (&qf)[2][8], long 
     }
 }
 
+// Approximate scores of rows [lo, hi) into keys[j - lo], the key rows staged through
+// shared memory with 16-byte cp.async: kStages chunks of kChunkRows rows in flight,
+// far more bytes than the register rounds of score_rows keep in flight, for CTAs that
+// cover a thousand rows (batched steps).  Needs d_idx <= 128 (one 16-byte chunk of a
+// row per thread of its 16-thread group).  stage: kStages * kChunkRows * 256 bytes.
+constexpr int kChunkRows = 128;
+constexpr int kStages = 3;
+constexpr size_t kStageBytes = static_cast<size_t>(kStages) * kChunkRows * 256;
+DS4A_DEVINL void score_rows_staged(const IndexerArgs &a, const float (&qf)[2][8], long long lo, long long hi,
+                                   uint32_t *keys, float &kn2, unsigned char *stage) {
+    const int tid = threadIdx.x, gl = tid % kGroup;
+    const int n_chunks = a.d_idx / 8;   // 16-byte chunks of a row (<= 16)
+    const long long n = hi - lo;
+    const int n_tiles = static_cast<int>((n + kChunkRows - 1) / kChunkRows);
+    auto issue = [&](int t) {
+        if (t < n_tiles) {
+            unsigned char *dst = stage + (t % kStages) * (kChunkRows * 256);
+            for (int i = tid; i < kChunkRows * 16; i += kThreads) {
+                const int r = i >> 4, ch = i & 15;
+                const long long j = lo + static_cast<long long>(t) * kChunkRows + r;
+                if (j < hi && ch < n_chunks) cp_async16(dst + i * 16, a.k_idx + j * a.d_idx + ch * 8);
+            }
+        }
+        cp_async_commit();   // one group per tile, empty past the last
+    };
+#pragma unroll
+    for (int t = 0; t < kStages - 1; ++t) issue(t);
+    for (int t = 0; t < n_tiles; ++t) {
+        cp_async_wait<kStages - 2>();   // tile t has landed (this thread's copies)
+        __syncthreads();                // ... and every thread's; tile t-1's stage is free
+        issue(t + kStages - 1);
+        const unsigned char *src = stage + (t % kStages) * (kChunkRows * 256);
+#pragma unroll
+        for (int pass = 0; pass < kChunkRows / kRowsPerPass; ++pass) {
+            const int r = pass * kRowsPerPass + tid / kGroup;
+            const long long j = lo + static_cast<long long>(t) * kChunkRows + r;
+            float s = 0.f, n2 = 0.f;
+            if (j < hi && gl < n_chunks) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(src + (r * 16 + gl) * 16);
+                const uint16_t *h = reinterpret_cast<const uint16_t *>(&raw);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float kv = h2f(h[e]);
+                    s = fmaf(qf[0][e], kv, s);
+                    n2 = fmaf(kv, kv, n2);
+                }
+            }
+#pragma unroll
+            for (int o = kGroup / 2; o > 0; o >>= 1) {
+                s += __shfl_xor_sync(0xffffffffu, s, o);
+                n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+            }
+            if (j < hi) {
+                kn2 = fmaxf(kn2, n2);
+                if (gl == 0) keys[j - lo] = float_key(s);
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+}
+
 // The sessions of a batched decode step: session s's inputs sit at fixed strides
 // from session 0's and its position is pos[s] (device memory, read early).
 struct DecodeBatch {
@@ -452,7 +514,13 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     float qf[2][8];
     float kn2 = 0.f;   // approximate path: largest squared key norm of this CTA's rows
     load_query(a.q_idx, a.d_idx, qf);
-    score_rows<kDeep, kApprox>(a, qf, j0, js, s_keys, j0, kn2);
+    if constexpr (kApprox) {
+        extern __shared__ __align__(16) unsigned char dyn_stage[];
+        if (a.d_idx <= 128) score_rows_staged(a, qf, j0, js, s_keys, kn2, dyn_stage);
+        else score_rows<kDeep, true>(a, qf, j0, js, s_keys, j0, kn2);
+    } else {
+        score_rows<kDeep, false>(a, qf, j0, js, s_keys, j0, kn2);
+    }
     pdl_wait();
     pdl_trigger();
     unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws);
@@ -631,8 +699,13 @@ cudaError_t launch_indexer_compress_batched(int B, const uint16_t *q_idx, const 
     int rows_per_cta = 0;
     const unsigned grid = decode_grid(cap * ratio, cap, ratio, per_session, rows_per_cta);
     // approximate scores with an exact band when every session's rows fit the band select
-    if (cap <= kBandMaxRows)
-        return launch(indexer_decode_kernel<true, 4, true>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a,
+    // and a CTA covers enough rows for the cheaper scoring to outweigh the band's rescoring;
+    // exact scores otherwise, one 64-row batch per round when a CTA covers two at most
+    if (cap <= kBandMaxRows && rows_per_cta >= 512)
+        return launch(indexer_decode_kernel<true, 4, true>, dim3(grid + 1, B), dim3(kThreads), kStageBytes, c, 1, a,
+                      rows_per_cta, ca, bt);
+    if (rows_per_cta <= 2 * kRowsPerCta)
+        return launch(indexer_decode_kernel<true, 1, false>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a,
                       rows_per_cta, ca, bt);
     return launch(indexer_decode_kernel<true, 4, false>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a,
                   rows_per_cta, ca, bt);
@@ -656,6 +729,9 @@ static cudaError_t configure_indexer(const Ctx &c) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, true>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kStageBytes));
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, false>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
