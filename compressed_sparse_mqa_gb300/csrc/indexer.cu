@@ -376,7 +376,7 @@ DS4A_DEVINL void score_rows(const IndexerArgs &a, const float (&qf)[2][8], long 
 // cover a thousand rows (batched steps).  Needs d_idx <= 128 (one 16-byte chunk of a
 // row per thread of its 16-thread group).  stage: kStages * kChunkRows * 256 bytes.
 constexpr int kChunkRows = 128;
-constexpr int kStages = 3;
+constexpr int kStages = 6;
 constexpr size_t kStageBytes = static_cast<size_t>(kStages) * kChunkRows * 256;
 DS4A_DEVINL void score_rows_staged(const IndexerArgs &a, const float (&qf)[2][8], long long lo, long long hi,
                                    uint32_t *keys, float &kn2, unsigned char *stage) {
@@ -448,6 +448,7 @@ struct DecodeBatch {
     long long cap;            // compressed rows allocated per session
     unsigned int *err;
     int W;
+    int comp_cta0;            // the compressor's update runs in scoring CTA 0 (no CTA of its own)
 };
 
 // one query per session: CTA x < n_score scores rows [x*rows_per_cta, (x+1)*rows_per_cta)
@@ -468,6 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     __shared__ bool s_last;
     __shared__ uint32_t s_keys[kStagedRows];
     __shared__ float s_red[kWarps];
+    __shared__ float s_cw[1];   // the compressor's score of the step's token (comp_cta0)
+    bool comp_skip = false;     // the token would complete a row past the session's capacity
     if (bt.pos != nullptr) {
         const long long sid = blockIdx.y;
         const long long p = bt.pos[sid];
@@ -478,10 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
         if (a.out_n) a.out_n += sid;
         a.ws += sid * bt.ws_stride;
         if constexpr (kCompress) {
-            if (blockIdx.x == gridDim.x - 1 && (p + 1) / c.ratio > bt.cap) {
+            if ((p + 1) / c.ratio > bt.cap) {
                 // the row this token completes is past the session's capacity: no update
-                if (threadIdx.x == 0) record_error(bt.err, DS4A_ERR_CAPACITY);
-                return;
+                comp_skip = true;
+                if (blockIdx.x == gridDim.x - 1 && !bt.comp_cta0) {
+                    if (threadIdx.x == 0) record_error(bt.err, DS4A_ERR_CAPACITY);
+                    return;
+                }
+                if (blockIdx.x == 0 && bt.comp_cta0 && threadIdx.x == 0) record_error(bt.err, DS4A_ERR_CAPACITY);
             }
             const long long slot = (p % bt.W) * c.D;
             c.pos = p;
@@ -493,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
         }
     }
     if constexpr (kCompress) {
-        if (blockIdx.x == gridDim.x - 1) {
+        if (!bt.comp_cta0 && blockIdx.x == gridDim.x - 1) {
             static_assert(sizeof(sm.scan) >= kWarps * sizeof(float), "one float per warp");
             compress_one_token(c, reinterpret_cast<float *>(s_keys), reinterpret_cast<float *>(sm.scan));
             return;
@@ -501,7 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     } else {
         (void)c;
     }
-    const unsigned int n_score = kCompress ? gridDim.x - 1 : gridDim.x;
+    // with comp_cta0, scoring CTA 0 also runs the compressor's update: its score before the
+    // dependency wait, the running state and a completed row after it
+    const bool comp_here = kCompress && bt.comp_cta0 && blockIdx.x == 0 && !comp_skip;
+    const unsigned int n_score = (kCompress && !bt.comp_cta0) ? gridDim.x - 1 : gridDim.x;
     const long long n_vis = visible_rows(a, 0);
     const long long j0 = static_cast<long long>(blockIdx.x) * rows_per_cta;
     const long long j1 = min(n_vis, j0 + rows_per_cta);
@@ -521,8 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     } else {
         score_rows<kDeep, false>(a, qf, j0, js, s_keys, j0, kn2);
     }
+    if (comp_here) cmp::segment_scores<kThreads>(c, c.pos, c.pos + 1, s_cw);
     pdl_wait();
     pdl_trigger();
+    if (comp_here) cmp::pool_segment<kThreads>(c, c.pos / c.ratio, c.pos, c.pos + 1, c.pos % c.ratio != 0, s_cw, s_red);
     unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws);
     unsigned int *kmax2_word = ticket + 1;   // approximate path: the session's largest squared key norm
     uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + kWsHeader);
@@ -691,13 +703,20 @@ cudaError_t launch_indexer_compress_batched(int B, const uint16_t *q_idx, const 
     if (e != cudaSuccess) return e;
     IndexerArgs a{q_idx, k_idx, out_idx, out_n, static_cast<unsigned char *>(ws), cap, 0, 1, d_idx, ratio, k};
     const cmp::CompressArgs ca{nullptr, nullptr, score_w, state, comp_k, comp_v, 0, 1, D, ratio};
+    // every session's CTAs in one wave when B allows: (SMs - B) / B scoring CTAs per
+    // session and one compressor CTA each; or, from 32 sessions on (where the separate
+    // CTAs would take a large share of the SMs), SMs / B scoring CTAs with the
+    // compressor's update in each session's CTA 0 (64 sessions: 131 -> 84 us per step;
+    // at 16 it measured slower).  The row split is sized for the largest row count (cap).
+    const int per_sep = c.num_sms > 2 * B ? (c.num_sms - B) / B : 1;
+    const int per_fold = c.num_sms / B > 1 ? c.num_sms / B : 1;
+    const bool fold = B >= 32 && per_fold > per_sep;
     DecodeBatch bt{pos, d_idx, cap * d_idx, k, static_cast<long long>(indexer_batched_ws_stride(cap)),
-                   ring_k, ring_v, static_cast<long long>(W) * D, 2 + 2LL * D, cap * D, cap, c.err, W};
-    // every session's scoring CTAs and its compressor CTA in one wave when B allows:
-    // (SMs - B) / B scoring CTAs per session, sized for the largest row count (cap)
-    const int per_session = c.num_sms > 2 * B ? (c.num_sms - B) / B : 1;
+                   ring_k, ring_v, static_cast<long long>(W) * D, 2 + 2LL * D, cap * D, cap, c.err, W,
+                   fold ? 1 : 0};
     int rows_per_cta = 0;
-    const unsigned grid = decode_grid(cap * ratio, cap, ratio, per_session, rows_per_cta);
+    const unsigned n_sc = decode_grid(cap * ratio, cap, ratio, fold ? per_fold : per_sep, rows_per_cta);
+    const unsigned grid = fold ? n_sc - 1 : n_sc;   // the launches below add the compressor's CTA
     // approximate scores with an exact band when every session's rows fit the band select
     // and a CTA covers enough rows for the cheaper scoring to outweigh the band's rescoring;
     // exact scores otherwise, one 64-row batch per round when a CTA covers two at most
