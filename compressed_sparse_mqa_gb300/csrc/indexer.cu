@@ -127,13 +127,13 @@ DS4A_DEVINL void score_loaded(const float (&qf)[2][8], const RowLoads &L, long l
 }
 
 // Approximate scores (fp32 FMA, error far below sel::band_select's eps) of the rows held in
-// L, as order-preserving keys, and the largest squared key norm among them (kn2).
+// L, as order-preserving keys, and the largest sum_c |q_c k_c| among them (bmax).
 DS4A_DEVINL void score_loaded_approx(const float (&qf)[2][8], const RowLoads &L, long long base, long long j1,
-                                     uint32_t *keys, float &kn2) {
+                                     uint32_t *keys, float &bmax) {
     const int tid = threadIdx.x, gl = tid % kGroup;
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-        float s = 0.f, n2 = 0.f;
+        float s = 0.f, m = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
             const uint16_t *h = reinterpret_cast<const uint16_t *>(&L.v[p][cc]);
@@ -141,17 +141,17 @@ DS4A_DEVINL void score_loaded_approx(const float (&qf)[2][8], const RowLoads &L,
             for (int e = 0; e < 8; ++e) {
                 const float kv = h2f(h[e]);
                 s = fmaf(qf[cc][e], kv, s);
-                n2 = fmaf(kv, kv, n2);
+                m = fmaf(fabsf(qf[cc][e]), fabsf(kv), m);
             }
         }
 #pragma unroll
         for (int o = kGroup / 2; o > 0; o >>= 1) {
             s += __shfl_xor_sync(0xffffffffu, s, o);
-            n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+            m += __shfl_xor_sync(0xffffffffu, m, o);
         }
         const long long j = base + p * kRowsPerPass + tid / kGroup;
         if (j < j1) {
-            kn2 = fmaxf(kn2, n2);
+            bmax = fmaxf(bmax, m);
             if (gl == 0) keys[j - base] = float_key(s);
         }
     }
@@ -351,10 +351,10 @@ DS4A_DEVINL void compress_one_token(const cmp::CompressArgs &c, float *s_w, floa
 // flight.  A single decode query spreads its rows at 64 per CTA and takes kDeep = 1:
 // the deeper round measured 0.8 us slower there.  kApprox: fp32 FMA scores (about a
 // quarter of the TwoSum arithmetic) for sel::band_select, which rescores the rows
-// near the k-th exactly; kn2 collects the largest squared key norm for its bound.
+// near the k-th exactly; bmax collects the largest sum_c |q_c k_c| for its bound.
 template <int kDeep, bool kApprox>
 DS4A_DEVINL void score_rows(const IndexerArgs &a, const float (&qf)[2][8], long long lo, long long hi,
-                           uint32_t *keys, long long kbase, float &kn2) {
+                           uint32_t *keys, long long kbase, float &bmax) {
     for (long long base = lo; base < hi; base += kDeep * kRowsPerCta) {
         RowLoads L[kDeep];
 #pragma unroll
@@ -363,7 +363,7 @@ DS4A_DEVINL void score_rows(const IndexerArgs &a, const float (&qf)[2][8], long 
         for (int u = 0; u < kDeep; ++u) {
             const long long bu = base + u * kRowsPerCta;
             if (bu < hi) {   // block-uniform
-                if constexpr (kApprox) score_loaded_approx(qf, L[u], bu, hi, keys + (bu - kbase), kn2);
+                if constexpr (kApprox) score_loaded_approx(qf, L[u], bu, hi, keys + (bu - kbase), bmax);
                 else score_loaded(qf, L[u], bu, hi, keys + (bu - kbase));
             }
         }
@@ -371,26 +371,58 @@ DS4A_DEVINL void score_rows(const IndexerArgs &a, const float (&qf)[2][8], long 
 }
 
 // Approximate scores of rows [lo, hi) into keys[j - lo], the key rows staged through
-// shared memory with 16-byte cp.async: kStages chunks of kChunkRows rows in flight,
-// far more bytes than the register rounds of score_rows keep in flight, for CTAs that
-// cover a thousand rows (batched steps).  Needs d_idx <= 128 (one 16-byte chunk of a
-// row per thread of its 16-thread group).  stage: kStages * kChunkRows * 256 bytes.
+// shared memory with 16-byte cp.async (kStages chunks of kChunkRows rows in flight: far
+// more bytes than the register rounds of score_rows keep in flight, for CTAs that cover
+// a thousand rows or more) and scored on the tensor cores: mma.sync m16n8k16 with a
+// chunk's 16-row tile as A and the query as column 0 of B, fp32 accumulation over the
+// exact fp16 products.  A second product of the absolute values gives each row's
+// sum_c |q_c k_c|; bmax collects the largest, and 2^-12 bmax bounds the error of every
+// score (far above the accumulation error of d_idx <= 128 products, each rounded once).
+// Needs d_idx a multiple of 32, <= 128.  stage: kStages * kChunkRows * 256 bytes;
+// part: 4 * kChunkRows floats.
 constexpr int kChunkRows = 128;
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr size_t kStageBytes = static_cast<size_t>(kStages) * kChunkRows * 256;
-DS4A_DEVINL void score_rows_staged(const IndexerArgs &a, const float (&qf)[2][8], long long lo, long long hi,
-                                   uint32_t *keys, float &kn2, unsigned char *stage) {
-    const int tid = threadIdx.x, gl = tid % kGroup;
-    const int n_chunks = a.d_idx / 8;   // 16-byte chunks of a row (<= 16)
+// the approximate path keeps the keys of up to this many rows per CTA in dynamic shared
+// memory before the dependency wait (after the stages)
+constexpr int kApproxStagedRows = 8192;
+constexpr size_t kApproxDynBytes = kStageBytes + kApproxStagedRows * sizeof(uint32_t);
+DS4A_DEVINL void score_rows_staged(const IndexerArgs &a, long long lo, long long hi, uint32_t *keys, float &bmax,
+                                   unsigned char *stage, float *part) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n_chunks = a.d_idx / 8;          // 16-byte chunks of a row
+    const int ksteps = a.d_idx / 32;           // 16-wide k-steps per half of d_idx
+    const int tile = warp & 7, khalf = warp >> 3;
     const long long n = hi - lo;
     const int n_tiles = static_cast<int>((n + kChunkRows - 1) / kChunkRows);
+    // B fragments: the query in column 0 (lanes 0-3 of each k-step), zeros elsewhere
+    uint32_t bq0[4], bq1[4], ba0[4], ba1[4];   // the query and its absolute values
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        bq0[s] = bq1[s] = ba0[s] = ba1[s] = 0u;
+        if (s < ksteps && (lane >> 2) == 0) {
+            const int k0 = (khalf * ksteps + s) * 16 + 2 * (lane & 3);
+            bq0[s] = *reinterpret_cast<const uint32_t *>(a.q_idx + k0);
+            bq1[s] = *reinterpret_cast<const uint32_t *>(a.q_idx + k0 + 8);
+            const __half2 x0 = __habs2(*reinterpret_cast<const __half2 *>(&bq0[s]));
+            const __half2 x1 = __habs2(*reinterpret_cast<const __half2 *>(&bq1[s]));
+            ba0[s] = *reinterpret_cast<const uint32_t *>(&x0);
+            ba1[s] = *reinterpret_cast<const uint32_t *>(&x1);
+        }
+    }
+    // chunk ch of row r sits at r * 256 + ((ch ^ (r & 7)) << 4): ldmatrix reads of 8 rows
+    // at one chunk column hit 8 different 16-byte bank groups
     auto issue = [&](int t) {
         if (t < n_tiles) {
             unsigned char *dst = stage + (t % kStages) * (kChunkRows * 256);
-            for (int i = tid; i < kChunkRows * 16; i += kThreads) {
-                const int r = i >> 4, ch = i & 15;
+            for (int i = tid; i < kChunkRows * n_chunks; i += kThreads) {
+                const int r = i / n_chunks, ch = i % n_chunks;
                 const long long j = lo + static_cast<long long>(t) * kChunkRows + r;
-                if (j < hi && ch < n_chunks) cp_async16(dst + i * 16, a.k_idx + j * a.d_idx + ch * 8);
+                const bool valid = j < hi;
+                const uint32_t sdst = static_cast<uint32_t>(__cvta_generic_to_shared(dst + r * 256 + ((ch ^ (r & 7)) << 4)));
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(sdst),
+                             "l"(a.k_idx + (valid ? j : lo) * a.d_idx + ch * 8), "r"(valid ? 16 : 0)
+                             : "memory");
             }
         }
         cp_async_commit();   // one group per tile, empty past the last
@@ -399,32 +431,39 @@ DS4A_DEVINL void score_rows_staged(const IndexerArgs &a, const float (&qf)[2][8]
     for (int t = 0; t < kStages - 1; ++t) issue(t);
     for (int t = 0; t < n_tiles; ++t) {
         cp_async_wait<kStages - 2>();   // tile t has landed (this thread's copies)
-        __syncthreads();                // ... and every thread's; tile t-1's stage is free
+        __syncthreads();                // ... and every thread's; tile t-1's stage and `part` are free
         issue(t + kStages - 1);
         const unsigned char *src = stage + (t % kStages) * (kChunkRows * 256);
+        float d[4] = {0.f, 0.f, 0.f, 0.f}, e4[4] = {0.f, 0.f, 0.f, 0.f};
+        const int r = tile * 16 + (lane & 15);   // this lane's ldmatrix row
 #pragma unroll
-        for (int pass = 0; pass < kChunkRows / kRowsPerPass; ++pass) {
-            const int r = pass * kRowsPerPass + tid / kGroup;
-            const long long j = lo + static_cast<long long>(t) * kChunkRows + r;
-            float s = 0.f, n2 = 0.f;
-            if (j < hi && gl < n_chunks) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(src + (r * 16 + gl) * 16);
-                const uint16_t *h = reinterpret_cast<const uint16_t *>(&raw);
+        for (int s = 0; s < 4; ++s) {
+            if (s < ksteps) {
+                const int ch = 2 * (khalf * ksteps + s) + (lane >> 4);
+                uint32_t af[4], aa[4];
+                ldmatrix_x4(af[0], af[1], af[2], af[3], src + r * 256 + ((ch ^ (r & 7)) << 4));
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float kv = h2f(h[e]);
-                    s = fmaf(qf[0][e], kv, s);
-                    n2 = fmaf(kv, kv, n2);
+                for (int e = 0; e < 4; ++e) {
+                    const __half2 x = __habs2(*reinterpret_cast<const __half2 *>(&af[e]));
+                    aa[e] = *reinterpret_cast<const uint32_t *>(&x);
                 }
+                mma_16816(d, af, bq0[s], bq1[s]);
+                mma_16816(e4, aa, ba0[s], ba1[s]);
             }
-#pragma unroll
-            for (int o = kGroup / 2; o > 0; o >>= 1) {
-                s += __shfl_xor_sync(0xffffffffu, s, o);
-                n2 += __shfl_xor_sync(0xffffffffu, n2, o);
-            }
+        }
+        if ((lane & 3) == 0) {   // column 0: rows lane/4 and lane/4 + 8 of the tile, this k-half
+            const int rr = tile * 16 + (lane >> 2);
+            part[khalf * kChunkRows + rr] = d[0];
+            part[khalf * kChunkRows + rr + 8] = d[2];
+            part[(2 + khalf) * kChunkRows + rr] = e4[0];
+            part[(2 + khalf) * kChunkRows + rr + 8] = e4[2];
+        }
+        __syncthreads();
+        if (tid < kChunkRows) {
+            const long long j = lo + static_cast<long long>(t) * kChunkRows + tid;
             if (j < hi) {
-                kn2 = fmaxf(kn2, n2);
-                if (gl == 0) keys[j - lo] = float_key(s);
+                keys[j - lo] = float_key(part[tid] + part[kChunkRows + tid]);
+                bmax = fmaxf(bmax, part[2 * kChunkRows + tid] + part[3 * kChunkRows + tid]);
             }
         }
     }
@@ -520,37 +559,40 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     // of the slice are scored into shared memory before waiting on the previous kernel.
     // A row the query's own token completes (which a compressor call just ahead may
     // write), the workspace and the output are read or written after the wait.
-    const long long js = max(j0, min(min(j1, j0 + kStagedRows), a.q_pos0 / a.ratio));
+    extern __shared__ __align__(16) unsigned char dyn_smem[];   // approximate path: stages, then keys
+    uint32_t *pre_keys = kApprox ? reinterpret_cast<uint32_t *>(dyn_smem + kStageBytes) : s_keys;
+    const long long pre_cap = kApprox ? kApproxStagedRows : kStagedRows;
+    const long long js = max(j0, min(min(j1, j0 + pre_cap), a.q_pos0 / a.ratio));
     float qf[2][8];
-    float kn2 = 0.f;   // approximate path: largest squared key norm of this CTA's rows
+    float bmax = 0.f;   // approximate path: largest sum_c |q_c k_c| of this CTA's rows
     load_query(a.q_idx, a.d_idx, qf);
     if constexpr (kApprox) {
-        extern __shared__ __align__(16) unsigned char dyn_stage[];
-        if (a.d_idx <= 128) score_rows_staged(a, qf, j0, js, s_keys, kn2, dyn_stage);
-        else score_rows<kDeep, true>(a, qf, j0, js, s_keys, j0, kn2);
+        __shared__ float s_part[4 * kChunkRows];
+        if (a.d_idx % 32 == 0 && a.d_idx <= 128) score_rows_staged(a, j0, js, pre_keys, bmax, dyn_smem, s_part);
+        else score_rows<kDeep, true>(a, qf, j0, js, pre_keys, j0, bmax);
     } else {
-        score_rows<kDeep, false>(a, qf, j0, js, s_keys, j0, kn2);
+        score_rows<kDeep, false>(a, qf, j0, js, pre_keys, j0, bmax);
     }
     if (comp_here) cmp::segment_scores<kThreads>(c, c.pos, c.pos + 1, s_cw);
     pdl_wait();
     pdl_trigger();
     if (comp_here) cmp::pool_segment<kThreads>(c, c.pos / c.ratio, c.pos, c.pos + 1, c.pos % c.ratio != 0, s_cw, s_red);
     unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws);
-    unsigned int *kmax2_word = ticket + 1;   // approximate path: the session's largest squared key norm
+    unsigned int *bmax_word = ticket + 1;   // approximate path: the session's largest sum_c |q_c k_c|
     uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + kWsHeader);
     __syncthreads();
-    for (long long j = j0 + threadIdx.x; j < js; j += kThreads) keys[j] = s_keys[j - j0];
-    score_rows<kDeep, kApprox>(a, qf, js, j1, keys, 0, kn2);
+    for (long long j = j0 + threadIdx.x; j < js; j += kThreads) keys[j] = pre_keys[j - j0];
+    score_rows<kDeep, kApprox>(a, qf, js, j1, keys, 0, bmax);
     if constexpr (kApprox) {
         // non-negative floats order like their bit patterns: one atomicMax per CTA
-        kn2 = warp_max(kn2);
-        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = kn2;
+        bmax = warp_max(bmax);
+        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = bmax;
         __syncthreads();
         if (threadIdx.x == 0) {
             float m = 0.f;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) m = fmaxf(m, s_red[w]);
-            atomicMax(kmax2_word, __float_as_uint(m));
+            atomicMax(bmax_word, __float_as_uint(m));
         }
     }
     // one acquire-release atomic per CTA: releases this CTA's keys (ordered before it
@@ -569,25 +611,15 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
         if (n <= a.k) {
             for (int i = threadIdx.x; i < a.k; i += kThreads) a.out_idx[i] = i < n ? i : -1;
         } else {
-            // eps bounds |approximate - exact| score for every row: 2^-12 |q| max |k|
-            if ((threadIdx.x >> 5) == 0) {
-                const int lane = threadIdx.x & 31;
-                float qn2 = 0.f;
-                for (int cidx = lane; cidx < a.d_idx; cidx += 32) {
-                    const float x = h2f(a.q_idx[cidx]);
-                    qn2 = fmaf(x, x, qn2);
-                }
-                qn2 = warp_sum(qn2);
-                if (lane == 0)
-                    u.band.eps = ldexpf(sqrtf(qn2 * __uint_as_float(__ldcg(kmax2_word))) * 1.01f, -12) + 1e-30f;
-            }
+            // eps bounds |approximate - exact| score for every row: 2^-12 max_j sum_c |q_c k_jc|
+            if (threadIdx.x == 0) u.band.eps = ldexpf(__uint_as_float(__ldcg(bmax_word)) * 1.01f, -12) + 1e-30f;
             __syncthreads();
             const float eps = u.band.eps;
             if (n <= kThreads * 8) band_select_regs<8>(a, keys, n, eps, u.band);
             else if (n <= kThreads * 16) band_select_regs<16>(a, keys, n, eps, u.band);
             else band_select_regs<kMaxItems>(a, keys, n, eps, u.band);
         }
-        if (threadIdx.x == 0) *kmax2_word = 0u;
+        if (threadIdx.x == 0) *bmax_word = 0u;
     } else {
         select_topk<true>(keys, static_cast<int>(n_vis), a.k, a.out_idx, a.out_n, sm);
     }
@@ -721,7 +753,7 @@ cudaError_t launch_indexer_compress_batched(int B, const uint16_t *q_idx, const 
     // and a CTA covers enough rows for the cheaper scoring to outweigh the band's rescoring;
     // exact scores otherwise, one 64-row batch per round when a CTA covers two at most
     if (cap <= kBandMaxRows && rows_per_cta >= 512)
-        return launch(indexer_decode_kernel<true, 4, true>, dim3(grid + 1, B), dim3(kThreads), kStageBytes, c, 1, a,
+        return launch(indexer_decode_kernel<true, 4, true>, dim3(grid + 1, B), dim3(kThreads), kApproxDynBytes, c, 1, a,
                       rows_per_cta, ca, bt);
     if (rows_per_cta <= 2 * kRowsPerCta)
         return launch(indexer_decode_kernel<true, 1, false>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a,
@@ -750,7 +782,7 @@ static cudaError_t configure_indexer(const Ctx &c) {
                                      cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kStageBytes));
+                                     static_cast<int>(kApproxDynBytes));
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, false>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
