@@ -24,6 +24,8 @@
 // waiting) selects and resets the ticket.  Many queries: the tensor-core path
 // (indexer_tc.cu) when the shapes allow it, else one CTA per query scores its
 // visible rows into shared memory and selects.
+#include <type_traits>
+
 #include "compress_dev.cuh"
 #include "ds4a_common.cuh"
 #include "ds4a_internal.h"
@@ -497,18 +499,26 @@ struct DecodeBatch {
 // session of a batched step.
 constexpr int kBandMaxRows = kThreads * kMaxItems;   // approximate path: rows per session
 
-template <bool kCompress, int kDeep, bool kApprox>
+// shared memory of the exact select, and of the band select of the approximate path
+struct ExactSmem {
+    SelectSmem sm;
+};
+union ApproxSmem {
+    SelectSmem sm;
+    sel::BandSmem<kThreads, kBandMaxRows> band;
+};
+
+// kFold: the compressor's update runs in scoring CTA 0 (DecodeBatch::comp_cta0).  The
+// single-session launches are instantiated without the batched-only paths: code and
+// shared memory they never use measured 0.4 us slower on a decode step.
+template <bool kCompress, int kDeep, bool kApprox, bool kFold>
 __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs a, int rows_per_cta,
                                                                      cmp::CompressArgs c, DecodeBatch bt) {
-    __shared__ union {
-        SelectSmem sm;
-        sel::BandSmem<kThreads, kBandMaxRows> band;
-    } u;
+    __shared__ typename std::conditional<kApprox, ApproxSmem, ExactSmem>::type u;
     SelectSmem &sm = u.sm;
     __shared__ bool s_last;
     __shared__ uint32_t s_keys[kStagedRows];
     __shared__ float s_red[kWarps];
-    __shared__ float s_cw[1];   // the compressor's score of the step's token (comp_cta0)
     bool comp_skip = false;     // the token would complete a row past the session's capacity
     if (bt.pos != nullptr) {
         const long long sid = blockIdx.y;
@@ -523,11 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
             if ((p + 1) / c.ratio > bt.cap) {
                 // the row this token completes is past the session's capacity: no update
                 comp_skip = true;
-                if (blockIdx.x == gridDim.x - 1 && !bt.comp_cta0) {
-                    if (threadIdx.x == 0) record_error(bt.err, DS4A_ERR_CAPACITY);
-                    return;
-                }
-                if (blockIdx.x == 0 && bt.comp_cta0 && threadIdx.x == 0) record_error(bt.err, DS4A_ERR_CAPACITY);
+                if (blockIdx.x == (kFold ? 0u : gridDim.x - 1) && threadIdx.x == 0)
+                    record_error(bt.err, DS4A_ERR_CAPACITY);
+                if (!kFold && blockIdx.x == gridDim.x - 1) return;
             }
             const long long slot = (p % bt.W) * c.D;
             c.pos = p;
@@ -538,8 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
             c.comp_v += sid * bt.comp_stride;
         }
     }
-    if constexpr (kCompress) {
-        if (!bt.comp_cta0 && blockIdx.x == gridDim.x - 1) {
+    if constexpr (kCompress && !kFold) {
+        if (blockIdx.x == gridDim.x - 1) {
             static_assert(sizeof(sm.scan) >= kWarps * sizeof(float), "one float per warp");
             compress_one_token(c, reinterpret_cast<float *>(s_keys), reinterpret_cast<float *>(sm.scan));
             return;
@@ -549,8 +557,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     }
     // with comp_cta0, scoring CTA 0 also runs the compressor's update: its score before the
     // dependency wait, the running state and a completed row after it
-    const bool comp_here = kCompress && bt.comp_cta0 && blockIdx.x == 0 && !comp_skip;
-    const unsigned int n_score = (kCompress && !bt.comp_cta0) ? gridDim.x - 1 : gridDim.x;
+    const bool comp_here = kCompress && kFold && blockIdx.x == 0 && !comp_skip;
+    const unsigned int n_score = (kCompress && !kFold) ? gridDim.x - 1 : gridDim.x;
+    (void)comp_skip;
     const long long n_vis = visible_rows(a, 0);
     const long long j0 = static_cast<long long>(blockIdx.x) * rows_per_cta;
     const long long j1 = min(n_vis, j0 + rows_per_cta);
@@ -573,10 +582,16 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     } else {
         score_rows<kDeep, false>(a, qf, j0, js, pre_keys, j0, bmax);
     }
-    if (comp_here) cmp::segment_scores<kThreads>(c, c.pos, c.pos + 1, s_cw);
+    __shared__ float s_cw[1];   // kFold: the compressor's score of the step's token
+    if constexpr (kFold) {
+        if (comp_here) cmp::segment_scores<kThreads>(c, c.pos, c.pos + 1, s_cw);
+    }
     pdl_wait();
     pdl_trigger();
-    if (comp_here) cmp::pool_segment<kThreads>(c, c.pos / c.ratio, c.pos, c.pos + 1, c.pos % c.ratio != 0, s_cw, s_red);
+    if constexpr (kFold) {
+        if (comp_here)
+            cmp::pool_segment<kThreads>(c, c.pos / c.ratio, c.pos, c.pos + 1, c.pos % c.ratio != 0, s_cw, s_red);
+    }
     unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws);
     unsigned int *bmax_word = ticket + 1;   // approximate path: the session's largest sum_c |q_c k_c|
     uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + kWsHeader);
@@ -694,7 +709,7 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
     if (n_q == 1) {
         int rows_per_cta = 0;
         const unsigned grid = decode_grid(q_pos0, n_rows, ratio, c.num_sms, rows_per_cta);
-        return launch(indexer_decode_kernel<false, 1, false>, dim3(grid), dim3(kThreads), 0, c, 1, a, rows_per_cta,
+        return launch(indexer_decode_kernel<false, 1, false, false>, dim3(grid), dim3(kThreads), 0, c, 1, a, rows_per_cta,
                       cmp::CompressArgs{}, DecodeBatch{});
     }
     if (indexer_prefill_tc_ok(n_q, n_rows, d_idx))
@@ -716,7 +731,7 @@ cudaError_t launch_indexer_compress(const uint16_t *q_idx, const uint16_t *k_idx
     int rows_per_cta = 0;
     // the scoring CTAs leave one SM for the compressor's CTA
     const unsigned grid = decode_grid(q_pos, n_rows, ratio, c.num_sms > 1 ? c.num_sms - 1 : 1, rows_per_cta);
-    return launch(indexer_decode_kernel<true, 1, false>, dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
+    return launch(indexer_decode_kernel<true, 1, false, false>, dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
                   DecodeBatch{});
 }
 
@@ -742,7 +757,7 @@ cudaError_t launch_indexer_compress_batched(int B, const uint16_t *q_idx, const 
     // at 16 it measured slower).  The row split is sized for the largest row count (cap).
     const int per_sep = c.num_sms > 2 * B ? (c.num_sms - B) / B : 1;
     const int per_fold = c.num_sms / B > 1 ? c.num_sms / B : 1;
-    const bool fold = B >= 32 && per_fold > per_sep;
+    const bool fold = B >= 32 && per_fold > per_sep && cap <= kBandMaxRows;   // folded: approximate path only
     DecodeBatch bt{pos, d_idx, cap * d_idx, k, static_cast<long long>(indexer_batched_ws_stride(cap)),
                    ring_k, ring_v, static_cast<long long>(W) * D, 2 + 2LL * D, cap * D, cap, c.err, W,
                    fold ? 1 : 0};
@@ -752,13 +767,17 @@ cudaError_t launch_indexer_compress_batched(int B, const uint16_t *q_idx, const 
     // approximate scores with an exact band when every session's rows fit the band select
     // and a CTA covers enough rows for the cheaper scoring to outweigh the band's rescoring;
     // exact scores otherwise, one 64-row batch per round when a CTA covers two at most
-    if (cap <= kBandMaxRows && rows_per_cta >= 512)
-        return launch(indexer_decode_kernel<true, 4, true>, dim3(grid + 1, B), dim3(kThreads), kApproxDynBytes, c, 1, a,
-                      rows_per_cta, ca, bt);
+    if (cap <= kBandMaxRows && rows_per_cta >= 512) {
+        if (fold)
+            return launch(indexer_decode_kernel<true, 4, true, true>, dim3(grid + 1, B), dim3(kThreads),
+                          kApproxDynBytes, c, 1, a, rows_per_cta, ca, bt);
+        return launch(indexer_decode_kernel<true, 4, true, false>, dim3(grid + 1, B), dim3(kThreads), kApproxDynBytes,
+                      c, 1, a, rows_per_cta, ca, bt);
+    }
     if (rows_per_cta <= 2 * kRowsPerCta)
-        return launch(indexer_decode_kernel<true, 1, false>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a,
+        return launch(indexer_decode_kernel<true, 1, false, false>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a,
                       rows_per_cta, ca, bt);
-    return launch(indexer_decode_kernel<true, 4, false>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a,
+    return launch(indexer_decode_kernel<true, 4, false, false>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a,
                   rows_per_cta, ca, bt);
 }
 
@@ -772,19 +791,21 @@ static cudaError_t configure_indexer(const Ctx &c) {
         cudaError_t e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kQuerySmem));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel<false, 1, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(indexer_decode_kernel<false, 1, false, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 1, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 1, false, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
+        for (auto kern : {indexer_decode_kernel<true, 4, true, false>, indexer_decode_kernel<true, 4, true, true>}) {
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kApproxDynBytes));
+        }
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, true>,
-                                     cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kApproxDynBytes));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, false>,
+            e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, false, false>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
