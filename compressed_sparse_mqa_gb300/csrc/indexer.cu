@@ -302,6 +302,23 @@ __device__ void select_topk(const uint32_t *src, int n, int k, int32_t *out, int
     if (out_n && threadIdx.x == 0) *out_n = n < k ? n : k;
 }
 
+// select_topk with the register-select size fixed at compile time (kItems 8, 16 or 32
+// keys a thread, for n <= 512 kItems), or the run-time choice (kItems 0): a decode
+// launch whose row count the host knows carries only the select it needs.
+template <int kItems>
+__device__ void select_topk_sized(const uint32_t *src, int n, int k, int32_t *out, int32_t *out_n, SelectSmem &sm) {
+    if constexpr (kItems == 0) {
+        select_topk<true>(src, n, k, out, out_n, sm);
+    } else {
+        if (n <= k) {
+            for (int i = threadIdx.x; i < k; i += kThreads) out[i] = i < n ? i : -1;
+        } else {
+            select_regs<kItems, true>(src, n, k, out, sm);
+        }
+        if (out_n && threadIdx.x == 0) *out_n = n < k ? n : k;
+    }
+}
+
 // ---- kernels -----------------------------------------------------------------------------
 
 struct IndexerArgs {
@@ -511,7 +528,7 @@ union ApproxSmem {
 // kFold: the compressor's update runs in scoring CTA 0 (DecodeBatch::comp_cta0).  The
 // single-session launches are instantiated without the batched-only paths: code and
 // shared memory they never use measured 0.4 us slower on a decode step.
-template <bool kCompress, int kDeep, bool kApprox, bool kFold>
+template <bool kCompress, int kDeep, bool kApprox, bool kFold, int kSelItems = 0>
 __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs a, int rows_per_cta,
                                                                      cmp::CompressArgs c, DecodeBatch bt) {
     __shared__ typename std::conditional<kApprox, ApproxSmem, ExactSmem>::type u;
@@ -636,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
         }
         if (threadIdx.x == 0) *bmax_word = 0u;
     } else {
-        select_topk<true>(keys, static_cast<int>(n_vis), a.k, a.out_idx, a.out_n, sm);
+        select_topk_sized<kSelItems>(keys, static_cast<int>(n_vis), a.k, a.out_idx, a.out_n, sm);
     }
     if (threadIdx.x == 0) *ticket = 0u;
 }
@@ -698,6 +715,25 @@ static unsigned decode_grid(long long q_pos, long long n_rows, int ratio, int sm
 
 static cudaError_t configure_indexer(const Ctx &c);
 
+// the register-select size a one-query launch over n_vis rows needs (0: the run-time choice)
+static int sel_items_for(long long n_vis) {
+    if (n_vis <= kThreads * 8LL) return 8;
+    if (n_vis <= kThreads * 16LL) return 16;
+    if (n_vis <= kThreads * static_cast<long long>(kMaxItems)) return kMaxItems;
+    return 0;
+}
+
+// a one-query decode kernel (kCompress: with the compressor's CTA) with the select its rows need
+template <bool kCompress>
+static auto decode_kernel_for(long long n_vis) {
+    switch (sel_items_for(n_vis)) {
+        case 8: return indexer_decode_kernel<kCompress, 1, false, false, 8>;
+        case 16: return indexer_decode_kernel<kCompress, 1, false, false, 16>;
+        case kMaxItems: return indexer_decode_kernel<kCompress, 1, false, false, kMaxItems>;
+        default: return indexer_decode_kernel<kCompress, 1, false, false, 0>;
+    }
+}
+
 cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
                            int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
                            int32_t *out_n, void *ws, const Ctx &c) {
@@ -709,7 +745,8 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
     if (n_q == 1) {
         int rows_per_cta = 0;
         const unsigned grid = decode_grid(q_pos0, n_rows, ratio, c.num_sms, rows_per_cta);
-        return launch(indexer_decode_kernel<false, 1, false, false>, dim3(grid), dim3(kThreads), 0, c, 1, a, rows_per_cta,
+        const long long n_vis = (q_pos0 + 1) / ratio < n_rows ? (q_pos0 + 1) / ratio : n_rows;
+        return launch(decode_kernel_for<false>(n_vis), dim3(grid), dim3(kThreads), 0, c, 1, a, rows_per_cta,
                       cmp::CompressArgs{}, DecodeBatch{});
     }
     if (indexer_prefill_tc_ok(n_q, n_rows, d_idx))
@@ -731,7 +768,8 @@ cudaError_t launch_indexer_compress(const uint16_t *q_idx, const uint16_t *k_idx
     int rows_per_cta = 0;
     // the scoring CTAs leave one SM for the compressor's CTA
     const unsigned grid = decode_grid(q_pos, n_rows, ratio, c.num_sms > 1 ? c.num_sms - 1 : 1, rows_per_cta);
-    return launch(indexer_decode_kernel<true, 1, false, false>, dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
+    const long long n_vis = (q_pos + 1) / ratio < n_rows ? (q_pos + 1) / ratio : n_rows;
+    return launch(decode_kernel_for<true>(n_vis), dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
                   DecodeBatch{});
 }
 
@@ -790,9 +828,12 @@ static cudaError_t configure_indexer(const Ctx &c) {
     if (configured_device != dev) {
         cudaError_t e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kQuerySmem));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(indexer_decode_kernel<false, 1, false, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
+        for (long long n_vis : {1LL * kThreads * 8, 1LL * kThreads * 16, 1LL * kThreads * kMaxItems, 1LL << 40}) {
+            for (auto kern : {decode_kernel_for<false>(n_vis), decode_kernel_for<true>(n_vis)})
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared);
+        }
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(indexer_decode_kernel<true, 1, false, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
