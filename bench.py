@@ -25,6 +25,7 @@ decode layer, the 2048-token prefill chunk and the 43-layer decode stack.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -289,65 +290,36 @@ def run_ours(args, rank, world, local):
     return line
 
 
-def loaded_cudart():
-    """The CUDA runtime library this process already has loaded (torch's), opened by
-    its own path so that its streams are torch's; None if there is none to reuse."""
-    import ctypes
-    try:
-        with open("/proc/self/maps") as f:
-            paths = [line.split()[-1] for line in f if "libcudart.so" in line]
-    except OSError:
-        return None
-    if not paths:
-        return None
-    rt = ctypes.CDLL(paths[0])
-    rt.cudaMemcpyAsync.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
-    rt.cudaStreamSynchronize.argtypes = [ctypes.c_void_p]
-    return rt
-
-
 def run_e2e(layers, stream, n_steps):
-    """Steps through the public API with the step's inputs copied in from pinned host
-    memory and the output read back, every step, on the host clock.  Each layer's
-    step is marshalled once (DecodeLayer.bind); the copies are cudaMemcpyAsync calls
-    on the step's stream (torch copies if the runtime library is not reachable)."""
+    """Steps through the public API with the step's inputs in pinned host memory and the
+    output read back, every step, on the host clock: one ds4a_decode_layer_step call per
+    step copies the token's K and V, the query and the indexer query in, runs the
+    layer's launches, copies the output out and waits for it (DecodeLayer.bind_host
+    marshals each layer copy's call once)."""
     import torch
 
     from compressed_sparse_mqa_gb300 import ds4a
     R = len(layers)
     L0 = layers[0]
     q_h = L0.q.cpu().pin_memory()
-    k_h = L0.ring_k[L0.slot:L0.slot + 1].cpu().pin_memory()
-    v_h = L0.ring_v[L0.slot:L0.slot + 1].cpu().pin_memory()
-    qi_h = L0.q_idx.cpu().pin_memory()
+    k_h = L0.ring_k[L0.slot].cpu().pin_memory()
+    v_h = L0.ring_v[L0.slot].cpu().pin_memory()
+    qi_h = L0.q_idx.cpu().pin_memory() if L0.topk else None
+    kt_h = L0.ki_tok.cpu().pin_memory() if L0.pooled_keys else None
     out_h = torch.empty_like(L0.out, device="cpu").pin_memory()
-    ins = [(q_h, lambda L: L.q), (k_h, lambda L: L.ring_k[L.slot:L.slot + 1]),
-           (v_h, lambda L: L.ring_v[L.slot:L.slot + 1]), (qi_h, lambda L: L.q_idx)]
-    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
+    ins = [h for h in (q_h, k_h, v_h, qi_h, kt_h) if h is not None]
+    h2d = sum(h.numel() * h.element_size() for h in ins)
     d2h = out_h.numel() * out_h.element_size()
-    rt = loaded_cudart()
-    sh = stream.cuda_stream
-    with torch.cuda.stream(stream):
-        bound = [L.bind() for L in layers]
-    copies = [[(dst(L).data_ptr(), h.data_ptr(), h.numel() * h.element_size()) for h, dst in ins] for L in layers]
+    bound = [L.bind_host(k_h, v_h, q_h, qi_h, out_h, ki_tok=kt_h, stream=stream) for L in layers]
+    # each step's inputs are written into the pinned buffers by the host first, as a
+    # caller producing them would (so no step reads inputs the GPU has seen before)
+    keep = [h.clone() for h in ins]
+    srcs = [(h.data_ptr(), s.data_ptr(), h.numel() * h.element_size()) for h, s in zip(ins, keep)]
 
     def one(t):
-        L = layers[t % R]
-        if rt is None:
-            for h, dst in ins:
-                dst(L).copy_(h, non_blocking=True)
-            bound[t % R]()
-            out_h.copy_(L.out, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-            return
-        for dst, src, n in copies[t % R]:
-            if rt.cudaMemcpyAsync(dst, src, n, 1, sh) != 0:
-                raise RuntimeError("cudaMemcpyAsync (host to device) failed")
+        for dst, src, n in srcs:
+            ctypes.memmove(dst, src, n)
         bound[t % R]()
-        if rt.cudaMemcpyAsync(out_h.data_ptr(), L.out.data_ptr(), d2h, 2, sh) != 0:
-            raise RuntimeError("cudaMemcpyAsync (device to host) failed")
-        if rt.cudaStreamSynchronize(sh) != 0:
-            raise RuntimeError("cudaStreamSynchronize failed")
 
     with torch.cuda.stream(stream):
         for t in range(20):
@@ -358,9 +330,10 @@ def run_e2e(layers, stream, n_steps):
             one(t)
         dt = time.perf_counter() - t0
     assert ds4a.ds4a_last_device_error() == 0
-    how = ("C-ABI calls marshalled once per layer (DecodeLayer.bind); "
-           + ("cudaMemcpyAsync" if rt is not None else "torch copies")
-           + " of q, new k/v and indexer query from pinned memory; D2H of out; stream sync each step; host clock")
+    how = ("per step: the host writes the token's K and V, q and the indexer query into pinned buffers, then one "
+           "ds4a_decode_layer_step call (marshalled once per layer copy): a kernel reads the pinned inputs over "
+           "the host link into the layer's arrays, the step's launches, the attention kernel writes out into a "
+           "pinned buffer, stream sync; host clock")
     return {"value": round(n_steps / dt, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n_steps, "how": how}
 

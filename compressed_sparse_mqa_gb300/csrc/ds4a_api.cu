@@ -379,6 +379,158 @@ int ds4a_compress_attn_decode_batched(int B, const float *score_w, int ratio, fl
                                                       nullptr, 0, ratio, scale, out, score_w, state, c));
 }
 
+// ---- one decode step of one layer from host memory ------------------------------------------
+
+// Every check that the calls ds4a_decode_layer_step makes would make, done before
+// anything is enqueued (so that a failing call leaves the device arrays as they were).
+static int check_layer(const ds4a_decode_layer_t *L, long long pos) {
+    if (!L || pos < 0) return DS4A_ERR_ARG;
+    int rc = check_heads(L->H, L->D);
+    if (rc != DS4A_OK) return rc;
+    if (L->W < 1 || L->W > 4096 || L->ratio < 0 || L->topk < 0 || L->cap < 0) return DS4A_ERR_ARG;
+    if (L->ratio > 1024 || L->topk > 2048) return DS4A_ERR_UNSUPPORTED;
+    if ((L->topk > 0 && L->ratio == 0) || (L->pooled_keys && L->topk == 0)) return DS4A_ERR_ARG;
+    if (!L->ring_k || !L->ring_v || !L->q || !L->out) return DS4A_ERR_ARG;
+    if (!aligned(L->ring_k, 16) || !aligned(L->ring_v, 16) || !aligned(L->q, 16) || !aligned(L->out, 16))
+        return DS4A_ERR_ARG;
+    if (L->ratio > 0) {
+        if (!L->score_w || !L->state || !L->comp_k || !L->comp_v) return DS4A_ERR_ARG;
+        if (!aligned(L->score_w, 4) || !aligned(L->state, 4) || !aligned(L->comp_k, 16) || !aligned(L->comp_v, 16))
+            return DS4A_ERR_ARG;
+        if ((pos + 1) / L->ratio > L->cap) return DS4A_ERR_CAPACITY;
+        if (L->W + (pos + 1) / L->ratio > 0x7fffffffLL) return DS4A_ERR_UNSUPPORTED;
+    }
+    if (L->topk > 0) {
+        if (L->d_idx < 8 || L->d_idx > 256 || L->d_idx % 8 != 0 || L->cap > 0x7fffffffLL) return DS4A_ERR_UNSUPPORTED;
+        if (!L->q_idx || !L->out_idx || (L->cap > 0 && !L->k_idx) || (L->pooled_keys && !L->k_idx_tok))
+            return DS4A_ERR_ARG;
+        if (!aligned(L->q_idx, 16) || !aligned(L->k_idx, 16) || !aligned(L->k_idx_tok, 16) ||
+            !aligned(L->out_idx, 4) || !aligned(L->out_n, 4))
+            return DS4A_ERR_ARG;
+        if (!L->ws || !aligned(L->ws, 16) || L->ws_bytes < ds4a::indexer_ws_bytes(1, L->cap, L->topk))
+            return DS4A_ERR_WORKSPACE;
+    }
+    return DS4A_OK;
+}
+
+// The device-visible address of a page-locked (or registered) host buffer, or nullptr
+// for any other pointer.
+static const void *device_view(const void *p) {
+    if (!p) return nullptr;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+int ds4a_decode_layer_step(const ds4a_decode_layer_t *L, long long pos, const ds4a_decode_host_inputs_t *in,
+                           uint16_t *out_host, void *stream) {
+    int rc = check_layer(L, pos);
+    if (rc != DS4A_OK) return rc;
+    const int H = L->H, D = L->D;
+    const long long slot = pos % L->W;
+    const int n_win = static_cast<int>(pos + 1 < L->W ? pos + 1 : L->W);
+    uint16_t *k_new = L->ring_k + slot * D;
+    uint16_t *v_new = L->ring_v + slot * D;
+    ds4a::Ctx c;
+    rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+
+    // the token's inputs, each to its device array
+    const unsigned row = static_cast<unsigned>(D) * 2, idx_row = static_cast<unsigned>(L->d_idx) * 2;
+    ds4a::IngestArgs ing{};
+    auto add = [&](void *dst, const void *src, unsigned n) {
+        if (src) ing.seg[ing.n++] = ds4a::IngestSeg{src, dst, n};
+    };
+    if (in) {
+        add(k_new, in->k, row);
+        add(v_new, in->v, row);
+        add(L->q, in->q, static_cast<unsigned>(H) * row);
+        if (L->topk > 0) {
+            add(L->q_idx, in->q_idx, idx_row);
+            if (L->pooled_keys) add(L->k_idx_tok, in->k_idx_tok, idx_row);
+            else if ((pos + 1) % L->ratio == 0)
+                add(L->k_idx + ((pos + 1) / L->ratio - 1) * L->d_idx, in->k_idx_row, idx_row);
+        }
+    }
+    // Page-locked inputs: one kernel reads them over the host link and writes the arrays.
+    // On an indexer layer the first kernel after it reads its own inputs (the indexer
+    // query, the token's K, V and indexer key) from the host buffers and runs beside it;
+    // the kernel after that starts once it has finished.  On the other layers the first
+    // kernel reads window rows early, so it is launched without programmatic dependence
+    // and starts once the input kernel has finished.  Other host memory: one copy each.
+    ds4a::IngestArgs views = ing;
+    bool mapped = true;
+    for (int s = 0; s < ing.n && mapped; ++s) mapped = (views.seg[s].src = device_view(ing.seg[s].src)) != nullptr;
+    const uint16_t *q_idx_r = L->q_idx, *k_r = k_new, *v_r = v_new, *ki_tok_r = L->k_idx_tok;
+    ds4a::Ctx c_first = c;
+    if (ing.n > 0 && mapped) {
+        if (ds4a::launch_ingest(views, c) != cudaSuccess) {
+            cudaGetLastError();
+            return DS4A_ERR_CUDA;
+        }
+        if (L->topk > 0) {
+            auto view = [](const uint16_t *host, const uint16_t *dflt) {
+                return host ? static_cast<const uint16_t *>(device_view(host)) : dflt;
+            };
+            q_idx_r = view(in->q_idx, q_idx_r);
+            k_r = view(in->k, k_r);
+            v_r = view(in->v, v_r);
+            if (L->pooled_keys) ki_tok_r = view(in->k_idx_tok, ki_tok_r);
+        } else {
+            c_first.pdl = false;
+        }
+    } else {
+        for (int s = 0; s < ing.n; ++s)
+            if (cudaMemcpyAsync(ing.seg[s].dst, ing.seg[s].src, ing.seg[s].bytes, cudaMemcpyHostToDevice, c.stream) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                return DS4A_ERR_CUDA;
+            }
+    }
+    // a page-locked output buffer is written by the attention kernel directly
+    const void *out_view = device_view(out_host);
+    const bool out_direct = out_view != nullptr && aligned(out_view, 16);
+    uint16_t *out = out_direct ? static_cast<uint16_t *>(const_cast<void *>(out_view)) : L->out;
+
+    // the step's launches (the device calls' launchers; every check has passed)
+    cudaError_t e = cudaSuccess;
+    if (L->topk > 0) {
+        if (L->pooled_keys) {
+            e = ds4a::launch_compress(k_r, v_r, 1, D, L->score_w, L->ratio, pos, L->state, L->comp_k, L->comp_v,
+                                      c_first, ki_tok_r, L->k_idx, L->d_idx);
+            if (e == cudaSuccess)
+                e = ds4a::launch_indexer(q_idx_r, 1, L->k_idx, L->cap, L->d_idx, pos, L->ratio, L->topk, L->out_idx,
+                                         L->out_n, L->ws, c);
+        } else {
+            e = ds4a::launch_indexer_compress(q_idx_r, L->k_idx, L->cap, L->d_idx, pos, L->ratio, L->topk, L->out_idx,
+                                              L->out_n, L->ws, k_r, v_r, D, L->score_w, L->state, L->comp_k,
+                                              L->comp_v, c_first);
+        }
+        if (e == cudaSuccess)
+            e = ds4a::launch_attn_decode(L->q, H, D, L->ring_k, L->ring_v, n_win, L->comp_k, L->comp_v, L->cap,
+                                         L->out_idx, L->topk, L->scale, out, c);
+    } else if (L->ratio > 0) {
+        e = ds4a::launch_compress_attn_decode(k_new, v_new, L->score_w, L->ratio, pos, L->state, L->q, H, D, L->ring_k,
+                                              L->ring_v, n_win, L->comp_k, L->comp_v, L->scale, out, c_first);
+    } else {
+        e = ds4a::launch_attn_decode(L->q, H, D, L->ring_k, L->ring_v, n_win, nullptr, nullptr, 0, nullptr, 0,
+                                     L->scale, out, c_first);
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    if (out_host) {
+        if ((!out_direct && cudaMemcpyAsync(out_host, L->out, static_cast<size_t>(H) * row, cudaMemcpyDeviceToHost,
+                                            c.stream) != cudaSuccess) ||
+            cudaStreamSynchronize(c.stream) != cudaSuccess) {
+            cudaGetLastError();
+            return DS4A_ERR_CUDA;
+        }
+    }
+    return DS4A_OK;
+}
+
 }  // extern "C"
 
 // ---- indexer entry point that allocates nothing -------------------------------------------

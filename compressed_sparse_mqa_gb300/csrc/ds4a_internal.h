@@ -85,6 +85,20 @@ cudaError_t launch_attn_prefill(const uint16_t *q, int T, int H, int D, const ui
                                 const int32_t *sel, int k_stride, long long q_pos0, int ratio,
                                 float scale, uint16_t *out, const Ctx &c);
 
+// ds4a_decode_layer_step's input kernel: up to kIngestSegs copies from device-visible
+// (page-locked, mapped) host memory into device arrays; sizes are even byte counts
+constexpr int kIngestSegs = 6;
+struct IngestSeg {
+    const void *src;
+    void *dst;
+    unsigned bytes;
+};
+struct IngestArgs {
+    IngestSeg seg[kIngestSegs];
+    int n;
+};
+cudaError_t launch_ingest(const IngestArgs &a, const Ctx &c);
+
 // measurement kernel: gather n_idx rows table[idx[i]] (D fp16 each) into shared memory
 cudaError_t launch_gather_probe(const uint16_t *table, long long n_table, int D, const int32_t *idx, long long n_idx,
                                 unsigned int *sink, const Ctx &c);

@@ -1,9 +1,9 @@
 """Thin ctypes binding of libds4a.so (include/ds4a.h).
 
-Argument marshalling only: every function takes torch CUDA tensors, checks
-dtype / contiguity / device, passes raw device pointers and the current CUDA
-stream to the C entry point of the same name, and raises Ds4aError on a non-zero
-status.  All arithmetic runs in the library's CUDA kernels.  There is no CPU
+Argument marshalling only: every function takes torch CUDA tensors (the host
+inputs and output of ds4a_decode_layer_step: CPU tensors), checks dtype /
+contiguity / device, passes raw pointers and the current CUDA stream to the C
+entry point of the same name, and raises Ds4aError on a non-zero status.  All arithmetic runs in the library's CUDA kernels.  There is no CPU
 fallback: if the library has not been built, loading it raises.
 """
 from __future__ import annotations
@@ -31,7 +31,7 @@ EXPORTED = ["ds4a_status_str", "ds4a_last_device_error", "ds4a_compress_append",
             "ds4a_attn_prefill", "ds4a_indexer_topk_compress", "ds4a_compress_attn_decode",
             "ds4a_indexer_topk_noalloc", "ds4a_test_set_wait_limit", "ds4a_compress_append_keys",
             "ds4a_decode_batched_workspace_bytes", "ds4a_indexer_topk_compress_batched", "ds4a_attn_decode_batched",
-            "ds4a_compress_attn_decode_batched", "ds4a_probe_gather"]
+            "ds4a_compress_attn_decode_batched", "ds4a_probe_gather", "ds4a_decode_layer_step"]
 
 
 class Ds4aError(RuntimeError):
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.ds4a_indexer_workspace_bytes.restype = SZ
         L.ds4a_attn_decode.argtypes = [P, I, I, P, P, I, P, P, LL, P, I, F, P, P, SZ, P]
         L.ds4a_attn_prefill.argtypes = [P, I, I, I, P, P, I, I, P, P, LL, P, I, LL, I, F, P, P, SZ, P]
+        L.ds4a_decode_layer_step.argtypes = [ctypes.POINTER(DecodeLayerDesc), LL, ctypes.POINTER(DecodeHostInputs),
+                                             P, P]
         for name in EXPORTED:
             if name not in ("ds4a_status_str", "ds4a_indexer_workspace_bytes", "ds4a_decode_batched_workspace_bytes"):
                 getattr(L, name).restype = I
@@ -369,6 +371,100 @@ def ds4a_compress_attn_decode_batched(score_w, ratio: int, state, comp_k, comp_v
     _check(lib().ds4a_compress_attn_decode_batched(*args), "ds4a_compress_attn_decode_batched")
 
 
+# ---- one decode step of one layer from host memory --------------------------------------------
+
+class DecodeLayerDesc(ctypes.Structure):
+    """ds4a_decode_layer_t: a layer's persistent device arrays (see decode_layer_desc)."""
+    _fields_ = [("H", ctypes.c_int), ("D", ctypes.c_int), ("W", ctypes.c_int), ("ratio", ctypes.c_int),
+                ("topk", ctypes.c_int), ("d_idx", ctypes.c_int), ("pooled_keys", ctypes.c_int),
+                ("scale", ctypes.c_float), ("cap", ctypes.c_longlong),
+                ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p), ("score_w", ctypes.c_void_p),
+                ("state", ctypes.c_void_p), ("comp_k", ctypes.c_void_p), ("comp_v", ctypes.c_void_p),
+                ("k_idx", ctypes.c_void_p), ("q", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
+                ("k_idx_tok", ctypes.c_void_p), ("out_idx", ctypes.c_void_p), ("out_n", ctypes.c_void_p),
+                ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t), ("out", ctypes.c_void_p)]
+
+
+class DecodeHostInputs(ctypes.Structure):
+    """ds4a_decode_host_inputs_t: host pointers of one step's inputs (None: already on the device)."""
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("q", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
+                ("k_idx_row", ctypes.c_void_p), ("k_idx_tok", ctypes.c_void_p)]
+
+
+def _host_ptr(t, dtype, numel, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) torch tensor")
+    if t.dtype != dtype or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous {dtype} tensor")
+    if t.numel() != numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+    return t.data_ptr()
+
+
+def decode_layer_desc(ring_k, ring_v, q, out, scale: float, ratio: int = 0, score_w=None, state=None, comp_k=None,
+                      comp_v=None, topk: int = 0, k_idx=None, q_idx=None, out_idx=None, out_n=None, ws=None,
+                      k_idx_tok=None) -> DecodeLayerDesc:
+    """The ds4a_decode_layer_t of a layer's device tensors: ring_k, ring_v [W, D], q and
+    out [H, D] fp16; on a compressing layer score_w [D] and state float, comp_k, comp_v
+    [cap, D] fp16; on an indexer layer k_idx [>= cap, d_idx], q_idx [d_idx], out_idx
+    [topk] int32, out_n or None, ws uint8, and k_idx_tok [d_idx] when the compressor
+    pools the indexer keys.  The descriptor holds the tensors' addresses: keep them alive."""
+    H, D = q.shape
+    W = ring_k.shape[0]
+    if ring_k.shape != (W, D) or ring_v.shape != (W, D) or out.shape != q.shape:
+        raise ValueError("decode_layer_desc: ring / output shapes")
+    desc = DecodeLayerDesc(H=H, D=D, W=W, ratio=ratio, topk=topk, scale=scale,
+                           ring_k=_ptr(ring_k, torch.float16, "ring_k"), ring_v=_ptr(ring_v, torch.float16, "ring_v"),
+                           q=_ptr(q, torch.float16, "q"), out=_ptr(out, torch.float16, "out"))
+    if ratio:
+        if comp_k.shape != comp_v.shape or comp_k.shape[1] != D or score_w.numel() != D:
+            raise ValueError("decode_layer_desc: compressed-row / score_w shapes")
+        desc.cap = comp_k.shape[0]
+        desc.score_w = _ptr(score_w, torch.float32, "score_w")
+        desc.state = _ptr(state, torch.float32, "state")
+        desc.comp_k = _ptr(comp_k, torch.float16, "comp_k")
+        desc.comp_v = _ptr(comp_v, torch.float16, "comp_v")
+    if topk:
+        d_idx = q_idx.numel()
+        if k_idx.shape[0] < desc.cap or k_idx.shape[1] != d_idx or out_idx.numel() < topk:
+            raise ValueError("decode_layer_desc: indexer shapes")
+        desc.d_idx = d_idx
+        desc.k_idx = _ptr(k_idx, torch.float16, "k_idx")
+        desc.q_idx = _ptr(q_idx, torch.float16, "q_idx")
+        desc.out_idx = _ptr(out_idx, torch.int32, "out_idx")
+        desc.out_n = _ptr(out_n, torch.int32, "out_n", optional=True)
+        desc.ws = _ptr(ws, torch.uint8, "ws")
+        desc.ws_bytes = ws.numel()
+        if k_idx_tok is not None:
+            desc.pooled_keys = 1
+            desc.k_idx_tok = _ptr(k_idx_tok, torch.float16, "k_idx_tok")
+    return desc
+
+
+def _marshal_decode_layer_step(desc: DecodeLayerDesc, pos: int, k=None, v=None, q=None, q_idx=None, k_idx_row=None,
+                               k_idx_tok=None, out_host=None, stream=None):
+    D, d = desc.D, desc.d_idx
+    f16 = torch.float16
+    ins = DecodeHostInputs(k=_host_ptr(k, f16, D, "k"), v=_host_ptr(v, f16, D, "v"),
+                           q=_host_ptr(q, f16, desc.H * D, "q"), q_idx=_host_ptr(q_idx, f16, d, "q_idx"),
+                           k_idx_row=_host_ptr(k_idx_row, f16, d, "k_idx_row"),
+                           k_idx_tok=_host_ptr(k_idx_tok, f16, d, "k_idx_tok"))
+    return (ctypes.byref(desc), pos, ctypes.byref(ins), _host_ptr(out_host, f16, desc.H * D, "out_host"),
+            _stream(stream))
+
+
+def ds4a_decode_layer_step(desc: DecodeLayerDesc, pos: int, k=None, v=None, q=None, q_idx=None, k_idx_row=None,
+                           k_idx_tok=None, out_host=None, stream=None):
+    """The decode step of the token at pos from host tensors (contiguous fp16 CPU
+    tensors, page-locked for asynchronous copies; None: that input is already on the
+    device); the output is copied into out_host ([H, D] fp16, CPU) and the stream waited
+    for, unless out_host is None."""
+    args = _marshal_decode_layer_step(desc, pos, k, v, q, q_idx, k_idx_row, k_idx_tok, out_host, stream)
+    _check(lib().ds4a_decode_layer_step(*args), "ds4a_decode_layer_step")
+
+
 _MARSHAL = {"ds4a_attn_decode": _marshal_attn_decode,
             "ds4a_indexer_topk_compress_batched": _marshal_indexer_topk_compress_batched,
             "ds4a_attn_decode_batched": _marshal_attn_decode_batched,
@@ -376,7 +472,8 @@ _MARSHAL = {"ds4a_attn_decode": _marshal_attn_decode,
             "ds4a_indexer_topk": _marshal_indexer_topk,
             "ds4a_compress_append_keys": _marshal_compress_append_keys,
             "ds4a_compress_attn_decode": _marshal_compress_attn_decode,
-            "ds4a_indexer_topk_compress": _marshal_indexer_topk_compress}
+            "ds4a_indexer_topk_compress": _marshal_indexer_topk_compress,
+            "ds4a_decode_layer_step": _marshal_decode_layer_step}
 
 
 def bind(name: str, *args, **kwargs):

@@ -168,6 +168,29 @@ class DecodeLayer:
         keep the position they were bound at: bind again after advancing.
         """
         p = self.p + 1
+        n_vis, completes = self._check_next(p, q_idx, kidx_row, ki_tok)
+        cur = torch.cuda.current_stream(self.q.device) if stream is None else stream
+        slot = p % self.W
+        with torch.cuda.stream(cur):
+            self.ring_k[slot].copy_(k.reshape(-1), non_blocking=True)
+            self.ring_v[slot].copy_(v.reshape(-1), non_blocking=True)
+            self.q.copy_(q.reshape(self.q.shape), non_blocking=True)
+            if self.topk:
+                self.q_idx.copy_(q_idx.reshape(-1), non_blocking=True)
+                if self.pooled_keys:
+                    self.ki_tok.copy_(ki_tok.reshape(self.ki_tok.shape), non_blocking=True)
+                elif completes:
+                    self.kidx[n_vis - 1].copy_(kidx_row.reshape(-1), non_blocking=True)
+        self._moved_to(p, n_vis)
+        return self.step(stream=stream)
+
+    def desc(self) -> "ds4a.DecodeLayerDesc":
+        """The layer's ds4a_decode_layer_t (its persistent device arrays)."""
+        return ds4a.decode_layer_desc(self.ring_k, self.ring_v, self.q, self.out, self.scale, self.ratio, self.w,
+                                      self.state, self.comp_k, self.comp_v, self.topk, self.kidx, self.q_idx,
+                                      self.sel, self.sel_n, self.ws, self.ki_tok)
+
+    def _check_next(self, p, q_idx, kidx_row, ki_tok):
         n_vis = (p + 1) // self.ratio if self.ratio else 0
         if self.ratio and n_vis > self.comp_k.shape[0]:
             raise ValueError(f"advance: row {n_vis - 1} is past the compressed-row capacity {self.comp_k.shape[0]}")
@@ -181,21 +204,42 @@ class DecodeLayer:
                 raise ValueError(f"advance: position {p} completes row {n_vis - 1}, whose indexer key is required")
             if n_vis > self.kidx.shape[0]:
                 raise ValueError("advance: past the indexer-key capacity")
-        cur = torch.cuda.current_stream(self.q.device) if stream is None else stream
-        slot = p % self.W
-        with torch.cuda.stream(cur):
-            self.ring_k[slot].copy_(k.reshape(-1), non_blocking=True)
-            self.ring_v[slot].copy_(v.reshape(-1), non_blocking=True)
-            self.q.copy_(q.reshape(self.q.shape), non_blocking=True)
-            if self.topk:
-                self.q_idx.copy_(q_idx.reshape(-1), non_blocking=True)
-                if self.pooled_keys:
-                    self.ki_tok.copy_(ki_tok.reshape(self.ki_tok.shape), non_blocking=True)
-                elif completes:
-                    self.kidx[n_vis - 1].copy_(kidx_row.reshape(-1), non_blocking=True)
-        self.p, self.slot, self.n_vis = p, slot, n_vis
+        return n_vis, completes
+
+    def _moved_to(self, p, n_vis):
+        self.p, self.slot, self.n_vis = p, p % self.W, n_vis
         self.n_win = min(self.W, p + 1)
-        return self.step(stream=stream)
+
+    def advance_host(self, k, v, q, q_idx=None, kidx_row=None, ki_tok=None, out=None, stream=None):
+        """advance() from host memory through one C call (ds4a_decode_layer_step):
+        k, v [D], q [H, D], q_idx, kidx_row and ki_tok [d_idx] are contiguous fp16 CPU
+        tensors (page-locked for asynchronous copies).  The output is copied into `out`
+        (an [H, D] fp16 CPU tensor, allocated when None) and returned once it is there."""
+        p = self.p + 1
+        n_vis, completes = self._check_next(p, q_idx, kidx_row, ki_tok)
+        if out is None:
+            out = torch.empty(self.H, self.D, dtype=torch.float16)
+        ds4a.ds4a_decode_layer_step(self.desc(), p, k.reshape(-1), v.reshape(-1), q.reshape(-1),
+                                    None if q_idx is None else q_idx.reshape(-1),
+                                    kidx_row.reshape(-1) if (completes and self.topk and not self.pooled_keys) else None,
+                                    None if ki_tok is None else ki_tok.reshape(-1), out, stream=stream)
+        self._moved_to(p, n_vis)
+        return out
+
+    def bind_host(self, k, v, q, q_idx=None, out=None, ki_tok=None, stream=None):
+        """The host-memory step at the current position marshalled once: a zero-argument
+        callable that copies the host tensors in, runs the step, copies the output into
+        `out` and waits (one C call).  For repeating one step, as bind()."""
+        desc = self.desc()
+        call = ds4a.bind("ds4a_decode_layer_step", desc, self.p, k.reshape(-1), v.reshape(-1), q.reshape(-1),
+                         None if q_idx is None else q_idx.reshape(-1), None,
+                         None if ki_tok is None else ki_tok.reshape(-1), out, stream=stream)
+
+        def run():
+            call()
+            return out
+        run.desc = desc          # keeps the descriptor alive with the call
+        return run
 
     def bind(self, stream=None):
         """The decode step marshalled once (the layer's tensors are persistent): a

@@ -22,7 +22,8 @@
  *     int32 arrays are 4-byte aligned.
  *   - Every array pointer is a DEVICE pointer owned by the caller.  The
  *     library allocates, frees and synchronises nothing (except
- *     ds4a_last_device_error, which synchronises the given stream).
+ *     ds4a_last_device_error, which synchronises the given stream, and
+ *     ds4a_decode_layer_step, which takes host inputs and waits for its output).
  *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *     stream.  Work is enqueued on it and returns before it runs.
  *   - Positions are absolute token indices, 0-based.  The compressed row j
@@ -367,6 +368,92 @@ int ds4a_compress_attn_decode_batched(int B, const float *score_w, int ratio, fl
                                       uint16_t *comp_v, long long cap, const uint16_t *q, int H, int D,
                                       const uint16_t *ring_k, const uint16_t *ring_v, int W, const long long *pos,
                                       float scale, uint16_t *out, void *stream);
+
+/*
+ * One decode step of one layer from host memory.
+ * ("DS4 (DwarfStar 4)", Key Techniques, "KV attention compression" and "KV cache
+ * with disk as first-class citizen": the raw 128-token window and the compressor
+ * fed one token at a time.)
+ *
+ * ds4a_decode_layer_t names a layer's persistent device arrays once -- the arrays
+ * the single-session calls above take -- and ds4a_decode_layer_step runs the
+ * decode step of the token at position pos from host buffers.  It copies the
+ * token's inputs into the layer's device arrays, enqueues the launches the device
+ * calls make, copies the output to the host and waits for it.  The launches, by
+ * layer kind:
+ *   - indexer layer (topk > 0): ds4a_indexer_topk_compress, then ds4a_attn_decode
+ *     over the kept rows;
+ *   - indexer layer with pooled keys: ds4a_compress_append_keys, ds4a_indexer_topk,
+ *     then ds4a_attn_decode;
+ *   - layer that attends every row (ratio > 0, topk = 0): ds4a_compress_attn_decode;
+ *   - window-only layer (ratio = 0): ds4a_attn_decode over the window.
+ * The window is the ring's min(W, pos+1) rows; the indexer ranks, and the
+ * compressor writes, up to cap rows.  The results are those calls' results, bit
+ * for bit.  The compressor state must hold the open block's tokens before pos
+ * (the layer has decoded pos-1, or was fed up to pos-1).
+ *
+ * This call is the exception to the conventions above: the pointers of
+ * ds4a_decode_host_inputs_t and out_host are HOST pointers, and the call waits for
+ * the stream when out_host is not NULL.  When every given input is page-locked
+ * (or registered) host memory, one kernel reads them over the host link and writes
+ * the device arrays; on an indexer layer the indexer (and compressor) launch reads
+ * its own inputs from the host buffers and runs beside that kernel, on the other
+ * layers the next launch starts when it has finished.  Otherwise each input is one
+ * cudaMemcpyAsync (pageable memory works, staged by the runtime).  A page-locked out_host is written by the attention kernel directly
+ * and the layer's out array is then left as it was; any other out_host receives a
+ * copy of out.  The host buffers must not change until the call has returned
+ * (with out_host = NULL: until the stream has reached the step's end).
+ */
+typedef struct ds4a_decode_layer {
+    int H, D;                    /* heads and head dim, as ds4a_attn_decode */
+    int W;                       /* ring rows, 1 .. 4096: token t in slot t % W */
+    int ratio;                   /* 0: window only; else tokens per compressed row, 1 .. 1024 */
+    int topk;                    /* 0: attend every visible row; else rows the indexer keeps, 1 .. 2048 */
+    int d_idx;                   /* indexer key width (topk > 0), multiple of 8, 8 .. 256 */
+    int pooled_keys;             /* 1: the compressor pools per-token indexer keys (topk > 0) */
+    float scale;                 /* softmax scale */
+    long long cap;               /* rows of comp_k, comp_v and k_idx */
+    uint16_t *ring_k, *ring_v;   /* [W, D] fp16 */
+    const float *score_w;        /* [D] float (ratio > 0) */
+    float *state;                /* [2 + 2D] float, + d_idx with pooled keys (ratio > 0) */
+    uint16_t *comp_k, *comp_v;   /* [cap, D] fp16 (ratio > 0) */
+    uint16_t *k_idx;             /* [cap, d_idx] fp16 (topk > 0) */
+    uint16_t *q;                 /* [H, D] fp16: the step's query */
+    uint16_t *q_idx;             /* [d_idx] fp16: the step's indexer query (topk > 0) */
+    uint16_t *k_idx_tok;         /* [d_idx] fp16: the token's indexer key (pooled keys) */
+    int32_t *out_idx;            /* [topk] int32 kept rows (topk > 0) */
+    int32_t *out_n;              /* [1] int32 kept-row count, or NULL */
+    void *ws;                    /* ds4a_indexer_workspace_bytes(1, cap, topk) bytes (topk > 0) */
+    size_t ws_bytes;
+    uint16_t *out;               /* [H, D] fp16 (not written when out_host is page-locked) */
+} ds4a_decode_layer_t;
+
+/* The step's host inputs.  A NULL pointer leaves that device array as it is (its
+ * input is already there). */
+typedef struct ds4a_decode_host_inputs {
+    const uint16_t *k, *v;       /* [D] fp16: the token's K and V, copied to ring slot pos % W */
+    const uint16_t *q;           /* [H, D] fp16, copied to q */
+    const uint16_t *q_idx;       /* [d_idx] fp16, copied to q_idx (topk > 0) */
+    const uint16_t *k_idx_row;   /* [d_idx] fp16: the indexer key of the row the token completes,
+                                    copied to k_idx row (pos+1)/ratio - 1; used only on an indexer
+                                    layer without pooled keys, when (pos+1) % ratio == 0 */
+    const uint16_t *k_idx_tok;   /* [d_idx] fp16, copied to k_idx_tok (pooled keys) */
+} ds4a_decode_host_inputs_t;
+
+/*
+ * ds4a_decode_layer_step -- the decode step of the token at pos (>= 0) of the
+ * layer `layer`, inputs from `in` (may be NULL: every input already on the
+ * device), output copied to out_host ([H, D] fp16, host) and the stream waited
+ * for; with out_host = NULL the call returns once the work is enqueued.
+ * Errors: every check of the calls it makes, done before anything is enqueued
+ * (DS4A_ERR_ARG for a NULL layer, a NULL or misaligned array its kind needs, or
+ * topk > 0 with ratio = 0 or pooled_keys with topk = 0; DS4A_ERR_CAPACITY when
+ * row (pos+1)/ratio - 1 is >= cap; DS4A_ERR_WORKSPACE for a missing or small
+ * workspace).  A failed copy or launch returns DS4A_ERR_CUDA; the device arrays
+ * may then hold the step's inputs.
+ */
+int ds4a_decode_layer_step(const ds4a_decode_layer_t *layer, long long pos, const ds4a_decode_host_inputs_t *in,
+                           uint16_t *out_host, void *stream);
 
 /*
  * ds4a_probe_gather -- MEASUREMENT CALL, not a step of the attention path; the

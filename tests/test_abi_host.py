@@ -208,3 +208,78 @@ def test_wait_limit_hook_validation(ds4a_lib):
     assert L.ds4a_test_set_wait_limit(-1) == ARG
     assert L.ds4a_test_set_wait_limit(20_000_000_000) == ARG
     assert L.ds4a_test_set_wait_limit(0) == 0
+
+
+def _desc(ds4a_lib, **kw):
+    """A ds4a_decode_layer_t of an indexer layer (H 8, D 64, W 32, ratio 4, top-16,
+    d_idx 32, cap 10) on fake, aligned addresses; kw overrides fields."""
+    d = ds4a_lib.DecodeLayerDesc(H=8, D=64, W=32, ratio=4, topk=16, d_idx=32, pooled_keys=0, scale=0.125, cap=10)
+    for f in ("ring_k", "ring_v", "score_w", "state", "comp_k", "comp_v", "k_idx", "q", "q_idx", "out_idx", "out_n",
+              "ws", "out"):
+        setattr(d, f, FAKE)
+    d.ws_bytes = 1 << 20
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_decode_layer_step_validation(ds4a_lib):
+    """Every check runs before the first copy or launch (these return before any CUDA
+    call): a missing layer, bad shapes, an indexer layer without a ratio, a missing
+    array, capacity and workspace."""
+    import ctypes as C
+    f = ds4a_lib.lib().ds4a_decode_layer_step
+    run = lambda d, pos=38: f(C.byref(d), pos, None, None, None)
+    assert f(None, 0, None, None, None) == ARG
+    assert run(_desc(ds4a_lib), pos=-1) == ARG
+    assert run(_desc(ds4a_lib, W=0)) == ARG
+    assert run(_desc(ds4a_lib, W=5000)) == ARG
+    assert run(_desc(ds4a_lib, H=12)) == UNSUP
+    assert run(_desc(ds4a_lib, D=96)) == UNSUP
+    assert run(_desc(ds4a_lib, ratio=0)) == ARG                  # an indexer layer needs a ratio
+    assert run(_desc(ds4a_lib, topk=0, pooled_keys=1)) == ARG    # pooled keys need the indexer
+    assert run(_desc(ds4a_lib, pooled_keys=1)) == ARG            # ... and the token's key array
+    assert run(_desc(ds4a_lib, topk=4096)) == UNSUP
+    assert run(_desc(ds4a_lib, d_idx=20)) == UNSUP
+    assert run(_desc(ds4a_lib, q_idx=None)) == ARG
+    assert run(_desc(ds4a_lib, ring_k=FAKE + 8)) == ARG           # misaligned
+    assert run(_desc(ds4a_lib, comp_v=None)) == ARG
+    assert run(_desc(ds4a_lib, ws_bytes=16)) == WS
+    assert run(_desc(ds4a_lib), pos=43) == CAP                   # row 10 of a 10-row capacity
+    assert run(_desc(ds4a_lib, topk=0, ratio=128, cap=0), pos=128) == CAP
+
+
+def test_decode_layer_struct_layout_matches_the_header(ds4a_lib, tmp_path):
+    """The binding's ctypes structures have the header's field offsets and sizes
+    (compiled with the host C compiler)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"ds4a_decode_layer_t": ds4a_lib.DecodeLayerDesc, "ds4a_decode_host_inputs_t": ds4a_lib.DecodeHostInputs}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "ds4a.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'printf("{cname}.{fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(line.rsplit(" ", 1) for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                                check=True).stdout.split("\n") if line)
+    for cname, py in structs.items():
+        assert int(got[cname]) == ctypes.sizeof(py), cname
+        for fname, _ in py._fields_:
+            assert int(got[f"{cname}.{fname}"]) == getattr(py, fname).offset, f"{cname}.{fname}"
+
+
+def test_host_step_binding_refuses_device_pointers_for_host_inputs(ds4a_lib):
+    import torch
+    d = _desc(ds4a_lib)
+    with pytest.raises(ValueError, match="elements"):
+        ds4a_lib.bind("ds4a_decode_layer_step", d, 38, torch.zeros(65, dtype=torch.float16))
+    with pytest.raises(TypeError):
+        ds4a_lib.bind("ds4a_decode_layer_step", d, 38, torch.zeros(64, dtype=torch.float32))
