@@ -825,10 +825,10 @@ __global__ void __launch_bounds__(kThreads) attn_prefill_kernel(PrefillArgs a) {
 }
 
 template <int D>
-cudaError_t configure(int &cluster, int *active16 = nullptr, int *active8 = nullptr) {
+cudaError_t configure(int &cluster, int *active16 = nullptr, int *active8 = nullptr, int *active4 = nullptr) {
     static thread_local int configured_device = -1;
     static thread_local int cluster_size = 16;
-    static thread_local int n_active16 = 0, n_active8 = 0;   // clusters of 16 / 8 resident at once
+    static thread_local int n_active16 = 0, n_active8 = 0, n_active4 = 0;   // clusters of 16 / 8 / 4 resident at once
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
@@ -875,12 +875,44 @@ cudaError_t configure(int &cluster, int *active16 = nullptr, int *active8 = null
             n_clusters = 0;
         n_active8 = n_clusters;
         cudaGetLastError();
+        attr.val.clusterDim.x = 4;
+        cfg.gridDim = dim3(4);
+        n_clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&n_clusters, attn_decode_kernel<D, false>, &cfg) != cudaSuccess)
+            n_clusters = 0;
+        n_active4 = n_clusters;
+        cudaGetLastError();
         configured_device = dev;
     }
     cluster = cluster_size;
     if (active16) *active16 = n_active16;
     if (active8) *active8 = n_active8;
+    if (active4) *active4 = n_active4;
     return cudaSuccess;
+}
+
+// Cluster size of a batched launch of B sessions of at most `rows` rows each.  The
+// clusters run in waves of `active` resident clusters, and a CTA's time grows with the
+// kBN-row tiles it attends on top of a fixed part (row table, exchange, merge) worth
+// about five tiles; the size with the smallest waves x (5 + tiles) wins, the larger
+// size on a tie.  Measured on 640-row sessions: 16 sessions run best in clusters of
+// 8 (12.4 us, against 16.0 in 16 and 13.4 in 4), 64 sessions in clusters of 4 (20.7 us,
+// against 27.9 in 8; clusters of 2 gave 22.8).
+int batched_cluster(int B, long long rows, int largest, int active16, int active8, int active4) {
+    int best = largest;
+    long long best_cost = -1;
+    for (int cs : {16, 8, 4}) {
+        const int active = cs == 16 ? active16 : cs == 8 ? active8 : active4;
+        if (cs > largest || active <= 0) continue;
+        const long long waves = (B + active - 1) / active;
+        const long long tiles = (rows + static_cast<long long>(kBN) * cs - 1) / (static_cast<long long>(kBN) * cs);
+        const long long cost = waves * (5 + tiles);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = cs;
+        }
+    }
+    return best;
 }
 
 }  // namespace
@@ -963,12 +995,11 @@ cudaError_t launch_attn_decode_batched(int B, const uint16_t *q, int H, int D, c
     a.W = W;
     a.ratio = ratio;
     a.n_sel_list = sel ? n_sel : 0;
-    int cluster = 16, active16 = 0, active8 = 0;
-    cudaError_t e = D == 128 ? configure<128>(cluster, &active16, &active8) : configure<64>(cluster, &active16, &active8);
+    int cluster = 16, active16 = 0, active8 = 0, active4 = 0;
+    cudaError_t e = D == 128 ? configure<128>(cluster, &active16, &active8, &active4)
+                             : configure<64>(cluster, &active16, &active8, &active4);
     if (e != cudaSuccess) return e;
-    // clusters of 16 while every session's cluster can be resident at once, else of 8
-    // (each CTA then attends twice the rows, but more sessions run side by side)
-    if (cluster == 16 && B > active16 && active8 > active16) cluster = 8;
+    cluster = batched_cluster(B, W + (sel ? static_cast<long long>(n_sel) : cap), cluster, active16, active8, active4);
     const dim3 grid(cluster, B);
     if (state != nullptr) {   // the compressor's update for each session's token, in the same launch
         const cmp::CompressArgs ca{nullptr, nullptr, score_w, state, const_cast<uint16_t *>(comp_k),

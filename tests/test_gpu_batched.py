@@ -65,6 +65,27 @@ def test_batched_sessions_match_single_sessions_and_oracle(layer, positions):
         check_out(h(Bl.out[s]), ref["out"], f"session {s} out")
 
 
+@pytest.mark.parametrize("layer", [2, 3])
+def test_many_sessions_match_the_oracle(layer):
+    """64 model-sized sessions in one call: more sessions than clusters of 16 can be
+    resident at once, so the attention launch splits each session over a smaller
+    cluster (a different split of its rows than the single-session call); every
+    session's kept rows must still be exact and its output within the tolerance."""
+    positions = [32768 + 37 * s for s in range(64)] if layer == 2 else [131071 + 129 * s for s in range(64)]
+    insts = _sessions(layer, positions)
+    Bl = BatchedDecodeLayer(insts)
+    Bl.step()
+    torch.cuda.synchronize()
+    assert ds4a.ds4a_last_device_error() == 0
+    out, sel = h(Bl.out), h(Bl.sel) if Bl.topk else None
+    for s, inst in enumerate(insts):
+        ref = oracle.decode_step(inst)
+        if inst.topk:
+            scores = oracle.index_scores(inst.q_idx, inst.kidx[: ref["n_vis"]])
+            check_sel(sel[s], ref["sel"], scores, inst.topk, f"session {s} sel")
+        check_out(out[s], ref["out"], f"session {s} out")
+
+
 @pytest.mark.parametrize("ratio,topk", [(4, 16), (128, 0)])
 def test_batched_advance_across_ring_wraps(ratio, topk):
     """Three small sessions at different positions, 70 steps each (the ring of 32 wraps
