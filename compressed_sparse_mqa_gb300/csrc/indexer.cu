@@ -390,103 +390,109 @@ DS4A_DEVINL void score_rows(const IndexerArgs &a, const float (&qf)[2][8], long 
 }
 
 // Approximate scores of rows [lo, hi) into keys[j - lo], the key rows staged through
-// shared memory with 16-byte cp.async (kStages chunks of kChunkRows rows in flight: far
-// more bytes than the register rounds of score_rows keep in flight, for CTAs that cover
-// a thousand rows or more) and scored on the tensor cores: mma.sync m16n8k16 with a
-// chunk's 16-row tile as A and the query as column 0 of B, fp32 accumulation over the
-// exact fp16 products.  A second product of the absolute values gives each row's
-// sum_c |q_c k_c|; bmax collects the largest, and 2^-12 bmax bounds the error of every
-// score (far above the accumulation error of d_idx <= 128 products, each rounded once).
-// Needs d_idx a multiple of 32, <= 128.  stage: kStages * kChunkRows * 256 bytes;
-// part: 4 * kChunkRows floats.
-constexpr int kChunkRows = 128;
-constexpr int kStages = 5;
-constexpr size_t kStageBytes = static_cast<size_t>(kStages) * kChunkRows * 256;
+// shared memory with 16-byte cp.async and scored on the tensor cores: mma.sync
+// m16n8k16 with a 16-row group as A and the query as column 0 of B, fp32 accumulation
+// over the exact fp16 products.  A second product of the absolute values gives each
+// row's sum_c |q_c k_c|; bmax collects the largest, and 2^-12 bmax bounds the error of
+// every score (far above the accumulation error of d_idx <= 128 products, each rounded
+// once).  Each of kScoreWarps warps runs its own pipeline over the groups
+// warp, warp + kScoreWarps, ... (kWarpStages groups of 16 rows staged, two in flight
+// while it scores the third) and writes its rows' keys itself: no block-wide barrier
+// until the end.  Needs d_idx a multiple of 16, <= 128.  stage: kStageBytes bytes.
+constexpr int kScoreWarps = 14;
+constexpr int kWarpStages = 3;
+constexpr int kGroupBytes = 16 * 256;   // 16 rows of up to 128 fp16
+constexpr size_t kStageBytes = static_cast<size_t>(kScoreWarps) * kWarpStages * kGroupBytes;
+static_assert(kScoreWarps <= kWarps, "scoring warps");
 // the approximate path keeps the keys of up to this many rows per CTA in dynamic shared
 // memory before the dependency wait (after the stages)
 constexpr int kApproxStagedRows = 8192;
 constexpr size_t kApproxDynBytes = kStageBytes + kApproxStagedRows * sizeof(uint32_t);
 DS4A_DEVINL void score_rows_staged(const IndexerArgs &a, long long lo, long long hi, uint32_t *keys, float &bmax,
-                                   unsigned char *stage, float *part) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n_chunks = a.d_idx / 8;          // 16-byte chunks of a row
-    const int ksteps = a.d_idx / 32;           // 16-wide k-steps per half of d_idx
-    const int tile = warp & 7, khalf = warp >> 3;
-    const long long n = hi - lo;
-    const int n_tiles = static_cast<int>((n + kChunkRows - 1) / kChunkRows);
-    // B fragments: the query in column 0 (lanes 0-3 of each k-step), zeros elsewhere
-    uint32_t bq0[4], bq1[4], ba0[4], ba1[4];   // the query and its absolute values
+                                   unsigned char *stage) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (warp < kScoreWarps) {
+        const int n_chunks = a.d_idx / 8;   // 16-byte chunks of a row
+        const int ksteps = a.d_idx / 16;    // 16-wide k-steps
+        // B fragments: the query in column 0 (lanes 0-3 of each k-step), zeros elsewhere
+        uint32_t bq0[8], bq1[8], ba0[8], ba1[8];   // the query and its absolute values
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        bq0[s] = bq1[s] = ba0[s] = ba1[s] = 0u;
-        if (s < ksteps && (lane >> 2) == 0) {
-            const int k0 = (khalf * ksteps + s) * 16 + 2 * (lane & 3);
-            bq0[s] = *reinterpret_cast<const uint32_t *>(a.q_idx + k0);
-            bq1[s] = *reinterpret_cast<const uint32_t *>(a.q_idx + k0 + 8);
-            const __half2 x0 = __habs2(*reinterpret_cast<const __half2 *>(&bq0[s]));
-            const __half2 x1 = __habs2(*reinterpret_cast<const __half2 *>(&bq1[s]));
-            ba0[s] = *reinterpret_cast<const uint32_t *>(&x0);
-            ba1[s] = *reinterpret_cast<const uint32_t *>(&x1);
-        }
-    }
-    // chunk ch of row r sits at r * 256 + ((ch ^ (r & 7)) << 4): ldmatrix reads of 8 rows
-    // at one chunk column hit 8 different 16-byte bank groups
-    auto issue = [&](int t) {
-        if (t < n_tiles) {
-            unsigned char *dst = stage + (t % kStages) * (kChunkRows * 256);
-            for (int i = tid; i < kChunkRows * n_chunks; i += kThreads) {
-                const int r = i / n_chunks, ch = i % n_chunks;
-                const long long j = lo + static_cast<long long>(t) * kChunkRows + r;
-                const bool valid = j < hi;
-                const uint32_t sdst = static_cast<uint32_t>(__cvta_generic_to_shared(dst + r * 256 + ((ch ^ (r & 7)) << 4)));
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(sdst),
-                             "l"(a.k_idx + (valid ? j : lo) * a.d_idx + ch * 8), "r"(valid ? 16 : 0)
-                             : "memory");
+        for (int s = 0; s < 8; ++s) {
+            bq0[s] = bq1[s] = ba0[s] = ba1[s] = 0u;
+            if (s < ksteps && lane < 4) {
+                const int k0 = s * 16 + 2 * lane;
+                bq0[s] = *reinterpret_cast<const uint32_t *>(a.q_idx + k0);
+                bq1[s] = *reinterpret_cast<const uint32_t *>(a.q_idx + k0 + 8);
+                const __half2 x0 = __habs2(*reinterpret_cast<const __half2 *>(&bq0[s]));
+                const __half2 x1 = __habs2(*reinterpret_cast<const __half2 *>(&bq1[s]));
+                ba0[s] = *reinterpret_cast<const uint32_t *>(&x0);
+                ba1[s] = *reinterpret_cast<const uint32_t *>(&x1);
             }
         }
-        cp_async_commit();   // one group per tile, empty past the last
-    };
+        const long long n = hi - lo;
+        const int n_groups = static_cast<int>((n + 15) / 16);
+        const int my_groups = n_groups > warp ? (n_groups - warp + kScoreWarps - 1) / kScoreWarps : 0;
+        unsigned char *mine = stage + static_cast<size_t>(warp) * kWarpStages * kGroupBytes;
+        // chunk ch of row r sits at r * 256 + ((ch ^ (r & 7)) << 4): ldmatrix reads of 8
+        // rows at one chunk column hit 8 different 16-byte bank groups
+        auto issue = [&](int i) {   // this warp's i-th group
+            if (i < my_groups) {
+                const long long g0 = lo + static_cast<long long>(warp + i * kScoreWarps) * 16;
+                unsigned char *dst = mine + (i % kWarpStages) * kGroupBytes;
 #pragma unroll
-    for (int t = 0; t < kStages - 1; ++t) issue(t);
-    for (int t = 0; t < n_tiles; ++t) {
-        cp_async_wait<kStages - 2>();   // tile t has landed (this thread's copies)
-        __syncthreads();                // ... and every thread's; tile t-1's stage and `part` are free
-        issue(t + kStages - 1);
-        const unsigned char *src = stage + (t % kStages) * (kChunkRows * 256);
-        float d[4] = {0.f, 0.f, 0.f, 0.f}, e4[4] = {0.f, 0.f, 0.f, 0.f};
-        const int r = tile * 16 + (lane & 15);   // this lane's ldmatrix row
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            if (s < ksteps) {
-                const int ch = 2 * (khalf * ksteps + s) + (lane >> 4);
-                uint32_t af[4], aa[4];
-                ldmatrix_x4(af[0], af[1], af[2], af[3], src + r * 256 + ((ch ^ (r & 7)) << 4));
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const __half2 x = __habs2(*reinterpret_cast<const __half2 *>(&af[e]));
-                    aa[e] = *reinterpret_cast<const uint32_t *>(&x);
+                for (int m = 0; m < 8; ++m) {   // 16 rows x 16 chunks over 32 lanes
+                    const int r = (lane >> 4) + 2 * m, ch = lane & 15;
+                    if (ch < n_chunks) {
+                        const long long j = g0 + r;
+                        const bool valid = j < hi;
+                        const uint32_t sdst =
+                            static_cast<uint32_t>(__cvta_generic_to_shared(dst + r * 256 + ((ch ^ (r & 7)) << 4)));
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(sdst),
+                                     "l"(a.k_idx + (valid ? j : lo) * a.d_idx + ch * 8), "r"(valid ? 16 : 0)
+                                     : "memory");
+                    }
                 }
-                mma_16816(d, af, bq0[s], bq1[s]);
-                mma_16816(e4, aa, ba0[s], ba1[s]);
+            }
+            cp_async_commit();   // one group per stage, empty past the last
+        };
+#pragma unroll
+        for (int i = 0; i < kWarpStages - 1; ++i) issue(i);
+        for (int i = 0; i < my_groups; ++i) {
+            cp_async_wait<kWarpStages - 2>();   // group i has landed (this lane's copies)
+            __syncwarp();                       // ... and every lane's; group i-1's stage is free
+            issue(i + kWarpStages - 1);
+            const unsigned char *src = mine + (i % kWarpStages) * kGroupBytes;
+            float d[4] = {0.f, 0.f, 0.f, 0.f}, e4[4] = {0.f, 0.f, 0.f, 0.f};
+            const int r = lane & 15;   // this lane's ldmatrix row
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                if (s < ksteps) {
+                    const int ch = 2 * s + (lane >> 4);
+                    uint32_t af[4], aa[4];
+                    ldmatrix_x4(af[0], af[1], af[2], af[3], src + r * 256 + ((ch ^ (r & 7)) << 4));
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half2 x = __habs2(*reinterpret_cast<const __half2 *>(&af[e]));
+                        aa[e] = *reinterpret_cast<const uint32_t *>(&x);
+                    }
+                    mma_16816(d, af, bq0[s], bq1[s]);
+                    mma_16816(e4, aa, ba0[s], ba1[s]);
+                }
+            }
+            if ((lane & 3) == 0) {   // column 0: rows lane/4 and lane/4 + 8 of the group
+                const long long j = lo + static_cast<long long>(warp + i * kScoreWarps) * 16 + (lane >> 2);
+                if (j < hi) {
+                    keys[j - lo] = float_key(d[0]);
+                    bmax = fmaxf(bmax, e4[0]);
+                }
+                if (j + 8 < hi) {
+                    keys[j + 8 - lo] = float_key(d[2]);
+                    bmax = fmaxf(bmax, e4[2]);
+                }
             }
         }
-        if ((lane & 3) == 0) {   // column 0: rows lane/4 and lane/4 + 8 of the tile, this k-half
-            const int rr = tile * 16 + (lane >> 2);
-            part[khalf * kChunkRows + rr] = d[0];
-            part[khalf * kChunkRows + rr + 8] = d[2];
-            part[(2 + khalf) * kChunkRows + rr] = e4[0];
-            part[(2 + khalf) * kChunkRows + rr + 8] = e4[2];
-        }
-        __syncthreads();
-        if (tid < kChunkRows) {
-            const long long j = lo + static_cast<long long>(t) * kChunkRows + tid;
-            if (j < hi) {
-                keys[j - lo] = float_key(part[tid] + part[kChunkRows + tid]);
-                bmax = fmaxf(bmax, part[2 * kChunkRows + tid] + part[3 * kChunkRows + tid]);
-            }
-        }
+        cp_async_wait<0>();
     }
-    cp_async_wait<0>();
     __syncthreads();
 }
 
@@ -593,8 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     float bmax = 0.f;   // approximate path: largest sum_c |q_c k_c| of this CTA's rows
     load_query(a.q_idx, a.d_idx, qf);
     if constexpr (kApprox) {
-        __shared__ float s_part[4 * kChunkRows];
-        if (a.d_idx % 32 == 0 && a.d_idx <= 128) score_rows_staged(a, j0, js, pre_keys, bmax, dyn_smem, s_part);
+        if (a.d_idx % 16 == 0 && a.d_idx <= 128) score_rows_staged(a, j0, js, pre_keys, bmax, dyn_smem);
         else score_rows<kDeep, true>(a, qf, j0, js, pre_keys, j0, bmax);
     } else {
         score_rows<kDeep, false>(a, qf, j0, js, pre_keys, j0, bmax);
