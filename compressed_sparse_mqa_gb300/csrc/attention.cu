@@ -536,37 +536,45 @@ constexpr int kRecvRows = 80;   // >= cluster size * ceil(H / cluster size) for 
 
 template <int D>
 __host__ __device__ constexpr size_t recv_offset() { return (sizeof(Smem<D>) + 127) / 128 * 128; }
+// One head's split-KV partial as exchanged between the CTAs of a cluster: O as D fp16
+// (its rounding, 2^-11 relative, is far inside the output's fp16), then the running
+// max m and sum l as fp32, padded to a 16-byte multiple for the bulk copies.
 template <int D>
-constexpr size_t decode_smem() { return recv_offset<D>() + kRecvRows * (D + 4) * sizeof(float); }
+__host__ __device__ constexpr int part_bytes() { return 2 * D + 16; }
+template <int D>
+constexpr size_t decode_smem() { return recv_offset<D>() + kRecvRows * part_bytes<D>(); }
 template <int D>
 constexpr size_t prefill_smem() { return sizeof(Smem<D>); }
 static_assert(4 * 32 * (128 / 2 + 4) * sizeof(float) <= sizeof(Smem<128>), "exchange fits in the tiles");
-static_assert(64 * (128 + 4) * sizeof(float) <= sizeof(Smem<128>) && 64 * (64 + 4) * sizeof(float) <= sizeof(Smem<64>),
+static_assert(64 * part_bytes<128>() <= sizeof(Smem<128>) && 64 * part_bytes<64>() <= sizeof(Smem<64>),
               "the send rows of 64 heads fit in the tiles");
+static_assert(part_bytes<128>() % 16 == 0 && part_bytes<64>() % 16 == 0, "bulk copies move 16-byte multiples");
 
 // Log-sum-exp merge of the (O, m, l) rows every rank sent for heads [hb, hb + nh):
-// recv[rank][local head][D + 4]; out[h] = sum_r w_r O_r / sum_r w_r l_r with
+// recv[rank][local head] (part_bytes each); out[h] = sum_r w_r O_r / sum_r w_r l_r with
 // w_r = 2^(m_r - max_r m_r).  CS: the cluster size (0: runtime cs).
 template <int D, int CS>
-DS4A_DEVINL void merge_heads(const float *recv, int hpc, int hb, int nh, uint16_t *out, int cs_rt = CS) {
+DS4A_DEVINL void merge_heads(const unsigned char *recv, int hpc, int hb, int nh, uint16_t *out, int cs_rt = CS) {
     const int cs = CS > 0 ? CS : cs_rt;
+    constexpr int RB = part_bytes<D>();
     for (int idx = threadIdx.x; idx < nh * (D / 2); idx += kThreads) {   // 2 columns per item
         const int hh = idx / (D / 2), d = (idx % (D / 2)) * 2;
+        auto row_of = [&](int r) { return recv + (r * hpc + hh) * RB; };
         float M = -INFINITY;
         if constexpr (CS > 0) {
 #pragma unroll
-            for (int r = 0; r < CS; ++r) M = fmaxf(M, recv[(r * hpc + hh) * (D + 4) + D]);
+            for (int r = 0; r < CS; ++r) M = fmaxf(M, *reinterpret_cast<const float *>(row_of(r) + 2 * D));
         } else {
-            for (int r = 0; r < cs; ++r) M = fmaxf(M, recv[(r * hpc + hh) * (D + 4) + D]);
+            for (int r = 0; r < cs; ++r) M = fmaxf(M, *reinterpret_cast<const float *>(row_of(r) + 2 * D));
         }
         float den = 0.f;
         float2 acc = make_float2(0.f, 0.f);
         auto add_rank = [&](int r) {
-            const float *row = recv + (r * hpc + hh) * (D + 4);
-            const float mr = row[D];
-            const float w = mr == -INFINITY ? 0.f : exp2f(mr - M);
-            den = fmaf(w, row[D + 1], den);
-            const float2 o = *reinterpret_cast<const float2 *>(row + d);
+            const unsigned char *row = row_of(r);
+            const float2 ml = *reinterpret_cast<const float2 *>(row + 2 * D);
+            const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+            den = fmaf(w, ml.y, den);
+            const float2 o = __half22float2(*reinterpret_cast<const __half2 *>(row + 2 * d));
             acc.x = fmaf(w, o.x, acc.x);
             acc.y = fmaf(w, o.y, acc.y);
         };
@@ -589,10 +597,11 @@ DS4A_DEVINL void merge_heads(const float *recv, int hpc, int hb, int nh, uint16_
 // steps update the state after the partials are sent.  No other CTA reads what
 // the compressor writes.
 template <int D, bool kCompress>
-__global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a, cmp::CompressArgs ca) {
+__global__ void __launch_bounds__(kThreads, kCompress ? 1 : 2) attn_decode_kernel(DecodeArgs a, cmp::CompressArgs ca) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
-    float *recv = reinterpret_cast<float *>(smem_raw + recv_offset<D>());
+    unsigned char *recv = smem_raw + recv_offset<D>();
+    constexpr int RB = part_bytes<D>();
     __shared__ __align__(8) uint64_t s_recv_bar;
     cg::cluster_group cluster = cg::this_cluster();
     const int cs = static_cast<int>(cluster.num_blocks());
@@ -634,7 +643,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a, cmp
         }
     }
     // heads [hb, hb + nh) are merged here: every CTA of the cluster sends (O, m, l) of
-    // each of them, a row of D + 4 floats (16-byte multiple), into this CTA's receive buffer
+    // each of them, a row of part_bytes (16-byte multiple), into this CTA's receive buffer
     const int hpc = (a.H + cs - 1) / cs;
     const int hb = rank * hpc;
     const int nh = max(0, min(a.H, hb + hpc) - hb);
@@ -643,7 +652,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a, cmp
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(
                          static_cast<uint32_t>(__cvta_generic_to_shared(&s_recv_bar))),
-                     "r"(static_cast<uint32_t>(cs * nh * (D + 4) * 4))
+                     "r"(static_cast<uint32_t>(cs * nh * RB))
                      : "memory");
     }
     // this CTA is running and its receive barrier is armed; waited on before the first remote store
@@ -691,23 +700,23 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a, cmp
         st.l[r] += __shfl_xor_sync(0xffffffffu, st.l[r], 2);
     }
 
-    // Stage (O, m, l) of each head in this CTA's own shared memory, send[h][D + 4] (the
-    // tiles are free once every warp is past them), then send the rows of each
-    // owner's heads with one bulk copy into recv[this rank] there; the copies
+    // Stage (O, m, l) of each head in this CTA's own shared memory, send[h] (part_bytes
+    // each; the tiles are free once every warp is past them), then send the rows of
+    // each owner's heads with one bulk copy into recv[this rank] there; the copies
     // complete on the owner's receive barrier.
-    float *send = reinterpret_cast<float *>(smem_raw);
+    unsigned char *send = smem_raw;
     __syncthreads();
     if (has_heads) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int h = h0 + g + 8 * r;
             if (h < a.H) {
-                float *row = send + h * (D + 4);
+                unsigned char *row = send + h * RB;
 #pragma unroll
                 for (int dn = 0; dn < D / 16; ++dn)
-                    *reinterpret_cast<float2 *>(row + dh * (D / 2) + dn * 8 + 2 * t) =
-                        make_float2(st.o[dn][2 * r], st.o[dn][2 * r + 1]);
-                if (t == 0 && dh == 0) *reinterpret_cast<float2 *>(row + D) = make_float2(st.m[r], st.l[r]);
+                    *reinterpret_cast<__half2 *>(row + 2 * (dh * (D / 2) + dn * 8 + 2 * t)) =
+                        __floats2half2_rn(st.o[dn][2 * r], st.o[dn][2 * r + 1]);
+                if (t == 0 && dh == 0) *reinterpret_cast<float2 *>(row + 2 * D) = make_float2(st.m[r], st.l[r]);
             }
         }
     }
@@ -720,8 +729,8 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(DecodeArgs a, cmp
         for (int o = warp; o < cs; o += kThreads / 32) {
             const int nho = min(a.H, (o + 1) * hpc) - o * hpc;
             if (nho > 0)
-                bulk_copy_to_cta(cluster_addr(recv + rank * hpc * (D + 4), o), send + o * hpc * (D + 4),
-                                 static_cast<uint32_t>(nho * (D + 4) * 4), cluster_addr(&s_recv_bar, o));
+                bulk_copy_to_cta(cluster_addr(recv + rank * hpc * RB, o), send + o * hpc * RB,
+                                 static_cast<uint32_t>(nho * RB), cluster_addr(&s_recv_bar, o));
         }
         asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
     }
