@@ -552,29 +552,34 @@ static_assert(part_bytes<128>() % 16 == 0 && part_bytes<64>() % 16 == 0, "bulk c
 
 // Log-sum-exp merge of the (O, m, l) rows every rank sent for heads [hb, hb + nh):
 // recv[rank][local head] (part_bytes each); out[h] = sum_r w_r O_r / sum_r w_r l_r with
-// w_r = 2^(m_r - max_r m_r).  CS: the cluster size (0: runtime cs).
+// w_r = 2^(m_r - max_r m_r).  First each (rank, head) weight w_r / sum_r w_r l_r, once
+// (the ranks of a head are consecutive lanes of one warp), then every column's sum.
+// wsh: cs * hpc floats of shared memory.  CS: the cluster size (0: runtime cs).
 template <int D, int CS>
-DS4A_DEVINL void merge_heads(const unsigned char *recv, int hpc, int hb, int nh, uint16_t *out, int cs_rt = CS) {
+DS4A_DEVINL void merge_heads(const unsigned char *recv, int hpc, int hb, int nh, uint16_t *out, float *wsh,
+                             int cs_rt = CS) {
     const int cs = CS > 0 ? CS : cs_rt;
     constexpr int RB = part_bytes<D>();
+    // cs is a power of two <= 16: the ranks of head hh are lanes (hh * cs + r) % 32
+    {
+        const int t = threadIdx.x, r = t % cs, hh = t / cs;
+        const bool valid = hh < nh;
+        float2 ml = make_float2(-INFINITY, 0.f);
+        if (valid) ml = *reinterpret_cast<const float2 *>(recv + (r * hpc + hh) * RB + 2 * D);
+        float M = ml.x;
+        for (int o = 1; o < cs; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+        float den = w * ml.y;
+        for (int o = 1; o < cs; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (valid) wsh[r * hpc + hh] = w / den;
+    }
+    __syncthreads();
     for (int idx = threadIdx.x; idx < nh * (D / 2); idx += kThreads) {   // 2 columns per item
         const int hh = idx / (D / 2), d = (idx % (D / 2)) * 2;
-        auto row_of = [&](int r) { return recv + (r * hpc + hh) * RB; };
-        float M = -INFINITY;
-        if constexpr (CS > 0) {
-#pragma unroll
-            for (int r = 0; r < CS; ++r) M = fmaxf(M, *reinterpret_cast<const float *>(row_of(r) + 2 * D));
-        } else {
-            for (int r = 0; r < cs; ++r) M = fmaxf(M, *reinterpret_cast<const float *>(row_of(r) + 2 * D));
-        }
-        float den = 0.f;
         float2 acc = make_float2(0.f, 0.f);
         auto add_rank = [&](int r) {
-            const unsigned char *row = row_of(r);
-            const float2 ml = *reinterpret_cast<const float2 *>(row + 2 * D);
-            const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-            den = fmaf(w, ml.y, den);
-            const float2 o = __half22float2(*reinterpret_cast<const __half2 *>(row + 2 * d));
+            const float w = wsh[r * hpc + hh];
+            const float2 o = __half22float2(*reinterpret_cast<const __half2 *>(recv + (r * hpc + hh) * RB + 2 * d));
             acc.x = fmaf(w, o.x, acc.x);
             acc.y = fmaf(w, o.y, acc.y);
         };
@@ -584,8 +589,7 @@ DS4A_DEVINL void merge_heads(const unsigned char *recv, int hpc, int hb, int nh,
         } else {
             for (int r = 0; r < cs; ++r) add_rank(r);
         }
-        const float inv = 1.f / den;
-        *reinterpret_cast<uint32_t *>(out + (hb + hh) * D + d) = pack_half2(acc.x * inv, acc.y * inv);
+        *reinterpret_cast<uint32_t *>(out + (hb + hh) * D + d) = pack_half2(acc.x, acc.y);
     }
 }
 
@@ -750,9 +754,10 @@ __global__ void __launch_bounds__(kThreads, kCompress ? 1 : 2) attn_decode_kerne
 
     // merge this CTA's heads from local shared memory (the loop over the cluster's ranks
     // unrolled for the usual cluster sizes)
-    if (cs == 16) merge_heads<D, 16>(recv, hpc, hb, nh, a.out);
-    else if (cs == 8) merge_heads<D, 8>(recv, hpc, hb, nh, a.out);
-    else merge_heads<D, 0>(recv, hpc, hb, nh, a.out, cs);
+    __shared__ float s_w[kRecvRows];   // the merge's (rank, head) weights
+    if (cs == 16) merge_heads<D, 16>(recv, hpc, hb, nh, a.out, s_w);
+    else if (cs == 8) merge_heads<D, 8>(recv, hpc, hb, nh, a.out, s_w);
+    else merge_heads<D, 0>(recv, hpc, hb, nh, a.out, s_w, cs);
     // this CTA's outgoing copies (each issuing lane's) have finished reading its shared memory
     if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
