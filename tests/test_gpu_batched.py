@@ -78,6 +78,18 @@ def test_many_sessions_match_the_oracle(layer):
     torch.cuda.synchronize()
     assert ds4a.ds4a_last_device_error() == 0
     out, sel = h(Bl.out), h(Bl.sel) if Bl.topk else None
+    # the kept rows and the compressor's update are the single-session calls' bits
+    # (the rows of a session are split differently across CTAs, the select is exact)
+    for s in (0, 1, 31, 63):
+        L = DecodeLayer(insts[s])
+        L.step()
+        torch.cuda.synchronize()
+        assert np.array_equal(h(Bl.state[s]), h(L.state)), f"session {s}: compressor state"
+        n = L.n_vis
+        assert np.array_equal(h(Bl.comp_k[s, :n]), h(L.comp_k[:n])), f"session {s}: rows"
+        if Bl.topk:
+            assert np.array_equal(sel[s], h(L.sel)), f"session {s}: kept rows"
+            assert int(Bl.sel_n[s]) == int(L.sel_n)
     for s, inst in enumerate(insts):
         ref = oracle.decode_step(inst)
         if inst.topk:
