@@ -193,6 +193,34 @@ int ds4a_indexer_topk_compress(const uint16_t *q_idx, const uint16_t *k_idx, lon
                                                    k_new, v_new, head_dim, score_w, state, comp_k, comp_v, c));
 }
 
+int ds4a_indexer_topk_compress_keys(const uint16_t *q_idx, uint16_t *k_idx, long long n_rows, int d_idx,
+                                    long long q_pos, int ratio, int k, int32_t *out_idx, int32_t *out_n, void *ws,
+                                    size_t ws_bytes, const uint16_t *k_new, const uint16_t *v_new,
+                                    const uint16_t *k_idx_tok, int head_dim, const float *score_w, float *state,
+                                    uint16_t *comp_k, uint16_t *comp_v, long long cap, void *stream) {
+    // the checks of ds4a_compress_append_keys (n_new = 1, comp_kidx = k_idx) and of ds4a_indexer_topk (n_q = 1)
+    if (n_rows < 0 || q_pos < 0 || ratio < 1 || k < 1 || cap < 0) return DS4A_ERR_ARG;
+    if (d_idx < 8 || d_idx > 256 || d_idx % 8 != 0 || k > 2048 || n_rows > 0x7fffffffLL)
+        return DS4A_ERR_UNSUPPORTED;
+    if (head_dim < 8 || head_dim > 256 || head_dim % 8 != 0 || ratio > 1024) return DS4A_ERR_UNSUPPORTED;
+    if (!q_idx || !out_idx || !k_idx) return DS4A_ERR_ARG;
+    if (!k_new || !v_new || !k_idx_tok || !score_w || !state || !comp_k || !comp_v) return DS4A_ERR_ARG;
+    if (!aligned(q_idx, 16) || !aligned(k_idx, 16) || !aligned(out_idx, 4) || !aligned(out_n, 4))
+        return DS4A_ERR_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_idx_tok, 16) || !aligned(score_w, 4) ||
+        !aligned(state, 4) || !aligned(comp_k, 2) || !aligned(comp_v, 2))
+        return DS4A_ERR_ARG;
+    if (!ws || !aligned(ws, 16) || ws_bytes < ds4a::indexer_ws_bytes(1, n_rows, k)) return DS4A_ERR_WORKSPACE;
+    // the row the token completes is written to comp_k, comp_v and k_idx
+    if ((q_pos + 1) / ratio > (cap < n_rows ? cap : n_rows)) return DS4A_ERR_CAPACITY;
+    ds4a::Ctx c;
+    int rc = make_ctx(stream, c);
+    if (rc != DS4A_OK) return rc;
+    return from_cuda(ds4a::launch_indexer_compress(q_idx, k_idx, n_rows, d_idx, q_pos, ratio, k, out_idx, out_n, ws,
+                                                   k_new, v_new, head_dim, score_w, state, comp_k, comp_v, c,
+                                                   k_idx_tok));
+}
+
 static int check_heads(int H, int D) {
     if (D != 64 && D != 128) return DS4A_ERR_UNSUPPORTED;
     if (H < 8 || H > 64 || H % 8 != 0) return DS4A_ERR_UNSUPPORTED;
@@ -499,11 +527,9 @@ int ds4a_decode_layer_step(const ds4a_decode_layer_t *L, long long pos, const ds
     cudaError_t e = cudaSuccess;
     if (L->topk > 0) {
         if (L->pooled_keys) {
-            e = ds4a::launch_compress(k_r, v_r, 1, D, L->score_w, L->ratio, pos, L->state, L->comp_k, L->comp_v,
-                                      c_first, ki_tok_r, L->k_idx, L->d_idx);
-            if (e == cudaSuccess)
-                e = ds4a::launch_indexer(q_idx_r, 1, L->k_idx, L->cap, L->d_idx, pos, L->ratio, L->topk, L->out_idx,
-                                         L->out_n, L->ws, c);
+            e = ds4a::launch_indexer_compress(q_idx_r, L->k_idx, L->cap, L->d_idx, pos, L->ratio, L->topk, L->out_idx,
+                                              L->out_n, L->ws, k_r, v_r, D, L->score_w, L->state, L->comp_k,
+                                              L->comp_v, c_first, ki_tok_r);
         } else {
             e = ds4a::launch_indexer_compress(q_idx_r, L->k_idx, L->cap, L->d_idx, pos, L->ratio, L->topk, L->out_idx,
                                               L->out_n, L->ws, k_r, v_r, D, L->score_w, L->state, L->comp_k,

@@ -30,10 +30,13 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
 
 // one decode query's indexer and the one-token compressor update of the same step,
 // in one launch (the compressor's arguments as launch_compress with n_new = 1, pos = q_pos)
+// k_idx_tok != nullptr: the compressor also pools the tokens' indexer keys into k_idx
+// (ds4a_compress_append_keys), and a row the token completes is ranked by its pooled key
 cudaError_t launch_indexer_compress(const uint16_t *q_idx, const uint16_t *k_idx, long long n_rows, int d_idx,
                                    long long q_pos, int ratio, int k, int32_t *out_idx, int32_t *out_n, void *ws,
                                    const uint16_t *k_new, const uint16_t *v_new, int D, const float *score_w,
-                                   float *state, uint16_t *comp_k, uint16_t *comp_v, const Ctx &c);
+                                   float *state, uint16_t *comp_k, uint16_t *comp_v, const Ctx &c,
+                                   const uint16_t *k_idx_tok = nullptr);
 
 // batched decode (B sessions, positions pos[B] in device memory): the indexer query
 // and the compressor update of each session's token; workspace bytes per session

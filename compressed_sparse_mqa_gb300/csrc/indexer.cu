@@ -569,10 +569,34 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
             c.comp_v += sid * bt.comp_stride;
         }
     }
+    // Pooled indexer keys (c.ki, one session): the compressor's CTA also pools the token's
+    // indexer key, and when the token completes a row it writes that row's key, scores it
+    // (the exact key, as the scoring CTAs compute it) into the workspace and takes a
+    // ticket like a scoring CTA; the scoring CTAs leave that row to it.
+    long long key_row = -1;
     if constexpr (kCompress && !kFold) {
+        if (c.ki != nullptr && bt.pos == nullptr && (a.q_pos0 + 1) % a.ratio == 0 &&
+            (a.q_pos0 + 1) / a.ratio <= a.n_rows)
+            key_row = (a.q_pos0 + 1) / a.ratio - 1;
         if (blockIdx.x == gridDim.x - 1) {
             static_assert(sizeof(sm.scan) >= kWarps * sizeof(float), "one float per warp");
             compress_one_token(c, reinterpret_cast<float *>(s_keys), reinterpret_cast<float *>(sm.scan));
+            if (key_row < 0) return;
+            __syncthreads();   // the row's key is in memory (this CTA's own writes)
+            const uint32_t kx = sel::exact_key16<true>(a.q_idx, c.comp_ki + key_row * a.d_idx, a.d_idx,
+                                                       threadIdx.x < 16);
+            unsigned int *ticket = reinterpret_cast<unsigned int *>(a.ws);
+            uint32_t *keys = reinterpret_cast<uint32_t *>(a.ws + kWsHeader);
+            if (threadIdx.x == 0) {
+                keys[key_row] = kx;
+                unsigned int old;
+                asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;\n" : "=r"(old) : "l"(ticket) : "memory");
+                s_last = old == gridDim.x - 1;   // every scoring CTA and this one
+            }
+            __syncthreads();
+            if (!s_last) return;
+            select_topk_sized<kSelItems>(keys, static_cast<int>(visible_rows(a, 0)), a.k, a.out_idx, a.out_n, sm);
+            if (threadIdx.x == 0) *ticket = 0u;
             return;
         }
     } else {
@@ -581,11 +605,12 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     // with comp_cta0, scoring CTA 0 also runs the compressor's update: its score before the
     // dependency wait, the running state and a completed row after it
     const bool comp_here = kCompress && kFold && blockIdx.x == 0 && !comp_skip;
-    const unsigned int n_score = (kCompress && !kFold) ? gridDim.x - 1 : gridDim.x;
+    // tickets: the scoring CTAs, and the compressor's CTA when it scores a row
+    const unsigned int n_score = (kCompress && !kFold) ? gridDim.x - (key_row < 0 ? 1u : 0u) : gridDim.x;
     (void)comp_skip;
     const long long n_vis = visible_rows(a, 0);
     const long long j0 = static_cast<long long>(blockIdx.x) * rows_per_cta;
-    const long long j1 = min(n_vis, j0 + rows_per_cta);
+    const long long j1 = min(key_row < 0 ? n_vis : key_row, j0 + rows_per_cta);
     // The query and the key rows complete before the query's token (j < floor(q_pos/ratio))
     // are inputs the kernel just ahead does not write, so up to kStagedRows of those rows
     // of the slice are scored into shared memory before waiting on the previous kernel.
@@ -762,14 +787,18 @@ cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx
 cudaError_t launch_indexer_compress(const uint16_t *q_idx, const uint16_t *k_idx, long long n_rows, int d_idx,
                                    long long q_pos, int ratio, int k, int32_t *out_idx, int32_t *out_n, void *ws,
                                    const uint16_t *k_new, const uint16_t *v_new, int D, const float *score_w,
-                                   float *state, uint16_t *comp_k, uint16_t *comp_v, const Ctx &c) {
+                                   float *state, uint16_t *comp_k, uint16_t *comp_v, const Ctx &c,
+                                   const uint16_t *k_idx_tok) {
     if (d_idx > kMaxDIdx || n_rows > 0x7fffffffLL || ratio > cmp::kMaxRatio || D > cmp::kMaxD)
         return cudaErrorInvalidValue;
     cudaError_t e = configure_indexer(c);
     if (e != cudaSuccess) return e;
     IndexerArgs a{q_idx, k_idx, out_idx, out_n, static_cast<unsigned char *>(ws), n_rows, q_pos,
                   1, d_idx, ratio, k};
-    const cmp::CompressArgs ca{k_new, v_new, score_w, state, comp_k, comp_v, q_pos, 1, D, ratio};
+    // with k_idx_tok the compressor also pools the tokens' indexer keys into k_idx
+    const cmp::CompressArgs ca{k_new, v_new, score_w, state, comp_k, comp_v, q_pos, 1, D, ratio,
+                               k_idx_tok, k_idx_tok ? const_cast<uint16_t *>(k_idx) : nullptr,
+                               k_idx_tok ? d_idx : 0};
     int rows_per_cta = 0;
     // the scoring CTAs leave one SM for the compressor's CTA
     const unsigned grid = decode_grid(q_pos, n_rows, ratio, c.num_sms > 1 ? c.num_sms - 1 : 1, rows_per_cta);

@@ -246,14 +246,17 @@ DS4A_DEVINL float key_to_float(uint32_t key) {
 }
 
 // TwoSum-exact score key of one row, computed by a group of 16 threads (all 32 lanes
-// of every warp call this; `valid` masks the rows).
+// of every warp call this; `valid` masks the rows).  kCoherent: the row is read
+// through L2 (a row this kernel has just written), else through the read-only path.
+template <bool kCoherent = false>
 DS4A_DEVINL uint32_t exact_key16(const uint16_t *q, const uint16_t *krow, int d_idx, bool valid) {
     const int gl = threadIdx.x & 15;
     float s = 0.f, c = 0.f;
     for (int ch = gl; ch < d_idx / 8; ch += 16) {
         if (valid) {
             const uint4 qa = *reinterpret_cast<const uint4 *>(q + ch * 8);
-            const uint4 ka = __ldg(reinterpret_cast<const uint4 *>(krow + ch * 8));
+            const uint4 ka = kCoherent ? __ldcg(reinterpret_cast<const uint4 *>(krow + ch * 8))
+                                       : __ldg(reinterpret_cast<const uint4 *>(krow + ch * 8));
             const uint16_t *hq = reinterpret_cast<const uint16_t *>(&qa);
             const uint16_t *hk = reinterpret_cast<const uint16_t *>(&ka);
 #pragma unroll

@@ -31,7 +31,8 @@ EXPORTED = ["ds4a_status_str", "ds4a_last_device_error", "ds4a_compress_append",
             "ds4a_attn_prefill", "ds4a_indexer_topk_compress", "ds4a_compress_attn_decode",
             "ds4a_indexer_topk_noalloc", "ds4a_test_set_wait_limit", "ds4a_compress_append_keys",
             "ds4a_decode_batched_workspace_bytes", "ds4a_indexer_topk_compress_batched", "ds4a_attn_decode_batched",
-            "ds4a_compress_attn_decode_batched", "ds4a_probe_gather", "ds4a_decode_layer_step"]
+            "ds4a_compress_attn_decode_batched", "ds4a_probe_gather", "ds4a_decode_layer_step",
+            "ds4a_indexer_topk_compress_keys"]
 
 
 class Ds4aError(RuntimeError):
@@ -62,6 +63,7 @@ def lib() -> ctypes.CDLL:
         L.ds4a_attn_decode_batched.argtypes = [I, P, I, I, P, P, I, P, P, P, LL, P, I, I, F, P, P]
         L.ds4a_compress_attn_decode_batched.argtypes = [I, P, I, P, P, P, LL, P, I, I, P, P, I, P, F, P, P]
         L.ds4a_indexer_topk_compress.argtypes = [P, P, LL, I, LL, I, I, P, P, P, SZ, P, P, I, P, P, P, P, LL, P]
+        L.ds4a_indexer_topk_compress_keys.argtypes = [P, P, LL, I, LL, I, I, P, P, P, SZ, P, P, P, I, P, P, P, P, LL, P]
         L.ds4a_compress_attn_decode.argtypes = [P, P, P, I, LL, P, P, P, LL, P, I, I, P, P, I, F, P, P]
         L.ds4a_indexer_workspace_bytes.argtypes = [I, LL, I]
         L.ds4a_indexer_workspace_bytes.restype = SZ
@@ -216,6 +218,28 @@ def ds4a_indexer_topk_compress(q_idx, k_idx, q_pos: int, ratio: int, k: int, out
     args = _marshal_indexer_topk_compress(q_idx, k_idx, q_pos, ratio, k, out_idx, out_n, ws, k_new, v_new, score_w,
                                           state, comp_k, comp_v, n_rows, stream)
     _check(lib().ds4a_indexer_topk_compress(*args), "ds4a_indexer_topk_compress")
+
+
+def _marshal_indexer_topk_compress_keys(q_idx, k_idx, q_pos: int, ratio: int, k: int, out_idx, out_n, ws, k_new,
+                                        v_new, k_idx_tok, score_w, state, comp_k, comp_v, n_rows=None, stream=None):
+    args = list(_marshal_indexer_topk_compress(q_idx, k_idx, q_pos, ratio, k, out_idx, out_n, ws, k_new, v_new,
+                                               score_w, state, comp_k, comp_v, n_rows, stream))
+    d = args[3]
+    if k_idx_tok is None or k_idx_tok.numel() != d or k_idx.numel() == 0:
+        raise ValueError("indexer_topk_compress_keys: k_idx_tok [d_idx] and k_idx rows are required")
+    # (q_idx, k_idx, rows, d, q_pos, ratio, k, out_idx, out_n, ws, ws_bytes, k_new, v_new, | k_idx_tok |, D, ...)
+    args.insert(13, _ptr(k_idx_tok, torch.float16, "k_idx_tok"))
+    return tuple(args)
+
+
+def ds4a_indexer_topk_compress_keys(q_idx, k_idx, q_pos: int, ratio: int, k: int, out_idx, out_n, ws, k_new, v_new,
+                                    k_idx_tok, score_w, state, comp_k, comp_v, n_rows=None, stream=None):
+    """ds4a_compress_append_keys of the token at q_pos (k_new, v_new [1, D], k_idx_tok [d]
+    or [1, d]) into comp rows and the indexer keys k_idx, and ds4a_indexer_topk of the
+    step's query over k_idx, in one launch."""
+    args = _marshal_indexer_topk_compress_keys(q_idx, k_idx, q_pos, ratio, k, out_idx, out_n, ws, k_new, v_new,
+                                               k_idx_tok, score_w, state, comp_k, comp_v, n_rows, stream)
+    _check(lib().ds4a_indexer_topk_compress_keys(*args), "ds4a_indexer_topk_compress_keys")
 
 
 def _marshal_compress_attn_decode(k_new, v_new, score_w, ratio: int, pos: int, state, comp_k, comp_v, q, win_k,
@@ -473,7 +497,8 @@ _MARSHAL = {"ds4a_attn_decode": _marshal_attn_decode,
             "ds4a_compress_append_keys": _marshal_compress_append_keys,
             "ds4a_compress_attn_decode": _marshal_compress_attn_decode,
             "ds4a_indexer_topk_compress": _marshal_indexer_topk_compress,
-            "ds4a_decode_layer_step": _marshal_decode_layer_step}
+            "ds4a_decode_layer_step": _marshal_decode_layer_step,
+            "ds4a_indexer_topk_compress_keys": _marshal_indexer_topk_compress_keys}
 
 
 def bind(name: str, *args, **kwargs):

@@ -259,12 +259,11 @@ class DecodeLayer:
         new_v = self.ring_v[self.slot: self.slot + 1]
         win_k, win_v = self.ring_k[: self.n_win], self.ring_v[: self.n_win]
         if self.pooled_keys:
-            # the compressor writes the key of a row this token completes before the indexer
-            # ranks it: three launches in stream order
-            return [("ds4a_compress_append_keys", (new_k, new_v, self.ki_tok, self.w, self.ratio, self.p, self.state,
-                                                   self.comp_k, self.comp_v, self.kidx)),
-                    ("ds4a_indexer_topk", (self.q_idx, self.kidx, self.p, self.ratio, self.topk, self.sel,
-                                           self.sel_n, self.ws)),
+            # the compressor writes the key of a row this token completes and the indexer
+            # ranks it in the same launch (its compressor CTA scores that row)
+            return [("ds4a_indexer_topk_compress_keys", (self.q_idx, self.kidx, self.p, self.ratio, self.topk,
+                                                         self.sel, self.sel_n, self.ws, new_k, new_v, self.ki_tok,
+                                                         self.w, self.state, self.comp_k, self.comp_v)),
                     ("ds4a_attn_decode", (self.q, win_k, win_v, self.comp_k, self.comp_v, self.sel, self.topk,
                                           self.scale, self.out))]
         if self.topk:

@@ -226,6 +226,30 @@ int ds4a_indexer_topk_noalloc(const uint16_t *q_idx, const uint16_t *k_idx, long
                               int32_t *out_n, void *stream);
 
 /*
+ * ds4a_indexer_topk_compress_keys -- one decode step's indexer query and the
+ * compressor update for its token on a layer whose compressor pools per-token
+ * indexer keys, in one launch.  Same results as ds4a_compress_append_keys(k_new,
+ * v_new, k_idx_tok, 1, head_dim, d_idx, score_w, ratio, q_pos, state, comp_k, comp_v,
+ * k_idx, cap, stream) followed by ds4a_indexer_topk(q_idx, 1, k_idx, n_rows, d_idx,
+ * q_pos, ratio, k, out_idx, out_n, ws, ws_bytes, stream), bit for bit.  When the
+ * token completes a row, the launch's compressor CTA writes the row (K, V and its
+ * pooled indexer key into k_idx), scores that key against q_idx exactly as the
+ * indexer scores a row, and joins the indexer's completion count, so the row is
+ * ranked in the same launch.  ("DS4 (DwarfStar 4)", Key Techniques, "KV attention
+ * compression": the learned indexer ranks the compressed rows.)
+ *   Arguments as the two calls; k_idx is written (the pooled key rows).  Errors: the
+ *   union of the two calls' checks; DS4A_ERR_CAPACITY when the row the token
+ *   completes is >= min(cap, n_rows).  Nothing is enqueued on error.
+ *   Early reads: q_idx, k_new, k_idx_tok, score_w and the rows j < floor(q_pos/ratio)
+ *   of k_idx.
+ */
+int ds4a_indexer_topk_compress_keys(const uint16_t *q_idx, uint16_t *k_idx, long long n_rows, int d_idx,
+                                    long long q_pos, int ratio, int k, int32_t *out_idx, int32_t *out_n, void *ws,
+                                    size_t ws_bytes, const uint16_t *k_new, const uint16_t *v_new,
+                                    const uint16_t *k_idx_tok, int head_dim, const float *score_w, float *state,
+                                    uint16_t *comp_k, uint16_t *comp_v, long long cap, void *stream);
+
+/*
  * ds4a_attn_decode -- one decode query: multi-query attention over the raw
  * window and the selected (or all) compressed rows, as one softmax.
  * ("DS4 (DwarfStar 4)", Architecture: 64 heads, 1 KV head, 128-token window;
@@ -383,8 +407,8 @@ int ds4a_compress_attn_decode_batched(int B, const float *score_w, int ratio, fl
  * layer kind:
  *   - indexer layer (topk > 0): ds4a_indexer_topk_compress, then ds4a_attn_decode
  *     over the kept rows;
- *   - indexer layer with pooled keys: ds4a_compress_append_keys, ds4a_indexer_topk,
- *     then ds4a_attn_decode;
+ *   - indexer layer with pooled keys: ds4a_indexer_topk_compress_keys, then
+ *     ds4a_attn_decode;
  *   - layer that attends every row (ratio > 0, topk = 0): ds4a_compress_attn_decode;
  *   - window-only layer (ratio = 0): ds4a_attn_decode over the window.
  * The window is the ring's min(W, pos+1) rows; the indexer ranks, and the

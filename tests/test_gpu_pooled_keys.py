@@ -163,3 +163,49 @@ def test_pooled_keys_prefill_chunk():
             check_out(out_h[i], ref, f"out[{i}]")
             compared += 1
     assert compared >= T // 2
+
+
+@pytest.mark.parametrize("ratio,p", [(4, 1), (4, 3), (4, 202), (4, 203), (4, 8191), (128, 1023), (128, 1100)])
+def test_fused_pooled_step_matches_the_two_calls(ratio, p):
+    """ds4a_indexer_topk_compress_keys gives the same bits as ds4a_compress_append_keys
+    followed by ds4a_indexer_topk: kept rows, count, running state, pooled K/V rows and
+    pooled indexer keys -- also when the token completes a row, which the launch's
+    compressor CTA writes and scores (p = 3, 203, 8191, 1023) -- and leaves the
+    workspace's completion count at zero."""
+    topk, d_idx, D, seed = 64, 64, 128, 12
+    n_done = p // ratio                 # rows complete before the token
+    n_rows = (p + 1) // ratio + 2       # room for the row the token may complete
+    ki_tok = dev(synth.normal_f16(seed, 5, synth.T_KIDX_TOK, (p + 1, d_idx)))
+    q_idx = dev(synth.normal_f16(seed, 5, synth.T_QIDX, (d_idx,)))
+    tok_k = dev(synth.normal_f16(seed, 5, synth.T_KRAW, (p + 1, D)))
+    tok_v = dev(synth.normal_f16(seed, 5, synth.T_VRAW, (p + 1, D)))
+    w = dev(synth.normal_f32(seed, 5, synth.T_W, (D,), 1.0 / math.sqrt(D)))
+    comp_k = torch.zeros(n_rows, D, dtype=torch.float16, device="cuda")
+    comp_v = torch.zeros_like(comp_k)
+    kidx = torch.zeros(n_rows, d_idx, dtype=torch.float16, device="cuda")
+    state = torch.zeros(2 + 2 * D + d_idx, dtype=torch.float32, device="cuda")
+    if p:
+        ds4a.ds4a_compress_append_keys(tok_k[:p], tok_v[:p], ki_tok[:p], w, ratio, 0, state, comp_k, comp_v, kidx)
+    torch.cuda.synchronize()
+    assert int((kidx[:n_done].abs().sum(dim=1) > 0).sum()) == n_done
+    nb = ds4a.ds4a_indexer_workspace_bytes(1, n_rows, topk)
+    outs = []
+    for fused in (False, True):
+        ck, cv, ki, st = comp_k.clone(), comp_v.clone(), kidx.clone(), state.clone()
+        sel = torch.full((topk,), 7, dtype=torch.int32, device="cuda")
+        sel_n = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+        ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+        if fused:
+            ds4a.ds4a_indexer_topk_compress_keys(q_idx, ki, p, ratio, topk, sel, sel_n, ws, tok_k[p:p + 1],
+                                                 tok_v[p:p + 1], ki_tok[p:p + 1], w, st, ck, cv)
+        else:
+            ds4a.ds4a_compress_append_keys(tok_k[p:p + 1], tok_v[p:p + 1], ki_tok[p:p + 1], w, ratio, p, st, ck, cv,
+                                           ki)
+            ds4a.ds4a_indexer_topk(q_idx, ki, p, ratio, topk, sel, sel_n, ws)
+        torch.cuda.synchronize()
+        outs.append([x.cpu().numpy() for x in (sel, sel_n, st, ck, cv, ki, ws)])
+    for name, a, b in zip(["sel", "sel_n", "state", "comp_k", "comp_v", "kidx", "workspace"], *outs):
+        assert np.array_equal(a, b), name
+    assert int(outs[1][1][0]) == min(topk, (p + 1) // ratio)
+    assert not outs[1][6][:256].any()   # the completion count is back at zero for the next call
+    assert ds4a.ds4a_last_device_error() == 0
