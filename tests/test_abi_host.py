@@ -283,3 +283,27 @@ def test_host_step_binding_refuses_device_pointers_for_host_inputs(ds4a_lib):
         ds4a_lib.bind("ds4a_decode_layer_step", d, 38, torch.zeros(65, dtype=torch.float16))
     with pytest.raises(TypeError):
         ds4a_lib.bind("ds4a_decode_layer_step", d, 38, torch.zeros(64, dtype=torch.float32))
+
+
+def test_indexer_topk_compress_keys_validation(ds4a_lib):
+    f = ds4a_lib.lib().ds4a_indexer_topk_compress_keys
+    # q_idx, k_idx, n_rows, d_idx, q_pos, ratio, k, out_idx, out_n, ws, ws_bytes, k_new, v_new, k_idx_tok,
+    # head_dim, score_w, state, comp_k, comp_v, cap, stream
+    ok = [FAKE, FAKE, 100, 64, 39, 4, 16, FAKE, None, FAKE, 1 << 20, FAKE, FAKE, FAKE, 128, FAKE, FAKE, FAKE, FAKE,
+          100, None]
+
+    def call(**kw):
+        args = list(ok)
+        names = ["q_idx", "k_idx", "n_rows", "d_idx", "q_pos", "ratio", "k", "out_idx", "out_n", "ws", "ws_bytes",
+                 "k_new", "v_new", "k_idx_tok", "head_dim", "score_w", "state", "comp_k", "comp_v", "cap", "stream"]
+        for name, v in kw.items():
+            args[names.index(name)] = v
+        return f(*args)
+    assert call(k_idx_tok=None) == ARG          # the token's indexer key is required
+    assert call(k_idx=None) == ARG              # the pooled keys are written into k_idx
+    assert call(d_idx=20) == UNSUP
+    assert call(k=4096) == UNSUP
+    assert call(ws_bytes=8) == WS
+    assert call(q_pos=403) == CAP               # completes row 100 of a 100-row capacity
+    assert call(n_rows=9, q_pos=39) == CAP      # row 9 is past the 9 key rows
+    assert call(k_idx_tok=FAKE + 8) == ARG      # misaligned
