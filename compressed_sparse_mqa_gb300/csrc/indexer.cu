@@ -534,7 +534,10 @@ union ApproxSmem {
 // kFold: the compressor's update runs in scoring CTA 0 (DecodeBatch::comp_cta0).  The
 // single-session launches are instantiated without the batched-only paths: code and
 // shared memory they never use measured 0.4 us slower on a decode step.
-template <bool kCompress, int kDeep, bool kApprox, bool kFold, int kSelItems = 0>
+// kKeyRow: one session whose compressor pools the tokens' indexer keys (c.ki): the
+// compressor's CTA also scores a row its token completes (a separate instantiation, so
+// that the other launches carry none of its code).
+template <bool kCompress, int kDeep, bool kApprox, bool kFold, int kSelItems = 0, bool kKeyRow = false>
 __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs a, int rows_per_cta,
                                                                      cmp::CompressArgs c, DecodeBatch bt) {
     __shared__ typename std::conditional<kApprox, ApproxSmem, ExactSmem>::type u;
@@ -575,13 +578,14 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
     // ticket like a scoring CTA; the scoring CTAs leave that row to it.
     long long key_row = -1;
     if constexpr (kCompress && !kFold) {
-        if (c.ki != nullptr && bt.pos == nullptr && (a.q_pos0 + 1) % a.ratio == 0 &&
-            (a.q_pos0 + 1) / a.ratio <= a.n_rows)
-            key_row = (a.q_pos0 + 1) / a.ratio - 1;
+        if constexpr (kKeyRow) {
+            if ((a.q_pos0 + 1) % a.ratio == 0 && (a.q_pos0 + 1) / a.ratio <= a.n_rows)
+                key_row = (a.q_pos0 + 1) / a.ratio - 1;
+        }
         if (blockIdx.x == gridDim.x - 1) {
             static_assert(sizeof(sm.scan) >= kWarps * sizeof(float), "one float per warp");
             compress_one_token(c, reinterpret_cast<float *>(s_keys), reinterpret_cast<float *>(sm.scan));
-            if (key_row < 0) return;
+            if (!kKeyRow || key_row < 0) return;
             __syncthreads();   // the row's key is in memory (this CTA's own writes)
             const uint32_t kx = sel::exact_key16<true>(a.q_idx, c.comp_ki + key_row * a.d_idx, a.d_idx,
                                                        threadIdx.x < 16);
@@ -753,14 +757,15 @@ static int sel_items_for(long long n_vis) {
     return 0;
 }
 
-// a one-query decode kernel (kCompress: with the compressor's CTA) with the select its rows need
-template <bool kCompress>
+// a one-query decode kernel (kCompress: with the compressor's CTA; kKeyRow: that CTA pools
+// indexer keys and scores the row its token completes) with the select its rows need
+template <bool kCompress, bool kKeyRow = false>
 static auto decode_kernel_for(long long n_vis) {
     switch (sel_items_for(n_vis)) {
-        case 8: return indexer_decode_kernel<kCompress, 1, false, false, 8>;
-        case 16: return indexer_decode_kernel<kCompress, 1, false, false, 16>;
-        case kMaxItems: return indexer_decode_kernel<kCompress, 1, false, false, kMaxItems>;
-        default: return indexer_decode_kernel<kCompress, 1, false, false, 0>;
+        case 8: return indexer_decode_kernel<kCompress, 1, false, false, 8, kKeyRow>;
+        case 16: return indexer_decode_kernel<kCompress, 1, false, false, 16, kKeyRow>;
+        case kMaxItems: return indexer_decode_kernel<kCompress, 1, false, false, kMaxItems, kKeyRow>;
+        default: return indexer_decode_kernel<kCompress, 1, false, false, 0, kKeyRow>;
     }
 }
 
@@ -803,8 +808,8 @@ cudaError_t launch_indexer_compress(const uint16_t *q_idx, const uint16_t *k_idx
     // the scoring CTAs leave one SM for the compressor's CTA
     const unsigned grid = decode_grid(q_pos, n_rows, ratio, c.num_sms > 1 ? c.num_sms - 1 : 1, rows_per_cta);
     const long long n_vis = (q_pos + 1) / ratio < n_rows ? (q_pos + 1) / ratio : n_rows;
-    return launch(decode_kernel_for<true>(n_vis), dim3(grid + 1), dim3(kThreads), 0, c, 1, a, rows_per_cta, ca,
-                  DecodeBatch{});
+    return launch(k_idx_tok ? decode_kernel_for<true, true>(n_vis) : decode_kernel_for<true>(n_vis), dim3(grid + 1),
+                  dim3(kThreads), 0, c, 1, a, rows_per_cta, ca, DecodeBatch{});
 }
 
 size_t indexer_batched_ws_stride(long long cap) {
@@ -863,7 +868,8 @@ static cudaError_t configure_indexer(const Ctx &c) {
         cudaError_t e = cudaFuncSetAttribute(indexer_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kQuerySmem));
         for (long long n_vis : {1LL * kThreads * 8, 1LL * kThreads * 16, 1LL * kThreads * kMaxItems, 1LL << 40}) {
-            for (auto kern : {decode_kernel_for<false>(n_vis), decode_kernel_for<true>(n_vis)})
+            for (auto kern : {decode_kernel_for<false>(n_vis), decode_kernel_for<true>(n_vis),
+                              decode_kernel_for<true, true>(n_vis)})
                 if (e == cudaSuccess)
                     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                              cudaSharedmemCarveoutMaxShared);
