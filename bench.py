@@ -301,24 +301,30 @@ def run_e2e(layers, stream, n_steps):
     from compressed_sparse_mqa_gb300 import ds4a
     R = len(layers)
     L0 = layers[0]
-    q_h = L0.q.cpu().pin_memory()
-    k_h = L0.ring_k[L0.slot].cpu().pin_memory()
-    v_h = L0.ring_v[L0.slot].cpu().pin_memory()
-    qi_h = L0.q_idx.cpu().pin_memory() if L0.topk else None
-    kt_h = L0.ki_tok.cpu().pin_memory() if L0.pooled_keys else None
+    # the step's inputs live in one page-locked block (q, k, v, the indexer query and,
+    # with pooled keys, the token's indexer key), each a view at a 16-byte offset
+    parts = [L0.q, L0.ring_k[L0.slot], L0.ring_v[L0.slot]] + ([L0.q_idx] if L0.topk else []) + \
+        ([L0.ki_tok] if L0.pooled_keys else [])
+    sizes = [t.numel() for t in parts]
+    offs = [sum((n + 7) // 8 * 8 for n in sizes[:i]) for i in range(len(sizes))]
+    block = torch.empty(offs[-1] + (sizes[-1] + 7) // 8 * 8, dtype=torch.float16).pin_memory()
+    views = [block[o:o + n] for o, n in zip(offs, sizes)]
+    for v, t in zip(views, parts):
+        v.copy_(t.reshape(-1).cpu())
+    q_h, k_h, v_h = views[0], views[1], views[2]
+    qi_h = views[3] if L0.topk else None
+    kt_h = views[-1] if L0.pooled_keys else None
     out_h = torch.empty_like(L0.out, device="cpu").pin_memory()
-    ins = [h for h in (q_h, k_h, v_h, qi_h, kt_h) if h is not None]
-    h2d = sum(h.numel() * h.element_size() for h in ins)
+    h2d = sum(n * 2 for n in sizes)
     d2h = out_h.numel() * out_h.element_size()
     bound = [L.bind_host(k_h, v_h, q_h, qi_h, out_h, ki_tok=kt_h, stream=stream) for L in layers]
-    # each step's inputs are written into the pinned buffers by the host first, as a
+    # each step's inputs are written into the pinned block by the host first, as a
     # caller producing them would (so no step reads inputs the GPU has seen before)
-    keep = [h.clone() for h in ins]
-    srcs = [(h.data_ptr(), s.data_ptr(), h.numel() * h.element_size()) for h, s in zip(ins, keep)]
+    src = block.clone()
+    dst_p, src_p, nbytes = block.data_ptr(), src.data_ptr(), block.numel() * 2
 
     def one(t):
-        for dst, src, n in srcs:
-            ctypes.memmove(dst, src, n)
+        ctypes.memmove(dst_p, src_p, nbytes)
         bound[t % R]()
 
     with torch.cuda.stream(stream):
@@ -330,7 +336,7 @@ def run_e2e(layers, stream, n_steps):
             one(t)
         dt = time.perf_counter() - t0
     assert ds4a.ds4a_last_device_error() == 0
-    how = ("per step: the host writes the token's K and V, q and the indexer query into pinned buffers, then one "
+    how = ("per step: the host writes the token's K and V, q and the indexer query into one pinned block, then one "
            "ds4a_decode_layer_step call (marshalled once per layer copy): a kernel reads the pinned inputs over "
            "the host link into the layer's arrays, the step's launches, the attention kernel writes out into a "
            "pinned buffer, stream sync; host clock")
