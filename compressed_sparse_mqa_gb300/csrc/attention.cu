@@ -122,6 +122,16 @@ DS4A_DEVINL void issue_loads(const RowSrc &s, const long long *off, uint16_t *kt
     }
 }
 
+// Bring rows [r0, r1) of a [*, D] fp16 array into L2: one bulk prefetch, which
+// returns no data (a row another kernel writes afterwards is still read correctly).
+template <int D>
+DS4A_DEVINL void prefetch_rows_l2(const uint16_t *base, long long r0, long long r1) {
+    if (r1 <= r0) return;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(base + r0 * D),
+                 "r"(static_cast<uint32_t>((r1 - r0) * D * 2))
+                 : "memory");
+}
+
 // Per-warp running state: rows g and g+8 of the warp's 16 heads.
 template <int D>
 struct WarpState {
@@ -679,6 +689,19 @@ __global__ void __launch_bounds__(kThreads, kCompress ? 1 : 2) attn_decode_kerne
         __syncthreads();
         issue_loads<D>(a.src, sm.off[0], sm.k[0], sm.v[0]);
         cp_async_commit();
+    }
+    if (a.pos == nullptr && threadIdx.x < 4) {
+        // one session: warm L2 with the rows this CTA gathers after the dependency wait
+        // (window rows past the first tile; compressed rows when every row is attended,
+        // since a kept-row list is known only after the wait)
+        const int pv0 = pre ? min(v1, v0 + kBN) : v0;
+        const int nw = a.src.n_w;
+        if (threadIdx.x < 2) {
+            prefetch_rows_l2<D>(threadIdx.x ? a.src.wv : a.src.wk, pv0, min(v1, nw));
+        } else if (!a.src.sel) {
+            const long long c0 = max(pv0, nw) - nw, c1 = min(static_cast<long long>(v1 - nw), a.src.n_comp);
+            prefetch_rows_l2<D>(threadIdx.x == 3 ? a.src.cv : a.src.ck, c0, c1);
+        }
     }
     // the query is an input no kernel of this library writes: loaded before the wait too
     uint32_t qa[D / 16][4];
