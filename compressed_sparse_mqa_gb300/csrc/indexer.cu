@@ -364,6 +364,11 @@ DS4A_DEVINL void compress_one_token(const cmp::CompressArgs &c, float *s_w, floa
     cmp::pool_segment<kThreads>(c, b, c.pos, c.pos + 1, resume, s_w, s_red);
 }
 
+// one cache line of global memory into L2 (no data returned, no alignment needed)
+DS4A_DEVINL void prefetch_l2_line(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+
 // Rows [lo, hi) of a slice scored into keys[j - kbase], kDeep 64-row batches per
 // round: the loads of a round are all issued before any of them is scored, so a
 // CTA that covers many rows (a batched step) keeps kDeep x 16 KB of key rows in
@@ -632,6 +637,44 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
         else score_rows<kDeep, true>(a, qf, j0, js, pre_keys, j0, bmax);
     } else {
         score_rows<kDeep, false>(a, qf, j0, js, pre_keys, j0, bmax);
+    }
+    if constexpr (kCompress && !kFold && !kApprox && (kSelItems == 8 || kSelItems == 16)) {
+        // Warm L2 with the compressed K and V rows the query most likely keeps: the
+        // best `want` of this CTA's pre-scored rows, want = its even share of the k
+        // kept rows plus 4.  A prefetch returns no data; attention gathers the kept
+        // rows once the selection is done.
+        const int nloc = static_cast<int>(js - j0);
+        if (nloc > 0 && nloc <= 64) {   // the ranking costs nloc^2 / 512 compares a thread
+            __syncthreads();   // pre_keys complete
+            const long long share = (static_cast<long long>(nloc) * a.k + n_vis - 1) / n_vis;
+            const int want = static_cast<int>(min(static_cast<long long>(nloc), share + 4));
+            const int row_bytes = c.D * 2;
+            // tpr threads (a power of two) rank each row, each against every tpr-th key
+            int tpr = 1;
+            while (tpr < 32 && tpr * 2 * nloc <= kThreads) tpr *= 2;
+            for (int rb = 0; rb < nloc; rb += kThreads / tpr) {   // block-uniform trip count
+                const int r = rb + static_cast<int>(threadIdx.x) / tpr, sub = threadIdx.x % tpr;
+                int above = 0;
+                if (r < nloc) {
+                    const uint32_t kr = pre_keys[r];
+                    for (int o = sub; o < nloc; o += tpr) {
+                        const uint32_t ko = pre_keys[o];
+                        above += (ko > kr) || (ko == kr && o < r);
+                    }
+                }
+                for (int m = 1; m < tpr; m <<= 1) above += __shfl_xor_sync(0xffffffffu, above, m);
+                if (r < nloc && sub == 0 && above < want) {
+                    const char *pk = reinterpret_cast<const char *>(c.comp_k + (j0 + r) * c.D);
+                    const char *pv = reinterpret_cast<const char *>(c.comp_v + (j0 + r) * c.D);
+                    for (int off = 0; off < row_bytes; off += 128) {
+                        prefetch_l2_line(pk + off);
+                        prefetch_l2_line(pv + off);
+                    }
+                    prefetch_l2_line(pk + row_bytes - 1);
+                    prefetch_l2_line(pv + row_bytes - 1);
+                }
+            }
+        }
     }
     __shared__ float s_cw[1];   // kFold: the compressor's score of the step's token
     if constexpr (kFold) {
