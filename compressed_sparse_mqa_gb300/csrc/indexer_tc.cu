@@ -31,7 +31,7 @@ namespace {
 
 constexpr int kTM = 128;                 // queries per tile (MMA M)
 constexpr int kTN = 256;                 // rows per tile (MMA N)
-constexpr int kGemmThreads = 128;
+constexpr int kGemmThreads = 256;   // two warps per TMEM lane quadrant
 
 struct TcScoreArgs {
     const uint16_t *q_idx;
@@ -110,9 +110,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
     }
 
     bool ok = true;
-    // Epilogue: lane l of warp w holds query row 32w + l.  Each 32 x 32 block goes
+    // Epilogue: lane l of warp w holds query row 32 (w % 4) + l, columns of part w / 4.  Each 32 x 32 block goes
     // through a padded shared tile so that a store instruction writes 128-byte runs
     // of four rows instead of 16 bytes of 32 rows.
+    constexpr int kColParts = kGemmThreads / 128;   // warps sharing a TMEM lane quadrant
+    constexpr int kPartCols = kTN / kColParts;
+    const int quad = warp & 3, cpart = warp >> 2;
     auto epilogue = [&](int it) {
         const int buf = it & 1;
         if (!tc::mbar_wait(&s_bar[buf], (it >> 1) & 1)) ok = false;
@@ -120,11 +123,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
         const long long col0 = static_cast<long long>(ns + it * a.n_split) * kTN;
         float *stg = s_stage[warp];
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTN; c0 += 32) {
+        for (int c0 = cpart * kPartCols; c0 < (cpart + 1) * kPartCols; c0 += 32) {
             uint32_t r[16];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                tc::ld_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + buf * kTN + c0 + 16 * h, r);
+                tc::ld_x16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * kTN + c0 + 16 * h, r);
                 tc::wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) stg[lane * 33 + 16 * h + j] = __uint_as_float(r[j]);
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) indexer_scores_tc_kernel(TcSc
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int row = 4 * k + (lane >> 3), cg = 4 * (lane & 7);
-                const int q = m0 + warp * 32 + row;
+                const int q = m0 + quad * 32 + row;
                 const float *src = stg + row * 33 + cg;
                 if (ok && q < a.n_q)
                     *reinterpret_cast<float4 *>(a.scores + static_cast<long long>(q) * a.ld + col0 + c0 + cg) =
