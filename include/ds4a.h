@@ -191,6 +191,11 @@ size_t ds4a_indexer_workspace_bytes(int n_q, long long n_rows, int k);
  *   (k_new, v_new: [1, head_dim] fp16, the token at position q_pos).
  *   Errors: the union of the two calls' checks; nothing is enqueued on error.
  *   Early reads: the union of the two calls' early reads.
+ *   L2 prefetch: with at most 8192 visible rows, the launch also asks L2 for the
+ *   comp_k / comp_v rows (below the visible count, hence inside the cap rows
+ *   passed) that its query most likely keeps, before its dependency wait, so
+ *   that the attention call which gathers them next finds them there.  A
+ *   prefetch returns no data: it reads nothing the results depend on.
  */
 int ds4a_indexer_topk_compress(const uint16_t *q_idx, const uint16_t *k_idx, long long n_rows, int d_idx,
                                long long q_pos, int ratio, int k, int32_t *out_idx, int32_t *out_n, void *ws,
@@ -269,7 +274,9 @@ int ds4a_indexer_topk_compress_keys(const uint16_t *q_idx, uint16_t *k_idx, long
  *   scale      softmax scale, 1/sqrt(D) in the model.
  *   out        [H, D] fp16.
  *   ws, ws_bytes  unused by this kernel design (pass NULL, 0); reserved.
- * Early reads: q and up to 64 window rows.
+ * Early reads: q and up to 64 window rows.  Each CTA also asks L2, before the
+ * dependency wait, for the window rows it gathers after it and, with sel NULL,
+ * for its compressed rows (a prefetch returns no data).
  */
 int ds4a_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
                      const uint16_t *win_v, int n_win, const uint16_t *comp_k,
@@ -293,7 +300,8 @@ int ds4a_attn_decode(const uint16_t *q, int H, int D, const uint16_t *win_k,
  *   (k_new, v_new: [1, D] fp16, the token at position pos).
  *   Attention arguments as ds4a_attn_decode; the window must hold the token at pos.
  *   Errors: the union of the two calls' checks; nothing is enqueued on error.
- *   Early reads: k_new, score_w, q and up to 64 window rows.
+ *   Early reads: k_new, score_w, q and up to 64 window rows; L2 prefetches as
+ *   ds4a_attn_decode with sel NULL.
  */
 int ds4a_compress_attn_decode(const uint16_t *k_new, const uint16_t *v_new, const float *score_w, int ratio,
                               long long pos, float *state, uint16_t *comp_k, uint16_t *comp_v, long long cap,
