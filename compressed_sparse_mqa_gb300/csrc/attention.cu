@@ -20,14 +20,18 @@
 // Decode: one query, rows split across one thread-block cluster of 16 CTAs (8
 // if 16 cannot be scheduled).  Inside a CTA the 8 warps split by head group x
 // half of d instead (compute_tile_dsplit): both halves compute the same scores,
-// and no partial state has to be combined across warps.  Each CTA sends its (m, l, O) of head h straight
-// into the shared memory of the CTA that owns h with asynchronous remote stores
-// (st.async) that count their bytes on the owner's receive mbarrier; each CTA
-// waits only for the bytes destined to it, then merges its own heads by
-// log-sum-exp from local shared memory.  A cluster arrive at kernel start (after
-// the receive barrier is armed), waited on just before the first remote store,
-// guarantees every peer is running and ready.  Window rows are cache state and, with the query, are gathered
-// before waiting on the previous kernel.  No workspace, no second launch, no spin.
+// and no partial state has to be combined across warps.  Each CTA stages its
+// (O as fp16, m, l) of every head in its own shared memory and sends the rows of
+// each owner's heads with one bulk copy into the owner's shared memory, counted in
+// bytes on the owner's receive mbarrier; each CTA waits only for the bytes destined
+// to it, then merges its own heads by log-sum-exp from local shared memory.  A
+// cluster arrive at kernel start (after the receive barrier is armed), waited on
+// just before the first copy, guarantees every peer is running and ready.  Window
+// rows are cache state and, with the query, are gathered before waiting on the
+// previous kernel.  No workspace, no second launch, no spin.  A tile costs a fixed
+// part (row table, loads, softmax) well above its per-row work, so a one-session
+// launch (and a batched compressor + attention launch) whose CTAs attend 65 .. 80
+// rows takes them as one 80-row tile instead of 64 + a remainder.
 // Prefill: one CTA per query walks the query's whole row list (the shapes the
 // tensor-core kernel in attention_tc.cu does not take).
 #include <cooperative_groups.h>
@@ -60,12 +64,12 @@ struct RowSrc {
     int n_w;
 };
 
-template <int D>
+template <int D, int BN = kBN>
 struct Smem {
-    uint16_t k[2][kBN * D];
-    uint16_t v[2][kBN * D];
-    long long off[2][kBN];   // element offset of the row in the window (>=0, tagged) / comp arrays; -1 = padding
-    int nvalid[2];           // rows of the tile inside the list (the rest is padding)
+    uint16_t k[2][BN * D];
+    uint16_t v[2][BN * D];
+    long long off[2][BN];   // element offset of the row in the window (>=0, tagged) / comp arrays; -1 = padding
+    int nvalid[2];          // rows of the tile inside the list (the rest is padding)
 };
 
 // Row offset encoding: bit 62 set -> window row.
@@ -77,11 +81,11 @@ DS4A_DEVINL uint32_t swz(int r, int ch) {
     return static_cast<uint32_t>(r * (D * 2) + ((ch ^ (r & 7)) << 4));
 }
 
-template <int D>
+template <int D, int BN = kBN>
 DS4A_DEVINL void build_table(const RowSrc &s, int v0, int v_end, long long *off, int *nvalid) {
     const int t = threadIdx.x;
-    if (t == 0) *nvalid = min(kBN, v_end - v0);
-    if (t < kBN) {
+    if (t == 0) *nvalid = min(BN, v_end - v0);
+    if (t < BN) {
         const int v = v0 + t;
         long long o = -1;
         if (v < v_end) {
@@ -98,12 +102,12 @@ DS4A_DEVINL void build_table(const RowSrc &s, int v0, int v_end, long long *off,
     }
 }
 
-template <int D>
+template <int D, int BN = kBN>
 DS4A_DEVINL void issue_loads(const RowSrc &s, const long long *off, uint16_t *kt, uint16_t *vt) {
     constexpr int kChunks = D / 8;
     unsigned char *kb = reinterpret_cast<unsigned char *>(kt);
     unsigned char *vb = reinterpret_cast<unsigned char *>(vt);
-    for (int i = threadIdx.x; i < kBN * kChunks; i += kThreads) {
+    for (int i = threadIdx.x; i < BN * kChunks; i += kThreads) {
         const int r = i / kChunks, ch = i % kChunks;
         const long long o = off[r];
         const uint32_t so = swz<D>(r, ch);
@@ -344,25 +348,25 @@ struct WarpStateH {
     float l[2];
 };
 
-template <int D>
+template <int D, int BN = kBN>
 DS4A_DEVINL void compute_tile_dsplit(const uint32_t (&qa)[D / 16][4], const uint16_t *kt, const uint16_t *vt,
                                      const long long *off, int nvalid, int dh, float scale_log2,
                                      WarpStateH<D> &st) {
     const int lane = threadIdx.x & 31, t = lane & 3;
     if (nvalid <= 0) return;
-    const int groups = min(kBN / 16, (nvalid + 15) / 16);   // 16-key groups holding list rows
+    const int groups = min(BN / 16, (nvalid + 15) / 16);   // 16-key groups holding list rows
     const unsigned char *kb = reinterpret_cast<const unsigned char *>(kt);
     const unsigned char *vb = reinterpret_cast<const unsigned char *>(vt);
-    float s[kBN / 8][4];
+    float s[BN / 8][4];
 #pragma unroll
-    for (int nt = 0; nt < kBN / 8; ++nt)
+    for (int nt = 0; nt < BN / 8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
     // S = Q K^T over the tile: ldmatrix x4 gives b0/b1 for two key tiles (one 16-key group)
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
-        for (int gq = 0; gq < kBN / 16; ++gq) {
+        for (int gq = 0; gq < BN / 16; ++gq) {
             if (gq < groups) {
                 const int key = gq * 16 + (lane & 7) + ((lane >> 4) << 3);
                 const int ch = 2 * ks + ((lane >> 3) & 1);
@@ -376,7 +380,7 @@ DS4A_DEVINL void compute_tile_dsplit(const uint32_t (&qa)[D / 16][4], const uint
     // scale into the log2 domain, mask padding rows, running max
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < kBN / 8; ++nt) {
+    for (int nt = 0; nt < BN / 8; ++nt) {
         const int kr = nt * 8 + 2 * t;
         const bool v0 = off[kr] >= 0, v1 = off[kr + 1] >= 0;
         s[nt][0] = v0 ? s[nt][0] * scale_log2 : -INFINITY;
@@ -407,9 +411,9 @@ DS4A_DEVINL void compute_tile_dsplit(const uint32_t (&qa)[D / 16][4], const uint
         st.o[dn][2] *= alpha[1];
         st.o[dn][3] *= alpha[1];
     }
-    uint32_t pa[kBN / 16][4];
+    uint32_t pa[BN / 16][4];
 #pragma unroll
-    for (int nt = 0; nt < kBN / 8; ++nt) {
+    for (int nt = 0; nt < BN / 8; ++nt) {
         const float p0 = exp2f(s[nt][0] - ref[0]), p1 = exp2f(s[nt][1] - ref[0]);
         const float p2 = exp2f(s[nt][2] - ref[1]), p3 = exp2f(s[nt][3] - ref[1]);
         st.l[0] += p0 + p1;
@@ -420,7 +424,7 @@ DS4A_DEVINL void compute_tile_dsplit(const uint32_t (&qa)[D / 16][4], const uint
     }
     // O += P V over this warp's half of d: ldmatrix.trans x4 gives b0/b1 for two d tiles
 #pragma unroll
-    for (int kk = 0; kk < kBN / 16; ++kk) {
+    for (int kk = 0; kk < BN / 16; ++kk) {
         if (kk < groups) {
 #pragma unroll
             for (int dn = 0; dn < D / 16; dn += 2) {
@@ -436,31 +440,31 @@ DS4A_DEVINL void compute_tile_dsplit(const uint32_t (&qa)[D / 16][4], const uint
 }
 
 // Walk virtual rows [v_begin, v_end) with the d-split engine (as attend_range).
-template <int D>
+template <int D, int BN = kBN>
 __device__ void attend_range_dsplit(const RowSrc &src, int v_begin, int v_end, const uint32_t (&qa)[D / 16][4],
-                                    bool has_heads, int dh, float scale_log2, Smem<D> &sm, WarpStateH<D> &st,
+                                    bool has_heads, int dh, float scale_log2, Smem<D, BN> &sm, WarpStateH<D> &st,
                                     bool tile0_issued) {
-    const int n_tiles = v_end > v_begin ? (v_end - v_begin + kBN - 1) / kBN : 0;
+    const int n_tiles = v_end > v_begin ? (v_end - v_begin + BN - 1) / BN : 0;
     if (n_tiles == 0) return;
     if (!tile0_issued) {
-        build_table<D>(src, v_begin, v_end, sm.off[0], &sm.nvalid[0]);
+        build_table<D, BN>(src, v_begin, v_end, sm.off[0], &sm.nvalid[0]);
         __syncthreads();
-        issue_loads<D>(src, sm.off[0], sm.k[0], sm.v[0]);
+        issue_loads<D, BN>(src, sm.off[0], sm.k[0], sm.v[0]);
         cp_async_commit();
     }
     for (int it = 0; it < n_tiles; ++it) {
         __syncthreads();
         if (it + 1 < n_tiles) {
             const int b = (it + 1) & 1;
-            build_table<D>(src, v_begin + (it + 1) * kBN, v_end, sm.off[b], &sm.nvalid[b]);
+            build_table<D, BN>(src, v_begin + (it + 1) * BN, v_end, sm.off[b], &sm.nvalid[b]);
             __syncthreads();
-            issue_loads<D>(src, sm.off[b], sm.k[b], sm.v[b]);
+            issue_loads<D, BN>(src, sm.off[b], sm.k[b], sm.v[b]);
         }
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
         const int b = it & 1;
-        if (has_heads) compute_tile_dsplit<D>(qa, sm.k[b], sm.v[b], sm.off[b], sm.nvalid[b], dh, scale_log2, st);
+        if (has_heads) compute_tile_dsplit<D, BN>(qa, sm.k[b], sm.v[b], sm.off[b], sm.nvalid[b], dh, scale_log2, st);
     }
     __syncthreads();
 }
@@ -543,16 +547,20 @@ struct DecodeArgs {
 };
 
 constexpr int kRecvRows = 80;   // >= cluster size * ceil(H / cluster size) for H <= 64
+// one session's fused compressor + attention launch whose CTAs attend kBN+1 .. kBigBN rows
+// each takes them as one tile (a tile costs a fixed part, row table, loads, softmax, far
+// above its per-row work)
+constexpr int kBigBN = 80;
 
-template <int D>
-__host__ __device__ constexpr size_t recv_offset() { return (sizeof(Smem<D>) + 127) / 128 * 128; }
+template <int D, int BN = kBN>
+__host__ __device__ constexpr size_t recv_offset() { return (sizeof(Smem<D, BN>) + 127) / 128 * 128; }
 // One head's split-KV partial as exchanged between the CTAs of a cluster: O as D fp16
 // (its rounding, 2^-11 relative, is far inside the output's fp16), then the running
 // max m and sum l as fp32, padded to a 16-byte multiple for the bulk copies.
 template <int D>
 __host__ __device__ constexpr int part_bytes() { return 2 * D + 16; }
-template <int D>
-constexpr size_t decode_smem() { return recv_offset<D>() + kRecvRows * part_bytes<D>(); }
+template <int D, int BN = kBN>
+constexpr size_t decode_smem() { return recv_offset<D, BN>() + kRecvRows * part_bytes<D>(); }
 template <int D>
 constexpr size_t prefill_smem() { return sizeof(Smem<D>); }
 static_assert(4 * 32 * (128 / 2 + 4) * sizeof(float) <= sizeof(Smem<128>), "exchange fits in the tiles");
@@ -610,11 +618,12 @@ DS4A_DEVINL void merge_heads(const unsigned char *recv, int hpc, int hb, int nh,
 // that attends it, so that CTA writes the row before it attends its rows; other
 // steps update the state after the partials are sent.  No other CTA reads what
 // the compressor writes.
-template <int D, bool kCompress>
-__global__ void __launch_bounds__(kThreads, kCompress ? 1 : 2) attn_decode_kernel(DecodeArgs a, cmp::CompressArgs ca) {
+template <int D, bool kCompress, int BN = kBN>
+__global__ void __launch_bounds__(kThreads, (kCompress || BN != kBN) ? 1 : 2)
+    attn_decode_kernel(DecodeArgs a, cmp::CompressArgs ca) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    Smem<D> &sm = *reinterpret_cast<Smem<D> *>(smem_raw);
-    unsigned char *recv = smem_raw + recv_offset<D>();
+    Smem<D, BN> &sm = *reinterpret_cast<Smem<D, BN> *>(smem_raw);
+    unsigned char *recv = smem_raw + recv_offset<D, BN>();
     constexpr int RB = part_bytes<D>();
     __shared__ __align__(8) uint64_t s_recv_bar;
     cg::cluster_group cluster = cg::this_cluster();
@@ -683,18 +692,18 @@ __global__ void __launch_bounds__(kThreads, kCompress ? 1 : 2) attn_decode_kerne
     if (comp_here) cmp::segment_scores<kThreads>(ca, ca.pos, ca.pos + 1, s_cw);
     // a first tile of window rows only (cache state) is gathered before the dependency wait
     // (not by a CTA that writes a compressed row before it attends)
-    const bool pre = v1 > v0 && min(v1, v0 + kBN) <= a.src.n_w && !(comp_here && a.comp_first);
+    const bool pre = v1 > v0 && min(v1, v0 + BN) <= a.src.n_w && !(comp_here && a.comp_first);
     if (pre) {
-        build_table<D>(a.src, v0, v1, sm.off[0], &sm.nvalid[0]);
+        build_table<D, BN>(a.src, v0, v1, sm.off[0], &sm.nvalid[0]);
         __syncthreads();
-        issue_loads<D>(a.src, sm.off[0], sm.k[0], sm.v[0]);
+        issue_loads<D, BN>(a.src, sm.off[0], sm.k[0], sm.v[0]);
         cp_async_commit();
     }
     if (a.pos == nullptr && threadIdx.x < 4) {
         // one session: warm L2 with the rows this CTA gathers after the dependency wait
         // (window rows past the first tile; compressed rows when every row is attended,
         // since a kept-row list is known only after the wait)
-        const int pv0 = pre ? min(v1, v0 + kBN) : v0;
+        const int pv0 = pre ? min(v1, v0 + BN) : v0;
         const int nw = a.src.n_w;
         if (threadIdx.x < 2) {
             prefetch_rows_l2<D>(threadIdx.x ? a.src.wv : a.src.wk, pv0, min(v1, nw));
@@ -720,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, kCompress ? 1 : 2) attn_decode_kerne
         for (int e = 0; e < 4; ++e) st.o[dn][e] = 0.f;
     st.m[0] = st.m[1] = -INFINITY;
     st.l[0] = st.l[1] = 0.f;
-    attend_range_dsplit<D>(a.src, v0, v1, qa, has_heads, dh, a.scale_log2, sm, st, pre);
+    attend_range_dsplit<D, BN>(a.src, v0, v1, qa, has_heads, dh, a.scale_log2, sm, st, pre);
 #pragma unroll
     for (int r = 0; r < 2; ++r) {   // quad-reduce the per-lane partial sums of l
         st.l[r] += __shfl_xor_sync(0xffffffffu, st.l[r], 1);
@@ -879,6 +888,15 @@ cudaError_t configure(int &cluster, int *active16 = nullptr, int *active8 = null
                 e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          cudaSharedmemCarveoutMaxShared);
         }
+        for (auto kern : {attn_decode_kernel<D, false, kBigBN>, attn_decode_kernel<D, true, kBigBN>}) {
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(decode_smem<D, kBigBN>()));
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
+        }
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(prefill_smem<D>()));
@@ -969,15 +987,20 @@ cudaError_t launch_attn_decode(const uint16_t *q, int H, int D, const uint16_t *
     a.comp_first = 0;
     a.test_wait_ns = test_wait_limit_ns();
     int cluster = 16;
-    cudaError_t e;
-    if (D == 128) {
-        if ((e = configure<128>(cluster)) != cudaSuccess) return e;
-        return launch(attn_decode_kernel<128, false>, dim3(cluster), dim3(kThreads), decode_smem<128>(), c, cluster, a,
-                      cmp::CompressArgs{});
-    }
-    if ((e = configure<64>(cluster)) != cudaSuccess) return e;
-    return launch(attn_decode_kernel<64, false>, dim3(cluster), dim3(kThreads), decode_smem<64>(), c, cluster, a,
-                  cmp::CompressArgs{});
+    cudaError_t e = D == 128 ? configure<128>(cluster) : configure<64>(cluster);
+    if (e != cudaSuccess) return e;
+    // CTAs that attend 65 .. 80 rows take them as one 80-row tile (as the fused launch does)
+    const int chunk = (a.n_rows + cluster - 1) / cluster;
+    const bool big = chunk > kBN && chunk <= kBigBN;
+    if (D == 128)
+        return big ? launch(attn_decode_kernel<128, false, kBigBN>, dim3(cluster), dim3(kThreads),
+                            decode_smem<128, kBigBN>(), c, cluster, a, cmp::CompressArgs{})
+                   : launch(attn_decode_kernel<128, false>, dim3(cluster), dim3(kThreads), decode_smem<128>(), c,
+                            cluster, a, cmp::CompressArgs{});
+    return big ? launch(attn_decode_kernel<64, false, kBigBN>, dim3(cluster), dim3(kThreads), decode_smem<64, kBigBN>(),
+                        c, cluster, a, cmp::CompressArgs{})
+               : launch(attn_decode_kernel<64, false>, dim3(cluster), dim3(kThreads), decode_smem<64>(), c, cluster, a,
+                        cmp::CompressArgs{});
 }
 
 cudaError_t launch_compress_attn_decode(const uint16_t *k_new, const uint16_t *v_new, const float *score_w, int ratio,
@@ -1002,10 +1025,16 @@ cudaError_t launch_compress_attn_decode(const uint16_t *k_new, const uint16_t *v
     // the CTA that attends the last row (the row a completing step writes), as the kernel splits the rows
     const int chunk = (a.n_rows + cluster - 1) / cluster;
     a.comp_rank = (a.n_rows - 1) / chunk;
+    const bool big = chunk > kBN && chunk <= kBigBN;
     if (D == 128)
-        return launch(attn_decode_kernel<128, true>, dim3(cluster), dim3(kThreads), decode_smem<128>(), c, cluster, a,
-                      ca);
-    return launch(attn_decode_kernel<64, true>, dim3(cluster), dim3(kThreads), decode_smem<64>(), c, cluster, a, ca);
+        return big ? launch(attn_decode_kernel<128, true, kBigBN>, dim3(cluster), dim3(kThreads),
+                            decode_smem<128, kBigBN>(), c, cluster, a, ca)
+                   : launch(attn_decode_kernel<128, true>, dim3(cluster), dim3(kThreads), decode_smem<128>(), c,
+                            cluster, a, ca);
+    return big ? launch(attn_decode_kernel<64, true, kBigBN>, dim3(cluster), dim3(kThreads), decode_smem<64, kBigBN>(),
+                        c, cluster, a, ca)
+               : launch(attn_decode_kernel<64, true>, dim3(cluster), dim3(kThreads), decode_smem<64>(), c, cluster, a,
+                        ca);
 }
 
 cudaError_t launch_attn_decode_batched(int B, const uint16_t *q, int H, int D, const uint16_t *ring_k,
@@ -1036,14 +1065,25 @@ cudaError_t launch_attn_decode_batched(int B, const uint16_t *q, int H, int D, c
     cudaError_t e = D == 128 ? configure<128>(cluster, &active16, &active8, &active4)
                              : configure<64>(cluster, &active16, &active8, &active4);
     if (e != cudaSuccess) return e;
-    cluster = batched_cluster(B, W + (sel ? static_cast<long long>(n_sel) : cap), cluster, active16, active8, active4);
+    const long long rows = W + (sel ? static_cast<long long>(n_sel) : cap);   // the largest session's
+    cluster = batched_cluster(B, rows, cluster, active16, active8, active4);
     const dim3 grid(cluster, B);
     if (state != nullptr) {   // the compressor's update for each session's token, in the same launch
         const cmp::CompressArgs ca{nullptr, nullptr, score_w, state, const_cast<uint16_t *>(comp_k),
                                    const_cast<uint16_t *>(comp_v), 0, 1, D, ratio};
+        // one 80-row tile when the largest session's CTAs attend 65 .. 80 rows, as the
+        // one-session launch does (a session that fits 64 rows gets the same bits either way)
+        const long long chunk = (rows + cluster - 1) / cluster;
+        const bool big = chunk > kBN && chunk <= kBigBN;
         if (D == 128)
-            return launch(attn_decode_kernel<128, true>, grid, dim3(kThreads), decode_smem<128>(), c, cluster, a, ca);
-        return launch(attn_decode_kernel<64, true>, grid, dim3(kThreads), decode_smem<64>(), c, cluster, a, ca);
+            return big ? launch(attn_decode_kernel<128, true, kBigBN>, grid, dim3(kThreads),
+                                decode_smem<128, kBigBN>(), c, cluster, a, ca)
+                       : launch(attn_decode_kernel<128, true>, grid, dim3(kThreads), decode_smem<128>(), c, cluster,
+                                a, ca);
+        return big ? launch(attn_decode_kernel<64, true, kBigBN>, grid, dim3(kThreads), decode_smem<64, kBigBN>(), c,
+                            cluster, a, ca)
+                   : launch(attn_decode_kernel<64, true>, grid, dim3(kThreads), decode_smem<64>(), c, cluster, a,
+                            ca);
     }
     if (D == 128)
         return launch(attn_decode_kernel<128, false>, grid, dim3(kThreads), decode_smem<128>(), c, cluster, a,

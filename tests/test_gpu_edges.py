@@ -115,10 +115,13 @@ def test_compressor_degenerate_ratios(ratio, D, n):
 
 
 @pytest.mark.parametrize("ratio,topk,window,p", [(1, 0, 128, 300), (4, 2048, 128, 40000), (4, 512, 4096, 20000),
-                                                 (128, 0, 4096, 9000), (0, 0, 4096, 6000), (4, 512, 1, 5000)])
+                                                 (128, 0, 4096, 9000), (0, 0, 4096, 6000), (4, 512, 1, 5000),
+                                                 (128, 0, 128, 114815), (128, 0, 128, 147500)])
 def test_decode_extreme_shapes(ratio, topk, window, p):
     """A decode step with ratio 1 (every token a row), the largest k (2048), the
-    largest window (4096 rows: up to 288 rows a CTA) and a one-row window."""
+    largest window (4096 rows: up to 288 rows a CTA) and a one-row window; and a
+    ratio-128 layer whose CTAs attend 65 rows each (a step that completes a row) and
+    80 rows each, the bounds of the fused launch's one-tile form."""
     inst = synth.decode_instance(seed=21, layer=2, H=64, D=128, window=window, ratio=ratio, d_idx=128, topk=topk,
                                  p=p, sigma_w=configs.SIGMA_W)
     L = DecodeLayer(inst)
