@@ -527,7 +527,7 @@ struct DecodeArgs {
     int H;
     int n_rows;        // n_win + n_sel
     float scale_log2;
-    int comp_rank;     // with the compressor: the CTA that runs its update (it attends the row it may write)
+    int comp_rank;     // with the compressor: the CTA that runs its update (the last row's CTA on a completing step, else 0)
     int comp_first;    // the update completes a block: its row is written before that CTA attends
     long long test_wait_ns;   // > 0 (test hook only): CTA 0 also waits this long on a barrier nobody completes
     // Batched decode: cluster blockIdx.y serves session s, whose inputs sit at fixed
@@ -615,9 +615,11 @@ DS4A_DEVINL void merge_heads(const unsigned char *recv, int hpc, int hb, int nh,
 // token (n_new = 1, arguments ca): its score before the dependency wait; the
 // running state and, when the token completes a block, the pooled row after it.
 // A completed row is the last row this call attends and a.comp_rank is the CTA
-// that attends it, so that CTA writes the row before it attends its rows; other
-// steps update the state after the partials are sent.  No other CTA reads what
-// the compressor writes.
+// that attends it, so that CTA writes the row before it attends its rows.  On the
+// other steps CTA 0 updates the state after its partials are sent: its first tile
+// (window rows) is gathered before the wait, so it finishes its tiles first and the
+// update overlaps the other CTAs' tiles.  No other CTA reads what the compressor
+// writes.
 template <int D, bool kCompress, int BN = kBN>
 __global__ void __launch_bounds__(kThreads, (kCompress || BN != kBN) ? 1 : 2)
     attn_decode_kernel(DecodeArgs a, cmp::CompressArgs ca) {
@@ -656,8 +658,8 @@ __global__ void __launch_bounds__(kThreads, (kCompress || BN != kBN) ? 1 : 2)
             ca.comp_k += sid * a.comp_stride;
             ca.comp_v += sid * a.comp_stride;
             const int chunk = (a.n_rows + cs - 1) / cs;
-            a.comp_rank = (a.n_rows - 1) / chunk;
             a.comp_first = (p + 1) % a.ratio == 0;
+            a.comp_rank = a.comp_first ? (a.n_rows - 1) / chunk : 0;
             if ((p + 1) / a.ratio > a.cap) {
                 // the row this token completes is past the session's capacity: no update
                 a.comp_rank = -1;
@@ -1024,7 +1026,7 @@ cudaError_t launch_compress_attn_decode(const uint16_t *k_new, const uint16_t *v
     if (e != cudaSuccess) return e;
     // the CTA that attends the last row (the row a completing step writes), as the kernel splits the rows
     const int chunk = (a.n_rows + cluster - 1) / cluster;
-    a.comp_rank = (a.n_rows - 1) / chunk;
+    a.comp_rank = a.comp_first ? (a.n_rows - 1) / chunk : 0;
     const bool big = chunk > kBN && chunk <= kBigBN;
     if (D == 128)
         return big ? launch(attn_decode_kernel<128, true, kBigBN>, dim3(cluster), dim3(kThreads),
