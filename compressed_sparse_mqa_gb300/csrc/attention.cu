@@ -7,7 +7,7 @@
 //
 // Tile engine (shared by decode and prefill).  A CTA of 8 warps walks a list of
 // "virtual rows" (window rows first, then compressed rows through `sel`) in
-// tiles of 64.  Each tile's K and V rows are gathered with 16-byte cp.async into
+// tiles of 64 (80 in some decode launches, below).  Each tile's K and V rows are gathered with 16-byte cp.async into
 // a double-buffered, XOR-swizzled shared-memory tile.  Warp w owns heads
 // 16(w%4) .. 16(w%4)+15 (the 64 heads of one query are the M dimension: they
 // all share each K/V row, 64 flop per byte) and keys 32(w/4) .. +31 of each
@@ -680,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, (kCompress || BN != kBN) ? 1 : 2)
                      "r"(static_cast<uint32_t>(cs * nh * RB))
                      : "memory");
     }
-    // this CTA is running and its receive barrier is armed; waited on before the first remote store
+    // this CTA is running and its receive barrier is armed; waited on before the first copy is sent
     cluster_arrive_release();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
