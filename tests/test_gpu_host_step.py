@@ -57,6 +57,8 @@ CASES = [
     (64, 128, 128, 4, 128, 512, False, 4000, 20, True),      # model-sized indexer layer
     (8, 64, 32, 4, 32, 16, False, 200, 30, False),           # indexer layer, pageable buffers
     (8, 64, 32, 128, 32, 0, False, 1000, 30, False),         # ratio-128 layer, pageable buffers
+    (64, 128, 128, 128, 128, 0, False, 131060, 16, True),    # model-sized ratio-128 layer: 72 rows a CTA (one
+                                                             # 80-row tile); completes row 1023 at 131071
 ]
 
 
