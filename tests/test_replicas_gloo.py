@@ -59,3 +59,18 @@ def test_single_process_needs_no_process_group():
     import bench
     assert bench.job_throughput(5.0, 100, 1) == (5.0, 100 / 0.005)
     bench.barrier(1)   # no-op without a process group
+
+
+@pytest.mark.timeout(300)
+def test_reference_arm_times_exactly_the_requested_rounds():
+    """bench.py --impl reference on rank 0: W untimed and exactly K timed rounds of one
+    oracle C2 step per usable core; the line reports K and W and a positive rate."""
+    import argparse
+    import bench
+    line = bench.run_reference(argparse.Namespace(steps=2, warmup=1), 0, 1)
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 1
+    cores = line["cpu_baseline"]["cores"]
+    assert cores == bench.cpu_cores() >= 1
+    assert line["value"] > 0 and line["e2e"]["value"] == line["value"]
+    assert f"{2 * cores} steps" in line["cpu_baseline"]["sample"]
+    assert line["ms_per_step"] > 0 and line["dtype"] == "f64"
