@@ -724,9 +724,13 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_decode_kernel(IndexerArgs
             if (threadIdx.x == 0) u.band.eps = ldexpf(__uint_as_float(__ldcg(bmax_word)) * 1.01f, -12) + 1e-30f;
             __syncthreads();
             const float eps = u.band.eps;
-            if (n <= kThreads * 8) band_select_regs<8>(a, keys, n, eps, u.band);
-            else if (n <= kThreads * 16) band_select_regs<16>(a, keys, n, eps, u.band);
-            else band_select_regs<kMaxItems>(a, keys, n, eps, u.band);
+            if constexpr (kSelItems != 0) {
+                band_select_regs<kSelItems>(a, keys, n, eps, u.band);
+            } else {
+                if (n <= kThreads * 8) band_select_regs<8>(a, keys, n, eps, u.band);
+                else if (n <= kThreads * 16) band_select_regs<16>(a, keys, n, eps, u.band);
+                else band_select_regs<kMaxItems>(a, keys, n, eps, u.band);
+            }
         }
         if (threadIdx.x == 0) *bmax_word = 0u;
     } else {
@@ -812,6 +816,16 @@ static auto decode_kernel_for(long long n_vis) {
     }
 }
 
+// a batched approximate-score launch with the band select its sessions' capacity needs
+template <bool kFold>
+static auto approx_kernel_for(long long cap) {
+    switch (sel_items_for(cap)) {
+        case 8: return indexer_decode_kernel<true, 4, true, kFold, 8>;
+        case 16: return indexer_decode_kernel<true, 4, true, kFold, 16>;
+        default: return indexer_decode_kernel<true, 4, true, kFold, kMaxItems>;
+    }
+}
+
 cudaError_t launch_indexer(const uint16_t *q_idx, int n_q, const uint16_t *k_idx, long long n_rows,
                            int d_idx, long long q_pos0, int ratio, int k, int32_t *out_idx,
                            int32_t *out_n, void *ws, const Ctx &c) {
@@ -889,10 +903,10 @@ cudaError_t launch_indexer_compress_batched(int B, const uint16_t *q_idx, const 
     // exact scores otherwise, one 64-row batch per round when a CTA covers two at most
     if (cap <= kBandMaxRows && rows_per_cta >= 512) {
         if (fold)
-            return launch(indexer_decode_kernel<true, 4, true, true>, dim3(grid + 1, B), dim3(kThreads),
-                          kApproxDynBytes, c, 1, a, rows_per_cta, ca, bt);
-        return launch(indexer_decode_kernel<true, 4, true, false>, dim3(grid + 1, B), dim3(kThreads), kApproxDynBytes,
-                      c, 1, a, rows_per_cta, ca, bt);
+            return launch(approx_kernel_for<true>(cap), dim3(grid + 1, B), dim3(kThreads), kApproxDynBytes, c, 1, a,
+                          rows_per_cta, ca, bt);
+        return launch(approx_kernel_for<false>(cap), dim3(grid + 1, B), dim3(kThreads), kApproxDynBytes, c, 1, a,
+                      rows_per_cta, ca, bt);
     }
     if (rows_per_cta <= 2 * kRowsPerCta)
         return launch(indexer_decode_kernel<true, 1, false, false>, dim3(grid + 1, B), dim3(kThreads), 0, c, 1, a,
@@ -920,13 +934,15 @@ static cudaError_t configure_indexer(const Ctx &c) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(indexer_decode_kernel<true, 1, false, false>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
-        for (auto kern : {indexer_decode_kernel<true, 4, true, false>, indexer_decode_kernel<true, 4, true, true>}) {
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         cudaSharedmemCarveoutMaxShared);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kApproxDynBytes));
+        for (long long cap : {1LL * kThreads * 8, 1LL * kThreads * 16, 1LL * kThreads * kMaxItems}) {
+            for (auto kern : {approx_kernel_for<false>(cap), approx_kernel_for<true>(cap)}) {
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared);
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kApproxDynBytes));
+            }
         }
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(indexer_decode_kernel<true, 4, false, false>,
