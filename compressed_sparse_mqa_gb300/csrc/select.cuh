@@ -300,6 +300,11 @@ __device__ void band_select(uint32_t (&key)[ITEMS], int n, int k, float eps, con
     const float ulp = ldexpf(1.f, ilogbf(big > 0.f ? big : 1.f) - 23);
     const float margin = 2.f * eps + 4.f * ulp;
     const float in_thr = t_hi + margin, out_thr = t_lo - margin;
+    // the same two tests on the order-preserving keys: s > in_thr <=> key > key(in_thr) and
+    // s >= out_thr <=> key >= key(out_thr), a zero threshold taken as +0 and -0 respectively
+    // (-0 and +0 are equal scores but distinct keys)
+    const uint32_t in_key = float_key(in_thr == 0.f ? 0.f : in_thr);
+    const uint32_t out_key = float_key(out_thr == 0.f ? -0.f : out_thr);
 
     // classify: certainly in, certainly out, or band (rescored exactly)
     if (tid == 0) {
@@ -313,11 +318,10 @@ __device__ void band_select(uint32_t (&key)[ITEMS], int n, int k, float eps, con
     for (int it = 0; it < ITEMS; ++it) {
         const int j = it * NT + tid;
         if (j < n) {
-            const float s = key_to_float(key[it]);
-            if (s > in_thr) {
+            if (key[it] > in_key) {
                 flags |= 1u << it;
                 ++my_in;
-            } else if (s >= out_thr) {
+            } else if (key[it] >= out_key) {
                 const uint32_t b = atomicAdd(&sm.band_n, 1u);
                 if (b < kBandCap) sm.band_idx[b] = j;
             }
